@@ -189,3 +189,74 @@ def fused_inputs(T: int, heads: int, head_dim: int, num_slots: int, seed: int, s
         "out_gate": f32_to_bf16_bits(normal_f32(seed, Tag.OUT_GATE, step, (T, heads, head_dim), 1.0, layer)),
         "norm_w": np.ones(head_dim, dtype=np.float32),
     }
+
+
+# ------------------------------------------------------------------------------------------------
+# device twin (gdn_synth/csrc/synth.cu): fills CUDA tensors with the same values, bit for bit
+# ------------------------------------------------------------------------------------------------
+import ctypes as _ct
+import os as _os
+import subprocess as _sp
+import threading as _th
+
+_HERE = _os.path.dirname(_os.path.abspath(__file__))
+_SYNTH_SRC = _os.path.join(_HERE, "csrc", "synth.cu")
+_SYNTH_LIB = _os.path.join(_HERE, "_lib", "libgdn_synth.so")
+_synth_lock = _th.Lock()
+_synth = None
+
+
+def build_device(force: bool = False) -> str:
+    """Compile synth.cu for sm_103a into gdn_synth/_lib/libgdn_synth.so (nvcc)."""
+    _os.makedirs(_os.path.dirname(_SYNTH_LIB), exist_ok=True)
+    if (not force and _os.path.exists(_SYNTH_LIB)
+            and _os.path.getmtime(_SYNTH_LIB) >= _os.path.getmtime(_SYNTH_SRC)):
+        return _SYNTH_LIB
+    tmp = f"{_SYNTH_LIB}.{_os.getpid()}.tmp"
+    _sp.run(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17",
+             "-Xcompiler", "-fPIC", "-shared", "-o", tmp, _SYNTH_SRC], check=True)
+    _os.replace(tmp, _SYNTH_LIB)
+    return _SYNTH_LIB
+
+
+def _device_lib():
+    global _synth
+    with _synth_lock:
+        if _synth is None:
+            L = _ct.CDLL(build_device())
+            L.synth_fill_normal.restype = _ct.c_int
+            L.synth_fill_normal.argtypes = [_ct.c_void_p, _ct.c_int64, _ct.c_uint64, _ct.c_uint32,
+                                            _ct.c_uint32, _ct.c_uint32, _ct.c_void_p, _ct.c_int64,
+                                            _ct.c_float, _ct.c_int, _ct.c_void_p]
+            L.synth_add_i32.restype = _ct.c_int
+            L.synth_add_i32.argtypes = [_ct.c_void_p, _ct.c_int32, _ct.c_void_p]
+            _synth = L
+    return _synth
+
+
+def fill_normal_(t, seed: int, tag: int, step: int, std: float, layer: int = 0, start: int = 0,
+                 step_ptr=None, stream=None):
+    """Fill a contiguous CUDA tensor (float32 or bfloat16) in place with the normals that
+    normal_f32(seed, tag, step, t.shape, std, layer, start) gives on the host (bf16: rounded to
+    nearest even). With step_ptr (a CUDA int32 tensor of one element) the step is
+    step + step_ptr[0], read on the device."""
+    import torch
+    if not t.is_cuda or not t.is_contiguous() or t.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("fill_normal_ needs a contiguous CUDA float32 or bfloat16 tensor")
+    s = torch.cuda.current_stream(t.device).cuda_stream if stream is None else stream
+    rc = _device_lib().synth_fill_normal(
+        t.data_ptr(), t.numel(), seed & 0xFFFFFFFFFFFFFFFF, tag, layer, step,
+        None if step_ptr is None else step_ptr.data_ptr(), start, float(scale_constant(std)),
+        int(t.dtype == torch.bfloat16), s)
+    if rc != 0:
+        raise RuntimeError(f"synth_fill_normal failed with CUDA error {rc}")
+    return t
+
+
+def add_i32_(p, d: int, stream=None):
+    """p[0] += d on the device (p: CUDA int32 tensor)."""
+    import torch
+    s = torch.cuda.current_stream(p.device).cuda_stream if stream is None else stream
+    rc = _device_lib().synth_add_i32(p.data_ptr(), int(d), s)
+    if rc != 0:
+        raise RuntimeError(f"synth_add_i32 failed with CUDA error {rc}")

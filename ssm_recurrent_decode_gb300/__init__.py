@@ -1,0 +1,351 @@
+"""Python binding of libgdn_decode.so, the GB300 (sm_103a) single-token gated delta-rule decode.
+
+Argument marshalling only: every function here takes torch tensors that already live on the GPU,
+passes their device pointers, sizes and strides through the C ABI declared in
+``include/gdn_decode.h``, and launches on the current torch stream. Every step of the decode runs
+in the library's CUDA kernels; there is no Python, PyTorch or CPU fallback, and a missing or
+unbuildable library raises.
+
+Entry points (same names as the C ABI):
+  gdn_decode_step          row b on state slot b
+  gdn_decode_step_indexed  row b on state slot cache_indices[b] (the packed decode over a pool)
+  gdn_decode_buffered      output-only decode that writes the state back once every L steps
+  gdn_decode_fused         conv1d update -> delta step (per-key or per-head decay) -> gated RMSNorm
+plus ``fused_recurrent_gated_delta_rule_packed_decode``, the packed call with the keyword names
+of "Microbenchmark: buffered output-only GDN decode (ReplaySSM Part A)" (_bench_cfg, run_packed).
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+
+from . import _build
+
+__all__ = [
+    "lib", "build", "GdnError", "GdnStepArgs", "GdnRingArgs", "GdnFusedArgs",
+    "gdn_decode_step", "gdn_decode_step_indexed", "gdn_decode_buffered", "gdn_decode_fused",
+    "gdn_strerror", "split_mixed_qkv", "fused_recurrent_gated_delta_rule_packed_decode",
+    "GDN_F32", "GDN_BF16", "GDN_DEVERR_BAD_INDEX", "GDN_DEVERR_BAD_WRITE_POS", "EXPORTS",
+]
+
+GDN_F32, GDN_BF16 = 0, 1
+GDN_GATE_RAW, GDN_GATE_DIRECT = 0, 1
+GDN_FUSED_GATE_KDA, GDN_FUSED_GATE_GDN = 0, 1
+GDN_ACT_SILU, GDN_ACT_SIGMOID = 0, 1
+GDN_DEVERR_BAD_INDEX, GDN_DEVERR_BAD_WRITE_POS = 0x1, 0x2
+ABI_VERSION = 1
+
+# every function the header declares
+EXPORTS = ("gdn_decode_step", "gdn_decode_step_indexed", "gdn_decode_buffered", "gdn_decode_fused",
+           "gdn_strerror", "gdn_abi_struct_size", "gdn_abi_version")
+
+_i32, _i64, _f32, _vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
+
+
+class GdnStepArgs(ctypes.Structure):
+    _fields_ = [("B", _i32), ("H", _i32), ("HV", _i32), ("K", _i32), ("V", _i32),
+                ("num_slots", _i32), ("in_dtype", _i32), ("out_dtype", _i32),
+                ("q", _vp), ("k", _vp), ("v", _vp),
+                ("q_stride", _i64), ("k_stride", _i64), ("v_stride", _i64),
+                ("gate_mode", _i32), ("a", _vp), ("b", _vp), ("A_log", _vp), ("dt_bias", _vp),
+                ("g", _vp), ("beta", _vp), ("scale", _f32), ("use_qk_l2norm", _i32),
+                ("state", _vp), ("out", _vp), ("err_flags", _vp)]
+
+
+class GdnRingArgs(ctypes.Structure):
+    _fields_ = [("L", _i32), ("ring_dtype", _i32), ("d_cache", _vp), ("k_cache", _vp),
+                ("g_cache", _vp), ("write_pos", _vp)]
+
+
+class GdnFusedArgs(ctypes.Structure):
+    _fields_ = [("T", _i32), ("heads", _i32), ("head_dim", _i32), ("num_slots", _i32),
+                ("x", _vp), ("x_stride", _i64), ("conv_w", _vp), ("conv_b", _vp),
+                ("conv_state", _vp), ("cs_stride_slot", _i64), ("cs_stride_chan", _i64),
+                ("cs_stride_tap", _i64), ("gate_kind", _i32), ("kda_gate_form", _i32),
+                ("raw_g", _vp), ("raw_beta", _vp), ("A_log", _vp), ("dt_bias", _vp),
+                ("lower_bound", _f32), ("scale", _f32), ("use_qk_l2norm", _i32),
+                ("state", _vp), ("state_indices", _vp), ("pad_slot_id", _i32),
+                ("out_gate", _vp), ("norm_w", _vp), ("norm_eps", _f32), ("gate_act", _i32),
+                ("out", _vp), ("err_flags", _vp)]
+
+
+class GdnError(RuntimeError):
+    """A non-zero status from the library (the message is gdn_strerror's)."""
+
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn}: {gdn_strerror(status)} (status {status})")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile libgdn_decode.so in-tree (nvcc, sm_103a); returns its path."""
+    return _build.build(force=force)
+
+
+def lib():
+    """The loaded library (built first if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build()
+            L = ctypes.CDLL(path)
+            for name in ("gdn_decode_step",):
+                getattr(L, name).argtypes = [ctypes.POINTER(GdnStepArgs), _vp]
+            L.gdn_decode_step_indexed.argtypes = [ctypes.POINTER(GdnStepArgs), _vp, _i32, _vp]
+            L.gdn_decode_buffered.argtypes = [ctypes.POINTER(GdnStepArgs), _vp, _i32,
+                                              ctypes.POINTER(GdnRingArgs), _vp]
+            L.gdn_decode_fused.argtypes = [ctypes.POINTER(GdnFusedArgs), _vp]
+            for name in ("gdn_decode_step", "gdn_decode_step_indexed", "gdn_decode_buffered",
+                         "gdn_decode_fused", "gdn_abi_version"):
+                getattr(L, name).restype = ctypes.c_int
+            L.gdn_strerror.argtypes = [ctypes.c_int]
+            L.gdn_strerror.restype = ctypes.c_char_p
+            L.gdn_abi_struct_size.argtypes = [ctypes.c_int]
+            L.gdn_abi_struct_size.restype = ctypes.c_size_t
+            sizes = [L.gdn_abi_struct_size(i) for i in range(3)]
+            want = [ctypes.sizeof(GdnStepArgs), ctypes.sizeof(GdnRingArgs), ctypes.sizeof(GdnFusedArgs)]
+            if sizes != want or L.gdn_abi_version() != ABI_VERSION:
+                raise RuntimeError(f"libgdn_decode.so ABI mismatch: struct sizes {sizes} vs {want}")
+            _lib = L
+    return _lib
+
+
+def gdn_strerror(status: int) -> str:
+    return lib().gdn_strerror(int(status)).decode()
+
+
+# ------------------------------------------------------------------------------------------------
+# marshalling helpers
+# ------------------------------------------------------------------------------------------------
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return GDN_F32
+    if t.dtype == torch.bfloat16:
+        return GDN_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}: float32 or bfloat16")
+
+
+def _ptr(t, name: str, dtype=None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor (this library has no CPU path)")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _dense(t, name: str):
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _rows(t, name: str, width: int):
+    """A [B, width] or [B, heads, dim] view whose rows are dense: returns the row stride."""
+    if t.dim() == 3:
+        if t.stride(2) != 1 or t.stride(1) != t.shape[2] or t.shape[1] * t.shape[2] != width:
+            raise ValueError(f"{name}: rows must be dense [heads, dim] of width {width}")
+    elif t.dim() == 2:
+        if t.stride(1) != 1 or t.shape[1] != width:
+            raise ValueError(f"{name}: expected [B, {width}] with unit inner stride")
+    else:
+        raise ValueError(f"{name}: expected a 2-D or 3-D tensor")
+    return t.stride(0)
+
+
+def _stream(stream):
+    if stream is None:
+        return _torch().cuda.current_stream().cuda_stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+def split_mixed_qkv(mixed_qkv, H: int, HV: int, K: int, V: int):
+    """Views q [B, H*K], k [B, H*K], v [B, HV*V] of a packed row [q | k | v] (no copy)."""
+    hk = H * K
+    return mixed_qkv[:, :hk], mixed_qkv[:, hk:2 * hk], mixed_qkv[:, 2 * hk:2 * hk + HV * V]
+
+
+def _step_args(q, k, v, state, out, *, H, a, b, A_log, dt_bias, g, beta, scale, use_qk_l2norm,
+               err_flags) -> GdnStepArgs:
+    torch = _torch()
+    if state.dim() != 4:
+        raise ValueError("state must be [num_slots, HV, V, K]")
+    _dense(state, "state")
+    num_slots, HV, V, K = state.shape
+    B = q.shape[0]
+    if H is None:
+        H = (q.shape[1] if q.dim() == 3 else q.shape[1] // K)
+    _dense(out, "out")
+    if out.numel() != B * HV * V:
+        raise ValueError(f"out must hold B*HV*V = {B * HV * V} elements")
+    s = GdnStepArgs()
+    s.B, s.H, s.HV, s.K, s.V, s.num_slots = B, H, HV, K, V, num_slots
+    s.in_dtype, s.out_dtype = _dtype_code(q), _dtype_code(out)
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k and v must share one dtype")
+    s.q, s.k, s.v = _ptr(q, "q"), _ptr(k, "k"), _ptr(v, "v")
+    s.q_stride, s.k_stride, s.v_stride = _rows(q, "q", H * K), _rows(k, "k", H * K), _rows(v, "v", HV * V)
+    if g is not None or beta is not None:
+        s.gate_mode = GDN_GATE_DIRECT
+        s.g = _ptr(_dense(g, "g"), "g", torch.float32)
+        s.beta = _ptr(_dense(beta, "beta"), "beta", torch.float32)
+    else:
+        s.gate_mode = GDN_GATE_RAW
+        for t, n in ((a, "a"), (b, "b")):
+            if t is None or t.dtype != q.dtype:
+                raise TypeError(f"{n} must be given with the dtype of q")
+        s.a, s.b = _ptr(_dense(a, "a"), "a"), _ptr(_dense(b, "b"), "b")
+        s.A_log = _ptr(_dense(A_log, "A_log"), "A_log", torch.float32)
+        s.dt_bias = _ptr(_dense(dt_bias, "dt_bias"), "dt_bias", torch.float32)
+    s.scale = 0.0 if scale is None else float(scale)
+    s.use_qk_l2norm = int(bool(use_qk_l2norm))
+    s.state = _ptr(state, "state", torch.float32)
+    s.out = _ptr(out, "out")
+    s.err_flags = _ptr(err_flags, "err_flags", torch.int32)
+    return s
+
+
+def _check(fn: str, rc: int):
+    if rc != 0:
+        raise GdnError(fn, rc)
+
+
+# ------------------------------------------------------------------------------------------------
+# entry points
+# ------------------------------------------------------------------------------------------------
+def gdn_decode_step(q, k, v, state, out, *, H=None, a=None, b=None, A_log=None, dt_bias=None,
+                    g=None, beta=None, scale=None, use_qk_l2norm=True, err_flags=None, stream=None):
+    """One decode step, row b on slot b. q, k: [B, H*K] (or [B, H, K]) row views; v: [B, HV*V];
+    gates either raw (a, b [B, HV] in the dtype of q; A_log, dt_bias [HV] fp32) or direct
+    (g, beta [B, HV] fp32); state [num_slots, HV, V, K] fp32 updated in place; out [B, HV, V]
+    (or [B, 1, HV, V]) fp32 or bf16."""
+    s = _step_args(q, k, v, state, out, H=H, a=a, b=b, A_log=A_log, dt_bias=dt_bias, g=g,
+                   beta=beta, scale=scale, use_qk_l2norm=use_qk_l2norm, err_flags=err_flags)
+    _check("gdn_decode_step", lib().gdn_decode_step(ctypes.byref(s), _stream(stream)))
+    return out
+
+
+def gdn_decode_step_indexed(q, k, v, state, out, cache_indices, *, pad_slot_id=-1, H=None, a=None,
+                            b=None, A_log=None, dt_bias=None, g=None, beta=None, scale=None,
+                            use_qk_l2norm=True, err_flags=None, stream=None):
+    """As gdn_decode_step, with row b on slot cache_indices[b] (int32 [B] on the device); rows
+    whose index is pad_slot_id are skipped (state untouched, out zeroed)."""
+    torch = _torch()
+    s = _step_args(q, k, v, state, out, H=H, a=a, b=b, A_log=A_log, dt_bias=dt_bias, g=g,
+                   beta=beta, scale=scale, use_qk_l2norm=use_qk_l2norm, err_flags=err_flags)
+    idx = _ptr(_dense(cache_indices, "cache_indices"), "cache_indices", torch.int32)
+    _check("gdn_decode_step_indexed",
+           lib().gdn_decode_step_indexed(ctypes.byref(s), idx, int(pad_slot_id), _stream(stream)))
+    return out
+
+
+def gdn_decode_buffered(q, k, v, state, out, d_cache, k_cache, g_cache, write_pos, *,
+                        cache_indices=None, pad_slot_id=-1, H=None, a=None, b=None, A_log=None,
+                        dt_bias=None, g=None, beta=None, scale=None, use_qk_l2norm=True,
+                        err_flags=None, stream=None):
+    """Buffered output-only decode. state holds the checkpoints; d_cache [num_slots, HV, L, V],
+    k_cache [num_slots, H, L, K] (both fp32 or both bf16), g_cache [num_slots, HV, L] fp32;
+    write_pos int32 [B] is read, never advanced (the caller moves it to (p+1) % L)."""
+    torch = _torch()
+    s = _step_args(q, k, v, state, out, H=H, a=a, b=b, A_log=A_log, dt_bias=dt_bias, g=g,
+                   beta=beta, scale=scale, use_qk_l2norm=use_qk_l2norm, err_flags=err_flags)
+    r = GdnRingArgs()
+    r.L = d_cache.shape[2]
+    if k_cache.dtype != d_cache.dtype:
+        raise TypeError("d_cache and k_cache must share one dtype")
+    r.ring_dtype = _dtype_code(d_cache)
+    expect = {"d_cache": (s.num_slots, s.HV, r.L, s.V), "k_cache": (s.num_slots, s.H, r.L, s.K),
+              "g_cache": (s.num_slots, s.HV, r.L)}
+    for name, t in (("d_cache", d_cache), ("k_cache", k_cache), ("g_cache", g_cache)):
+        if tuple(t.shape) != expect[name]:
+            raise ValueError(f"{name} must be {expect[name]}, got {tuple(t.shape)}")
+        _dense(t, name)
+    r.d_cache, r.k_cache = _ptr(d_cache, "d_cache"), _ptr(k_cache, "k_cache")
+    r.g_cache = _ptr(g_cache, "g_cache", torch.float32)
+    r.write_pos = _ptr(_dense(write_pos, "write_pos"), "write_pos", torch.int32)
+    idx = None if cache_indices is None else _ptr(_dense(cache_indices, "cache_indices"),
+                                                  "cache_indices", torch.int32)
+    _check("gdn_decode_buffered",
+           lib().gdn_decode_buffered(ctypes.byref(s), idx, int(pad_slot_id), ctypes.byref(r),
+                                     _stream(stream)))
+    return out
+
+
+def gdn_decode_fused(x, conv_w, conv_state, raw_g, raw_beta, A_log, dt_bias, state, state_indices,
+                     out_gate, norm_w, out, *, conv_b=None, pad_slot_id=0, gate_kind="kda",
+                     kda_gate_form=0, lower_bound=-5.0, scale=None, use_qk_l2norm=True,
+                     norm_eps=1e-5, gate_act="silu", err_flags=None, stream=None):
+    """Fused decode: conv update -> delta step -> gated RMSNorm, one launch.
+    x bf16 [T, 3*dim]; conv_w fp32 [3*dim, 4]; conv_state bf16 with logical shape
+    [num_slots, 3*dim, 3] (any strides: the "DS" layout is the plain tensor, the "SD" layout a
+    transposed view of [num_slots, 3, 3*dim]); raw_g bf16 [T, heads, D] (kda) or [T, heads] (gdn);
+    raw_beta bf16 [T, heads]; A_log fp32 [heads]; dt_bias fp32 [heads*D] (kda) or [heads] (gdn);
+    state fp32 [num_slots, heads, D, D]; state_indices int32 [T]; out_gate bf16 [T, heads, D];
+    norm_w fp32 [D]; out bf16 [T, heads, D]."""
+    torch = _torch()
+    _dense(state, "state")
+    num_slots, heads, D, _ = state.shape
+    T = x.shape[0]
+    f = GdnFusedArgs()
+    f.T, f.heads, f.head_dim, f.num_slots = T, heads, D, num_slots
+    if x.stride(1) != 1:
+        raise ValueError("x must have unit inner stride")
+    f.x, f.x_stride = _ptr(x, "x", torch.bfloat16), x.stride(0)
+    f.conv_w = _ptr(_dense(conv_w, "conv_w"), "conv_w", torch.float32)
+    f.conv_b = _ptr(conv_b, "conv_b", torch.float32)
+    if tuple(conv_state.shape) != (num_slots, 3 * heads * D, 3):
+        raise ValueError("conv_state must have logical shape [num_slots, 3*dim, 3]")
+    f.conv_state = _ptr(conv_state, "conv_state", torch.bfloat16)
+    f.cs_stride_slot, f.cs_stride_chan, f.cs_stride_tap = conv_state.stride()
+    f.gate_kind = {"kda": GDN_FUSED_GATE_KDA, "gdn": GDN_FUSED_GATE_GDN}[gate_kind]
+    f.kda_gate_form = int(kda_gate_form)
+    f.raw_g = _ptr(_dense(raw_g, "raw_g"), "raw_g", torch.bfloat16)
+    f.raw_beta = _ptr(_dense(raw_beta, "raw_beta"), "raw_beta", torch.bfloat16)
+    f.A_log = _ptr(_dense(A_log, "A_log"), "A_log", torch.float32)
+    f.dt_bias = _ptr(_dense(dt_bias, "dt_bias"), "dt_bias", torch.float32)
+    f.lower_bound = float(lower_bound)
+    f.scale = 0.0 if scale is None else float(scale)
+    f.use_qk_l2norm = int(bool(use_qk_l2norm))
+    f.state = _ptr(state, "state", torch.float32)
+    f.state_indices = _ptr(_dense(state_indices, "state_indices"), "state_indices", torch.int32)
+    f.pad_slot_id = int(pad_slot_id)
+    f.out_gate = _ptr(_dense(out_gate, "out_gate"), "out_gate", torch.bfloat16)
+    f.norm_w = _ptr(_dense(norm_w, "norm_w"), "norm_w", torch.float32)
+    f.norm_eps = float(norm_eps)
+    f.gate_act = {"silu": GDN_ACT_SILU, "sigmoid": GDN_ACT_SIGMOID}[gate_act]
+    f.out = _ptr(_dense(out, "out"), "out", torch.bfloat16)
+    f.err_flags = _ptr(err_flags, "err_flags", torch.int32)
+    _check("gdn_decode_fused", lib().gdn_decode_fused(ctypes.byref(f), _stream(stream)))
+    return out
+
+
+def fused_recurrent_gated_delta_rule_packed_decode(mixed_qkv, a, b, A_log, dt_bias, scale,
+                                                   initial_state, out, ssm_state_indices,
+                                                   use_qk_l2norm_in_kernel=True, pad_slot_id=-1,
+                                                   err_flags=None, stream=None):
+    """The packed decode with the keyword names of the sglang microbenchmark's run_packed:
+    mixed_qkv [B, 2*H*K + HV*V], a, b [B, HV], A_log, dt_bias [HV], initial_state
+    [num_slots, HV, V, K] fp32 (updated in place), out [B, 1, HV, V], ssm_state_indices int32 [B].
+    H is recovered from the row width."""
+    _, HV, V, K = initial_state.shape
+    width = mixed_qkv.shape[1]
+    if (width - HV * V) <= 0 or (width - HV * V) % (2 * K):
+        raise ValueError("mixed_qkv width does not match 2*H*K + HV*V")
+    H = (width - HV * V) // (2 * K)
+    q, k, v = split_mixed_qkv(mixed_qkv, H, HV, K, V)
+    return gdn_decode_step_indexed(q, k, v, initial_state, out, ssm_state_indices,
+                                   pad_slot_id=pad_slot_id, H=H, a=a, b=b, A_log=A_log,
+                                   dt_bias=dt_bias, scale=scale,
+                                   use_qk_l2norm=use_qk_l2norm_in_kernel, err_flags=err_flags,
+                                   stream=stream)

@@ -1,0 +1,157 @@
+// api.cu -- the C ABI of libgdn_decode.so: host-side argument checks and kernel dispatch.
+// Nothing here allocates, synchronises or touches device memory; every check runs on the host
+// before the first CUDA call, and a rejected call launches nothing.
+#include <cstdint>
+#include <cmath>
+#include <cstring>
+
+#include "gdn_launch.h"
+
+namespace {
+
+constexpr int kAbiVersion = 1;
+
+bool k_supported(int K) { return K == 16 || K == 32 || K == 64 || K == 128; }
+bool dtype_ok(int d) { return d == GDN_F32 || d == GDN_BF16; }
+size_t dtype_size(int d) { return d == GDN_BF16 ? 2 : 4; }
+bool aligned(const void *p, size_t bytes) { return (reinterpret_cast<uintptr_t>(p) % bytes) == 0; }
+
+// Checks shared by every entry point that takes gdn_step_args.
+int check_step(const gdn_step_args *a, bool indexed)
+{
+    if (!a) return GDN_ERR_NULL;
+    if (a->B < 0 || a->H < 1 || a->HV < 1 || a->num_slots < 1) return GDN_ERR_SHAPE;
+    if (a->HV % a->H != 0) return GDN_ERR_SHAPE;
+    if (!k_supported(a->K) || a->V < 1 || a->V > 1024) return GDN_ERR_SHAPE;
+    if ((int64_t)a->B * a->HV > INT32_MAX) return GDN_ERR_SHAPE;
+    if (!indexed && a->num_slots < a->B) return GDN_ERR_SHAPE;
+    if (!dtype_ok(a->in_dtype) || !dtype_ok(a->out_dtype)) return GDN_ERR_DTYPE;
+    if (a->gate_mode != GDN_GATE_RAW && a->gate_mode != GDN_GATE_DIRECT) return GDN_ERR_ARG;
+    if (a->B == 0) return GDN_OK;
+    if (!a->q || !a->k || !a->v || !a->state || !a->out) return GDN_ERR_NULL;
+    if (a->gate_mode == GDN_GATE_RAW && (!a->a || !a->b || !a->A_log || !a->dt_bias)) return GDN_ERR_NULL;
+    if (a->gate_mode == GDN_GATE_DIRECT && (!a->g || !a->beta)) return GDN_ERR_NULL;
+    const size_t es = dtype_size(a->in_dtype);
+    // q and k are read four elements at a time
+    if (!aligned(a->q, 4 * es) || !aligned(a->k, 4 * es)) return GDN_ERR_ALIGN;
+    if (a->q_stride % 4 != 0 || a->k_stride % 4 != 0) return GDN_ERR_ALIGN;
+    if (!aligned(a->v, es) || !aligned(a->out, dtype_size(a->out_dtype))) return GDN_ERR_ALIGN;
+    if (a->q_stride < (int64_t)a->H * a->K || a->k_stride < (int64_t)a->H * a->K ||
+        a->v_stride < (int64_t)a->HV * a->V)
+        return GDN_ERR_SHAPE;
+    if (!aligned(a->state, 16)) return GDN_ERR_ALIGN;
+    if (a->gate_mode == GDN_GATE_RAW && (!aligned(a->a, es) || !aligned(a->b, es))) return GDN_ERR_ALIGN;
+    return GDN_OK;
+}
+
+gdn::StepLaunch make_step(const gdn_step_args *a, const int32_t *idx, int32_t pad)
+{
+    gdn::StepLaunch p;
+    std::memset(&p, 0, sizeof(p));
+    p.a = *a;
+    p.idx = idx;
+    p.pad = pad;
+    p.G = a->HV / a->H;
+    p.scale = a->scale != 0.f ? a->scale : 1.0f / std::sqrt((float)a->K);
+    return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gdn_decode_step(const gdn_step_args *args, gdn_stream_t stream)
+{
+    int rc = check_step(args, false);
+    if (rc != GDN_OK || args->B == 0) return rc;
+    return gdn::launch_step(make_step(args, nullptr, 0), reinterpret_cast<cudaStream_t>(stream));
+}
+
+int gdn_decode_step_indexed(const gdn_step_args *args, const int32_t *cache_indices,
+                            int32_t pad_slot_id, gdn_stream_t stream)
+{
+    int rc = check_step(args, true);
+    if (rc != GDN_OK || args->B == 0) return rc;
+    if (!cache_indices) return GDN_ERR_NULL;
+    return gdn::launch_step(make_step(args, cache_indices, pad_slot_id),
+                            reinterpret_cast<cudaStream_t>(stream));
+}
+
+int gdn_decode_buffered(const gdn_step_args *args, const int32_t *cache_indices,
+                        int32_t pad_slot_id, const gdn_ring_args *ring, gdn_stream_t stream)
+{
+    int rc = check_step(args, cache_indices != nullptr);
+    if (rc != GDN_OK) return rc;
+    if (!ring) return GDN_ERR_NULL;
+    if (ring->L < 1 || ring->L > 64) return GDN_ERR_ARG;
+    if (!dtype_ok(ring->ring_dtype)) return GDN_ERR_DTYPE;
+    if (args->B == 0) return GDN_OK;
+    if (!ring->d_cache || !ring->k_cache || !ring->g_cache || !ring->write_pos) return GDN_ERR_NULL;
+    if (!aligned(ring->k_cache, 4 * dtype_size(ring->ring_dtype)) ||
+        !aligned(ring->d_cache, dtype_size(ring->ring_dtype)) || !aligned(ring->g_cache, 4))
+        return GDN_ERR_ALIGN;
+    if (gdn::buffered_smem_bytes(ring->L, args->V, args->K) > 200 * 1024) return GDN_ERR_SHAPE;
+    gdn::StepLaunch p = make_step(args, cache_indices, pad_slot_id);
+    p.L = ring->L;
+    p.d_cache = ring->d_cache;
+    p.k_cache = ring->k_cache;
+    p.g_cache = ring->g_cache;
+    p.write_pos = ring->write_pos;
+    return gdn::launch_buffered(p, ring->ring_dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int gdn_decode_fused(const gdn_fused_args *a, gdn_stream_t stream)
+{
+    if (!a) return GDN_ERR_NULL;
+    if (a->T < 0 || a->heads < 1 || a->num_slots < 1) return GDN_ERR_SHAPE;
+    if (!k_supported(a->head_dim)) return GDN_ERR_SHAPE;
+    if ((int64_t)a->T * a->heads > INT32_MAX) return GDN_ERR_SHAPE;
+    if (a->gate_kind != GDN_FUSED_GATE_KDA && a->gate_kind != GDN_FUSED_GATE_GDN) return GDN_ERR_ARG;
+    if (a->kda_gate_form != 0 && a->kda_gate_form != 1) return GDN_ERR_ARG;
+    if (a->gate_act != GDN_ACT_SILU && a->gate_act != GDN_ACT_SIGMOID) return GDN_ERR_ARG;
+    if (a->T == 0) return GDN_OK;
+    if (!a->x || !a->conv_w || !a->conv_state || !a->raw_g || !a->raw_beta || !a->A_log ||
+        !a->dt_bias || !a->state || !a->state_indices || !a->out_gate || !a->norm_w || !a->out)
+        return GDN_ERR_NULL;
+    const int64_t dim = (int64_t)a->heads * a->head_dim;
+    if (a->x_stride < 3 * dim) return GDN_ERR_SHAPE;
+    if (!aligned(a->x, 2) || !aligned(a->conv_state, 2) || !aligned(a->raw_g, 2) ||
+        !aligned(a->raw_beta, 2) || !aligned(a->out_gate, 2) || !aligned(a->out, 2))
+        return GDN_ERR_ALIGN;
+    if (!aligned(a->conv_w, 16) || !aligned(a->state, 16) || !aligned(a->A_log, 4) ||
+        !aligned(a->dt_bias, 4) || !aligned(a->norm_w, 4) || (a->conv_b && !aligned(a->conv_b, 4)))
+        return GDN_ERR_ALIGN;
+    gdn::FusedLaunch p;
+    std::memset(&p, 0, sizeof(p));
+    p.a = *a;
+    p.scale = a->scale != 0.f ? a->scale : 1.0f / std::sqrt((float)a->head_dim);
+    return gdn::launch_fused(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+const char *gdn_strerror(int status)
+{
+    switch (status) {
+    case GDN_OK: return "ok";
+    case GDN_ERR_NULL: return "a required pointer is NULL";
+    case GDN_ERR_SHAPE: return "unsupported or inconsistent size";
+    case GDN_ERR_DTYPE: return "unsupported dtype";
+    case GDN_ERR_ALIGN: return "a pointer or stride breaks the alignment rule";
+    case GDN_ERR_LAUNCH: return "the CUDA launch failed";
+    case GDN_ERR_ARG: return "invalid argument";
+    default: return "unknown status";
+    }
+}
+
+size_t gdn_abi_struct_size(int which)
+{
+    switch (which) {
+    case 0: return sizeof(gdn_step_args);
+    case 1: return sizeof(gdn_ring_args);
+    case 2: return sizeof(gdn_fused_args);
+    default: return 0;
+    }
+}
+
+int gdn_abi_version(void) { return kAbiVersion; }
+
+}  // extern "C"

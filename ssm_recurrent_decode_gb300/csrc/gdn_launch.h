@@ -1,0 +1,41 @@
+// gdn_launch.h -- launch parameters shared by the host layer (api.cu) and the kernels
+// (internal to libgdn_decode.so; the public interface is include/gdn_decode.h).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "gdn_decode.h"
+
+namespace gdn {
+
+// Everything one launch of the step or buffered kernel needs, resolved and validated on the host.
+struct StepLaunch {
+    gdn_step_args a;          // the caller's arguments (device pointers, sizes, strides)
+    const int32_t *idx;       // slot of each row, or nullptr for row b -> slot b
+    int32_t pad;              // rows whose index equals this are skipped
+    int32_t G;                // value heads per q/k head
+    float scale;              // resolved q scale
+    // buffered decode only
+    int32_t L;
+    void *d_cache;
+    void *k_cache;
+    float *g_cache;
+    const int32_t *write_pos;
+};
+
+struct FusedLaunch {
+    gdn_fused_args a;
+    float scale;
+};
+
+// Host launchers, one per kernel family; each dispatches on K and the dtypes. They return
+// GDN_OK or GDN_ERR_LAUNCH / GDN_ERR_SHAPE and never synchronise.
+int launch_step(const StepLaunch &p, cudaStream_t stream);
+int launch_buffered(const StepLaunch &p, int ring_dtype, cudaStream_t stream);
+int launch_fused(const FusedLaunch &p, cudaStream_t stream);
+
+// Dynamic shared memory the buffered kernel needs for ring length L, value dim V and key dim K.
+size_t buffered_smem_bytes(int L, int V, int K);
+
+}  // namespace gdn

@@ -1,0 +1,160 @@
+// gdn_tile.cuh -- the per-tile machinery of the decode kernels (internal to libgdn_decode.so).
+//
+// One CTA of 8 warps owns one state tile S[V, K] (fp32, key index contiguous). A state row of K
+// floats is read by LPR = K/4 lanes, one 16-byte vector each, so a warp instruction moves 512
+// contiguous bytes. Every thread keeps R = 16 such vectors in registers: the tile is read from
+// HBM once, both row dots (S.k and S.q) are taken from the registers, and the updated tile is
+// written back from the same registers. Nothing of the tile is re-read.
+//
+// Step arithmetic (single pass over S). With the decay D = diag(exp(g_k)) (all equal for the
+// per-head gate), S_bar = S D and the update S' = S_bar + delta k^T give
+//     u     = S_bar k  = S (D k)
+//     delta = beta (v - u)
+//     o     = S' q     = S (D q) + delta (k . q)
+//     S'    = S D + delta k^T
+// so one read of S feeds both dots. This is the step of "Optimization Log: Qwen3.5-27B Dense on
+// B200", section "Kernel 4: Fused DeltaNet Recurrent (FLAGSHIP)" (Math block: decay, S^T k,
+// delta, rank-1 update, S^T q), regrouped; that page's two-pass design reads S twice.
+#pragma once
+
+#include "gdn_common.cuh"
+#include "gdn_decode.h"
+
+namespace gdn {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr unsigned kFull = 0xFFFFFFFFu;
+
+template <int K>
+struct Tile {
+    static_assert(K == 16 || K == 32 || K == 64 || K == 128, "K must be 16, 32, 64 or 128");
+    static constexpr int LPR = K / 4;               // lanes per state row
+    static constexpr int RPI = 32 / LPR;            // rows per warp instruction
+    static constexpr int R = 16;                    // 16-byte vectors per thread per pass
+    static constexpr int N = 2 * R;                 // partial dots per thread (R for S.k, R for S.q)
+    static constexpr int M = N / LPR;               // fully reduced dots per lane
+    static constexpr int HALF = LPR / 2;            // lanes [0, HALF) of a row group end with S.k
+    static constexpr int ROWS_WARP = R * RPI;
+    static constexpr int ROWS_PASS = kWarps * ROWS_WARP;
+
+    int lane, warp, sub, grp, col;
+    float4 s[R];
+
+    __device__ __forceinline__ void init()
+    {
+        lane = threadIdx.x & 31;
+        warp = threadIdx.x >> 5;
+        sub = lane % LPR;
+        grp = lane / LPR;
+        col = sub * 4;
+    }
+
+    // state row held in vector i of the pass that starts at row0
+    __device__ __forceinline__ int row(int row0, int i) const
+    {
+        return row0 + warp * ROWS_WARP + i * RPI + grp;
+    }
+
+    // chunk index whose reduced dot this lane holds in slot m (see reduce_scatter)
+    __device__ __forceinline__ int owned_chunk(int m) const { return (sub % HALF) * M + m; }
+    __device__ __forceinline__ bool holds_k_dot() const { return sub < HALF; }
+
+    __device__ __forceinline__ void load(const float *tile, int V, int row0)
+    {
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            const int r = row(row0, i);
+            s[i] = r < V ? ld_stream(tile + (size_t)r * K + col) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+
+    // x[i] = S_i . kd, x[R + i] = S_i . qd over this lane's four columns
+    __device__ __forceinline__ void partial_dots(float4 kd, float4 qd, float (&x)[N]) const
+    {
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            x[i] = dot4(s[i], kd);
+            x[R + i] = dot4(s[i], qd);
+        }
+    }
+
+    // Butterfly reduce-scatter over the LPR lanes of a row group: at offset o a lane keeps one
+    // half of its values and adds the partner's copy of that half. After log2(LPR) steps lane
+    // `sub` holds the complete sums of indices sub*M .. sub*M + M-1 in x[0 .. M). That is
+    // N - N/LPR shuffles per lane instead of N * log2(LPR) for N separate reductions.
+    __device__ __forceinline__ void reduce_scatter(float (&x)[N]) const
+    {
+#pragma unroll
+        for (int o = LPR / 2, n = N; o >= 1; o >>= 1, n >>= 1) {
+            const bool upper = (lane & o) != 0;
+#pragma unroll
+            for (int j = 0; j < n / 2; ++j) {
+                const float send = upper ? x[j] : x[j + n / 2];
+                const float keep = upper ? x[j + n / 2] : x[j];
+                x[j] = keep + __shfl_xor_sync(kFull, send, o);
+            }
+        }
+    }
+
+    // delta of chunk i (the value sits on lane grp*LPR + i/M, slot i%M)
+    __device__ __forceinline__ float delta_of(const float (&dv)[M], int i) const
+    {
+        return __shfl_sync(kFull, dv[i % M], (lane & ~(LPR - 1)) + i / M);
+    }
+
+    // upper lanes receive the delta of the lower lane that owns the same chunk
+    __device__ __forceinline__ float delta_for_q(float dm) const
+    {
+        return __shfl_up_sync(kFull, dm, HALF);
+    }
+
+    // S' = S * dec + delta k^T, written back with streaming stores
+    __device__ __forceinline__ void update_store(float *tile, int V, int row0, float4 dec,
+                                                 float4 kh, const float (&dv)[M])
+    {
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            const float d = delta_of(dv, i);
+            const int r = row(row0, i);
+            if (r < V) st_stream(tile + (size_t)r * K + col, decay_update4(dec, s[i], d, kh));
+        }
+    }
+};
+
+// L2 normalisation of the q/k head held in four-element chunks by every row group of a warp:
+// returns x / sqrt(|x|^2 + eps) * s (or x * s when disabled).
+template <int LPR>
+__device__ __forceinline__ float4 l2_normalise4(float4 x, bool enabled, float s)
+{
+    const float ss = group_sum<LPR>(dot4(x, x));
+    const float r = enabled ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
+    return scale4(x, r * s);
+}
+
+__device__ __forceinline__ void store_out(void *out, int dtype, size_t i, float x)
+{
+    if (dtype == GDN_BF16)
+        static_cast<bf16 *>(out)[i] = __float2bfloat16_rn(x);
+    else
+        static_cast<float *>(out)[i] = x;
+}
+
+// g = -exp(A_log) softplus(a + dt_bias), beta = sigmoid(b) (raw mode) or the given values
+template <typename Tin>
+__device__ __forceinline__ void step_gates(const gdn_step_args &a, int b, int hv, float &g,
+                                           float &beta)
+{
+    const size_t gi = (size_t)b * a.HV + hv;
+    if (a.gate_mode == GDN_GATE_RAW) {
+        const float av = to_f32(static_cast<const Tin *>(a.a)[gi]);
+        const float bv = to_f32(static_cast<const Tin *>(a.b)[gi]);
+        g = -expf(a.A_log[hv]) * softplus_f(av + a.dt_bias[hv]);
+        beta = sigmoid_f(bv);
+    } else {
+        g = a.g[gi];
+        beta = a.beta[gi];
+    }
+}
+
+}  // namespace gdn

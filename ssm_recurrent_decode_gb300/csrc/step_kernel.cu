@@ -1,0 +1,110 @@
+// step_kernel.cu -- the packed / indexed single-token decode step (gdn_decode_step and
+// gdn_decode_step_indexed).
+//
+// Grid: one CTA per (row b, value head hv), blockIdx.x = b * HV + hv, so the G value heads that
+// share a q/k head sit next to each other and find its q/k in L2. Each CTA streams its 64 KB
+// (K = V = 128) fp32 tile in with 16-byte loads, takes S.(Dk) and S.(Dq) from registers, and
+// writes S' back with 16-byte streaming stores: one HBM read and one HBM write of the state,
+// which is the whole roofline of this memory-bound matrix-vector step.
+//
+// Sources: "Optimization Log: Qwen3.5-27B Dense on B200", "Kernel 4: Fused DeltaNet Recurrent
+// (FLAGSHIP)" (the Math block); "Microbenchmark: buffered output-only GDN decode (ReplaySSM Part
+// A)", _bench_cfg / run_packed (packed mixed_qkv, gates from a, b, A_log, dt_bias, in-kernel q/k
+// L2 norm with scale K^-1/2, ssm_state_indices, state [num_slots, HV, V, K] updated in place,
+// out [B, 1, HV, V]); _state_bytes_per_step (k [H, K] shared across HV // H value heads).
+#include "gdn_launch.h"
+#include "gdn_tile.cuh"
+
+namespace gdn {
+
+template <int K, typename Tin>
+__global__ void __launch_bounds__(kThreads, 2) step_kernel(const __grid_constant__ StepLaunch P)
+{
+    using TL = Tile<K>;
+    const gdn_step_args &a = P.a;
+    const int HV = a.HV, V = a.V;
+    const int b = blockIdx.x / HV, hv = blockIdx.x - b * HV, h = hv / P.G;
+    const size_t out_base = ((size_t)b * HV + hv) * V;
+
+    int slot = b;
+    if (P.idx) {
+        slot = P.idx[b];
+        const bool pad = slot == P.pad;
+        if (pad || slot < 0 || slot >= a.num_slots) {   // uniform over the CTA
+            if (!pad && threadIdx.x == 0) raise_flag(a.err_flags, GDN_DEVERR_BAD_INDEX);
+            for (int r = threadIdx.x; r < V; r += kThreads) store_out(a.out, a.out_dtype, out_base + r, 0.f);
+            return;
+        }
+    }
+    float *S = a.state + ((size_t)slot * HV + hv) * (size_t)V * K;
+
+    TL t;
+    t.init();
+    t.load(S, V, 0);   // the tile's loads go out first; everything below overlaps them
+
+    const Tin *qp = static_cast<const Tin *>(a.q) + (size_t)b * a.q_stride + (size_t)h * K;
+    const Tin *kp = static_cast<const Tin *>(a.k) + (size_t)b * a.k_stride + (size_t)h * K;
+    const Tin *vp = static_cast<const Tin *>(a.v) + (size_t)b * a.v_stride + (size_t)hv * V;
+    const float4 q4 = load4(qp + t.col), k4 = load4(kp + t.col);
+    float g, beta;
+    step_gates<Tin>(a, b, hv, g, beta);
+
+    const float4 kh = l2_normalise4<TL::LPR>(k4, a.use_qk_l2norm != 0, 1.f);
+    const float4 qh = l2_normalise4<TL::LPR>(q4, a.use_qk_l2norm != 0, P.scale);
+    const float kq = group_sum<TL::LPR>(dot4(kh, qh));
+    const float e = expf(g);
+    const float4 dec = make_float4(e, e, e, e);
+    const float4 kd = scale4(kh, e), qd = scale4(qh, e);
+
+    for (int row0 = 0; row0 < V; row0 += TL::ROWS_PASS) {
+        if (row0) t.load(S, V, row0);
+        float vv[TL::M];
+#pragma unroll
+        for (int m = 0; m < TL::M; ++m) {
+            const int r = t.row(row0, t.owned_chunk(m));
+            vv[m] = (t.holds_k_dot() && r < V) ? to_f32(vp[r]) : 0.f;
+        }
+        float x[TL::N];
+        t.partial_dots(kd, qd, x);
+        t.reduce_scatter(x);
+        // lanes [0, HALF) of a row group: x[m] = u of their rows -> delta
+        float dv[TL::M];
+#pragma unroll
+        for (int m = 0; m < TL::M; ++m) dv[m] = beta * (vv[m] - x[m]);
+        // lanes [HALF, LPR): x[m] = S (D q) of the same rows -> o = x + delta (k . q)
+#pragma unroll
+        for (int m = 0; m < TL::M; ++m) {
+            const float dq = t.delta_for_q(dv[m]);
+            const int r = t.row(row0, t.owned_chunk(m));
+            if (!t.holds_k_dot() && r < V) store_out(a.out, a.out_dtype, out_base + r, fmaf(dq, kq, x[m]));
+        }
+        t.update_store(S, V, row0, dec, kh, dv);
+    }
+}
+
+template <int K, typename Tin>
+static int launch_step_t(const StepLaunch &p, cudaStream_t stream)
+{
+    const unsigned tiles = (unsigned)p.a.B * (unsigned)p.a.HV;
+    step_kernel<K, Tin><<<tiles, kThreads, 0, stream>>>(p);
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
+}
+
+template <typename Tin>
+static int launch_step_k(const StepLaunch &p, cudaStream_t stream)
+{
+    switch (p.a.K) {
+    case 16: return launch_step_t<16, Tin>(p, stream);
+    case 32: return launch_step_t<32, Tin>(p, stream);
+    case 64: return launch_step_t<64, Tin>(p, stream);
+    case 128: return launch_step_t<128, Tin>(p, stream);
+    default: return GDN_ERR_SHAPE;
+    }
+}
+
+int launch_step(const StepLaunch &p, cudaStream_t stream)
+{
+    return p.a.in_dtype == GDN_BF16 ? launch_step_k<bf16>(p, stream) : launch_step_k<float>(p, stream);
+}
+
+}  // namespace gdn

@@ -1,0 +1,144 @@
+"""CPU checks of the C-ABI library: it builds, loads, exports every function include/gdn_decode.h
+declares, agrees with the binding on struct layout, and rejects bad arguments on the host before
+any CUDA call (so these run without a GPU: no call here reaches a launch)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import ssm_recurrent_decode_gb300 as gdn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))
+           if f.endswith(".h")]
+
+
+def declared_functions():
+    names = []
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(gdn_\w+)\s*\(", text, re.M):
+            names.append(m.group(1))
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in gdn.EXPORTS:
+        assert n in names, n
+    assert set(names) == set(gdn.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol():
+    L = gdn.lib()
+    for n in declared_functions():
+        assert hasattr(L, n), f"{n} not exported"
+
+
+def test_struct_layout_and_version():
+    L = gdn.lib()
+    assert L.gdn_abi_struct_size(0) == ctypes.sizeof(gdn.GdnStepArgs)
+    assert L.gdn_abi_struct_size(1) == ctypes.sizeof(gdn.GdnRingArgs)
+    assert L.gdn_abi_struct_size(2) == ctypes.sizeof(gdn.GdnFusedArgs)
+    assert L.gdn_abi_struct_size(9) == 0
+    assert L.gdn_abi_version() == gdn.ABI_VERSION
+
+
+def test_strerror():
+    assert gdn.gdn_strerror(0) == "ok"
+    assert "NULL" in gdn.gdn_strerror(-1)
+    assert gdn.gdn_strerror(12345) == "unknown status"
+
+
+def _valid_args():
+    """Step arguments with fake, aligned, never dereferenced device addresses."""
+    s = gdn.GdnStepArgs()
+    s.B, s.H, s.HV, s.K, s.V, s.num_slots = 4, 2, 4, 128, 128, 4
+    s.in_dtype, s.out_dtype = gdn.GDN_BF16, gdn.GDN_BF16
+    base = 1 << 40
+    s.q, s.k, s.v = base, base + 512, base + 1024
+    s.q_stride = s.k_stride = s.v_stride = 2 * 2 * 128 + 4 * 128
+    s.gate_mode = 0
+    s.a, s.b, s.A_log, s.dt_bias = base + 4096, base + 8192, base + 12288, base + 16384
+    s.state, s.out = base + (1 << 30), base + (1 << 31)
+    return s
+
+
+BAD = [
+    ("null q", lambda s: setattr(s, "q", None), -1),
+    ("null state", lambda s: setattr(s, "state", None), -1),
+    ("null gate input", lambda s: setattr(s, "A_log", None), -1),
+    ("K unsupported", lambda s: setattr(s, "K", 96), -2),
+    ("V too large", lambda s: setattr(s, "V", 2048), -2),
+    ("HV not a multiple of H", lambda s: setattr(s, "HV", 3), -2),
+    ("num_slots below B", lambda s: setattr(s, "num_slots", 2), -2),
+    ("negative B", lambda s: setattr(s, "B", -1), -2),
+    ("bad dtype", lambda s: setattr(s, "in_dtype", 7), -3),
+    ("q misaligned", lambda s: setattr(s, "q", (1 << 40) + 2), -4),
+    ("k stride not a multiple of 4", lambda s: setattr(s, "k_stride", 1026), -4),
+    ("state misaligned", lambda s: setattr(s, "state", (1 << 40) + 8), -4),
+    ("row stride too short", lambda s: setattr(s, "v_stride", 100), -2),
+    ("bad gate mode", lambda s: setattr(s, "gate_mode", 5), -6),
+    ("direct gate without g", lambda s: setattr(s, "gate_mode", 1), -1),
+]
+
+
+@pytest.mark.parametrize("name,mutate,code", BAD, ids=[b[0] for b in BAD])
+def test_step_rejects_bad_arguments_on_the_host(name, mutate, code):
+    s = _valid_args()
+    mutate(s)
+    assert gdn.lib().gdn_decode_step(ctypes.byref(s), None) == code
+
+
+def test_null_args_and_null_indices():
+    L = gdn.lib()
+    assert L.gdn_decode_step(None, None) == -1
+    assert L.gdn_decode_fused(None, None) == -1
+    s = _valid_args()
+    assert L.gdn_decode_step_indexed(ctypes.byref(s), None, -1, None) == -1
+
+
+def test_empty_batch_launches_nothing():
+    s = _valid_args()
+    s.B = 0
+    assert gdn.lib().gdn_decode_step(ctypes.byref(s), None) == 0
+
+
+def test_buffered_ring_checks():
+    L = gdn.lib()
+    s = _valid_args()
+    r = gdn.GdnRingArgs()
+    r.L, r.ring_dtype = 0, gdn.GDN_BF16
+    assert L.gdn_decode_buffered(ctypes.byref(s), None, -1, ctypes.byref(r), None) == -6
+    r.L = 65
+    assert L.gdn_decode_buffered(ctypes.byref(s), None, -1, ctypes.byref(r), None) == -6
+    r.L = 8
+    assert L.gdn_decode_buffered(ctypes.byref(s), None, -1, ctypes.byref(r), None) == -1
+    assert L.gdn_decode_buffered(ctypes.byref(s), None, -1, None, None) == -1
+    r.ring_dtype = 3
+    assert L.gdn_decode_buffered(ctypes.byref(s), None, -1, ctypes.byref(r), None) == -3
+
+
+def test_fused_checks():
+    L = gdn.lib()
+    f = gdn.GdnFusedArgs()
+    f.T, f.heads, f.head_dim, f.num_slots = 2, 4, 128, 4
+    assert L.gdn_decode_fused(ctypes.byref(f), None) == -1          # NULL pointers
+    f.head_dim = 100
+    assert L.gdn_decode_fused(ctypes.byref(f), None) == -2
+    f.head_dim, f.gate_kind = 128, 4
+    assert L.gdn_decode_fused(ctypes.byref(f), None) == -6
+    f.gate_kind, f.T = 0, 0
+    assert L.gdn_decode_fused(ctypes.byref(f), None) == 0
+
+
+def test_binding_refuses_cpu_tensors():
+    torch = pytest.importorskip("torch")
+    x = torch.zeros((2, 2 * 2 * 16 + 4 * 16))
+    q, k, v = gdn.split_mixed_qkv(x, 2, 4, 16, 16)
+    with pytest.raises(TypeError, match="CUDA"):
+        gdn.gdn_decode_step(q, k, v, torch.zeros((2, 4, 16, 16)), torch.zeros((2, 4, 16)), H=2,
+                            a=torch.zeros(2, 4), b=torch.zeros(2, 4), A_log=torch.zeros(4),
+                            dt_bias=torch.zeros(4))
