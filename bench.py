@@ -231,9 +231,88 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------------------------------------------
-# GPU arm
+# GPU arm: shared timing harness
 # ------------------------------------------------------------------------------------------------
-def packed_workload(B, H, HV, K, V, seed, device):
+def max_over_ranks(values, world):
+    """Element-wise maximum of a list of floats over all ranks (gloo all-reduce); identity at N=1."""
+    import torch
+    t = torch.tensor(values, dtype=torch.float64)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+class Harness:
+    def __init__(self, args):
+        import torch
+        self.torch = torch
+        self.args = args
+        self.rank, self.world, local = dist_env()
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("gloo")
+        self.dev = torch.device("cuda", local)
+        torch.cuda.set_device(self.dev)
+        self.stream = torch.cuda.current_stream(self.dev)
+
+    def barrier(self):
+        self.torch.cuda.synchronize(self.dev)
+        if self.world > 1:
+            self.torch.distributed.barrier()
+
+    def time_steps(self, step, steps, warmup, sample_clocks=True):
+        """warm-up, then `steps` calls of step(i) bracketed by barrier + synchronize, timed with
+        CUDA events on the launching stream. Returns (ms per step, clocks record)."""
+        torch = self.torch
+        for i in range(warmup):
+            step(i)
+        clocks = ClockSampler(self.dev.index) if sample_clocks else None
+        if clocks:
+            clocks.start()
+        self.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.time()
+        e0.record(self.stream)
+        for i in range(steps):
+            step(i)
+        e1.record(self.stream)
+        self.barrier()
+        t1 = time.time()
+        if clocks:
+            clocks.mark(t0, t1)
+        return e0.elapsed_time(e1) / steps, (clocks.stop() if clocks else None)
+
+    def finish(self, line):
+        if self.rank == 0 and line is not None:
+            print(json.dumps(line), flush=True)
+        if self.world > 1:
+            self.torch.distributed.destroy_process_group()
+        return 0
+
+
+def roofline(achieved_bytes_per_launch, ms, kernel, traffic_key):
+    peak, src = hbm_peak()
+    ach = achieved_bytes_per_launch / (ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": round(ach, 2), "peak": peak, "unit": "GB/s",
+            "frac": round(ach / peak, 4), "peak_source": f"{src} (hbm copy, burst)",
+            "traffic": measured_traffic(kernel, traffic_key),
+            "algorithmic_bytes_per_launch": int(achieved_bytes_per_launch)}
+
+
+def base_line(h, value, ms, steps, warmup, workload, config, kernel_launches):
+    return {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": h.world,
+            "steps": steps, "warmup": warmup, "ms_per_step": round(ms, 6),
+            "us_per_step": round(ms * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": workload, **config, "parallelism": f"replicas x{h.world}"},
+            "gpu_launches": kernel_launches}
+
+
+# ------------------------------------------------------------------------------------------------
+# workloads
+# ------------------------------------------------------------------------------------------------
+def packed_workload(B, H, HV, K, V, seed, device, layer=0):
     import torch
     import gdn_synth as syn
     width = 2 * H * K + HV * V
@@ -244,127 +323,332 @@ def packed_workload(B, H, HV, K, V, seed, device):
     dt_bias = torch.empty(HV, dtype=torch.float32, device=device)
     state = torch.empty((B, HV, V, K), dtype=torch.float32, device=device)
     r = syn.GdnRecipe()
-    syn.fill_normal_(x, seed, syn.Tag.QKV, 0, r.qkv_std)
-    syn.fill_normal_(a, seed, syn.Tag.A, 0, r.a_std)
-    syn.fill_normal_(b, seed, syn.Tag.B, 0, r.b_std)
-    syn.fill_normal_(A_log, seed, syn.Tag.A_LOG, 0, r.A_log_std)
-    syn.fill_normal_(dt_bias, seed, syn.Tag.DT_BIAS, 0, r.dt_bias_std)
-    syn.fill_normal_(state, seed, syn.Tag.STATE, 0, r.state_std)
-    idx = torch.from_numpy(syn.permutation(seed, B)).to(device)
+    syn.fill_normal_(x, seed, syn.Tag.QKV, 0, r.qkv_std, layer)
+    syn.fill_normal_(a, seed, syn.Tag.A, 0, r.a_std, layer)
+    syn.fill_normal_(b, seed, syn.Tag.B, 0, r.b_std, layer)
+    syn.fill_normal_(A_log, seed, syn.Tag.A_LOG, 0, r.A_log_std, layer)
+    syn.fill_normal_(dt_bias, seed, syn.Tag.DT_BIAS, 0, r.dt_bias_std, layer)
+    syn.fill_normal_(state, seed, syn.Tag.STATE, 0, r.state_std, layer)
+    idx = torch.from_numpy(syn.permutation(seed + 7919 * layer, B)).to(device)
     out = torch.empty((B, 1, HV, V), dtype=torch.bfloat16, device=device)
     return dict(x=x, a=a, b=b, A_log=A_log, dt_bias=dt_bias, state=state, idx=idx, out=out)
 
 
+def packed_io_bytes(B, H, HV, K, V):
+    """Bytes of the step's inputs and outputs besides the state: mixed_qkv, a, b, A_log, dt_bias,
+    cache indices, out."""
+    return B * (2 * H * K + HV * V) * 2 + 2 * B * HV * 2 + 2 * HV * 4 + B * 4 + B * HV * V * 2
+
+
 def run_packed(args):
-    import torch
     import ssm_recurrent_decode_gb300 as gdn
-    rank, world, local = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("gloo")
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
+    h = Harness(args)
+    torch = h.torch
     gdn.lib()
     B, H, HV, K, V = args.B, 16, 32, 128, 128
-    w = packed_workload(B, H, HV, K, V, seed=1234 + rank, device=dev)
+    w = packed_workload(B, H, HV, K, V, seed=1234 + h.rank, device=h.dev)
     q, k, v = gdn.split_mixed_qkv(w["x"], H, HV, K, V)
-    stream = torch.cuda.current_stream(dev)
+    sid = h.stream.cuda_stream
 
-    def step():
+    def step(_):
         gdn.gdn_decode_step_indexed(q, k, v, w["state"], w["out"], w["idx"], H=H, a=w["a"],
-                                    b=w["b"], A_log=w["A_log"], dt_bias=w["dt_bias"],
-                                    stream=stream.cuda_stream)
+                                    b=w["b"], A_log=w["A_log"], dt_bias=w["dt_bias"], stream=sid)
 
-    def barrier():
-        torch.cuda.synchronize(dev)
-        if world > 1:
-            torch.distributed.barrier()
-
-    for _ in range(args.warmup):
-        step()
-    clocks = ClockSampler(dev.index)
-    clocks.start()
-    barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0 = time.time()
-    e0.record(stream)
-    for _ in range(args.steps):
-        step()
-    e1.record(stream)
-    barrier()
-    t1 = time.time()
-    clocks.mark(t0, t1)
-    ms = e0.elapsed_time(e1) / args.steps
-    clk = clocks.stop()
+    ms, clk = h.time_steps(step, args.steps, args.warmup)
 
     # end to end through the public API: pinned host inputs in, output back to pinned host memory
-    hx = torch.empty_like(w["x"], device="cpu").pin_memory().copy_(w["x"].cpu())
-    ha = torch.empty_like(w["a"], device="cpu").pin_memory().copy_(w["a"].cpu())
-    hb = torch.empty_like(w["b"], device="cpu").pin_memory().copy_(w["b"].cpu())
-    hout = torch.empty_like(w["out"], device="cpu").pin_memory()
-    e2e_steps = max(1, min(args.steps, 2000))
+    hx = w["x"].cpu().pin_memory()
+    ha, hb = w["a"].cpu().pin_memory(), w["b"].cpu().pin_memory()
+    hout = torch.empty(w["out"].shape, dtype=w["out"].dtype).pin_memory()
 
-    def e2e_step():
+    def e2e_step(i):
         w["x"].copy_(hx, non_blocking=True)
         w["a"].copy_(ha, non_blocking=True)
         w["b"].copy_(hb, non_blocking=True)
-        step()
+        step(i)
         hout.copy_(w["out"], non_blocking=True)
 
-    for _ in range(3):
-        e2e_step()
-    barrier()
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    barrier()
-    ms_e2e = e0.elapsed_time(e1) / e2e_steps
-    h2d = hx.numel() * 2 + ha.numel() * 2 + hb.numel() * 2
+    e2e_steps = max(1, min(args.steps, 2000))
+    ms_e2e, _ = h.time_steps(e2e_step, e2e_steps, 3, sample_clocks=False)
+    h2d = (hx.numel() + ha.numel() + hb.numel()) * 2
     d2h = hout.numel() * 2
-
-    times = torch.tensor([ms, ms_e2e], dtype=torch.float64)
-    if world > 1:
-        torch.distributed.all_reduce(times, op=torch.distributed.ReduceOp.MAX)
-    ms, ms_e2e = float(times[0]), float(times[1])
-    if rank != 0:
-        torch.distributed.destroy_process_group()
-        return 0
+    ms, ms_e2e = max_over_ranks([ms, ms_e2e], h.world)
+    if h.rank != 0:
+        return h.finish(None)
 
     state_bytes = 2 * B * HV * V * K * 4
-    io_bytes = (B * (2 * H * K + HV * V) * 2 + 2 * B * HV * 2 + 2 * HV * 4 + B * 4
-                + B * HV * V * 2)
-    gbs = world * state_bytes / (ms * 1e-3) / 1e9
-    peak, peak_src = hbm_peak()
-    achieved = (state_bytes + io_bytes) / (ms * 1e-3) / 1e9
-    line = {
-        "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 6),
-        "us_per_step": round(ms * 1e3, 3), "pct_of_peak": round(100 * gbs / world / peak, 2),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic",
-        "config": {"workload": f"gdn packed decode over a slot pool: B={B} H={H} HV={HV} K=V={K}, "
-                               f"bf16 mixed_qkv/a/b/out, fp32 state [{B},{HV},{V},{K}], "
-                               f"permuted int32 cache indices",
-                   "B": B, "H": H, "HV": HV, "K": K, "V": V, "input_dtype": "bf16",
-                   "state_dtype": "f32", "state_bytes_per_step": state_bytes,
-                   "l2": "state larger than L2 (1.07 GB vs 129 MB): no flush between steps",
-                   "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "peak_source": f"{peak_src} (hbm copy)",
-                     "traffic": measured_traffic("step", f"packed_B{B}"),
-                     "algorithmic_bytes_per_launch": state_bytes + io_bytes},
-        "cpu_baseline": cpu_baseline(H, HV, K, V, seed=7, budget_s=args.cpu_budget),
-        "e2e": {"value": round(world * state_bytes / (ms_e2e * 1e-3) / 1e9, 2), "unit": "GB/s",
-                "us_per_step": round(ms_e2e * 1e3, 3), "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps,
-        "clocks": clk,
-    }
-    print(json.dumps(line), flush=True)
-    if world > 1:
-        torch.distributed.destroy_process_group()
-    return 0
+    gbs = h.world * state_bytes / (ms * 1e-3) / 1e9
+    peak, _ = hbm_peak()
+    line = base_line(
+        h, gbs, ms, args.steps, args.warmup,
+        f"gdn packed decode over a slot pool: B={B} H={H} HV={HV} K=V={K}, bf16 mixed_qkv/a/b/out, "
+        f"fp32 state [{B},{HV},{V},{K}], permuted int32 cache indices",
+        {"B": B, "H": H, "HV": HV, "K": K, "V": V, "input_dtype": "bf16", "state_dtype": "f32",
+         "state_bytes_per_step": state_bytes,
+         "l2": "state larger than L2 (1.07 GB vs 129 MB at B=256): no flush between steps"},
+        args.steps)
+    line["pct_of_peak"] = round(100 * gbs / h.world / peak, 2)
+    line["roofline"] = roofline(state_bytes + packed_io_bytes(B, H, HV, K, V), ms, "step", f"packed_B{B}")
+    line["cpu_baseline"] = cpu_baseline(H, HV, K, V, seed=7, budget_s=args.cpu_budget)
+    line["e2e"] = {"value": round(h.world * state_bytes / (ms_e2e * 1e-3) / 1e9, 2), "unit": "GB/s",
+                   "us_per_step": round(ms_e2e * 1e3, 3), "h2d_bytes_per_step": h2d,
+                   "d2h_bytes_per_step": d2h}
+    line["clocks"] = clk
+    return h.finish(line)
+
+
+def run_buffered(args):
+    """Buffered output-only decode at the packed shapes: every step reads the checkpoint tile,
+    appends d/k/g records, and the step at write_pos == L-1 folds the ring and writes the tile.
+    The timed loop runs whole cycles (all L phases, every row at the same phase), so the mean is
+    the exact cycle average; each phase is also timed on its own."""
+    import ssm_recurrent_decode_gb300 as gdn
+    h = Harness(args)
+    torch = h.torch
+    gdn.lib()
+    B, H, HV, K, V, L = args.B, 16, 32, 128, 128, args.L
+    w = packed_workload(B, H, HV, K, V, seed=4321 + h.rank, device=h.dev)
+    q, k, v = gdn.split_mixed_qkv(w["x"], H, HV, K, V)
+    d_cache = torch.zeros((B, HV, L, V), dtype=torch.bfloat16, device=h.dev)
+    k_cache = torch.zeros((B, H, L, K), dtype=torch.bfloat16, device=h.dev)
+    g_cache = torch.zeros((B, HV, L), dtype=torch.float32, device=h.dev)
+    pos = [torch.full((B,), p, dtype=torch.int32, device=h.dev) for p in range(L)]
+    sid = h.stream.cuda_stream
+
+    def step(i):
+        gdn.gdn_decode_buffered(q, k, v, w["state"], w["out"], d_cache, k_cache, g_cache,
+                                pos[i % L], cache_indices=w["idx"], H=H, a=w["a"], b=w["b"],
+                                A_log=w["A_log"], dt_bias=w["dt_bias"], stream=sid)
+
+    steps = max(L, (args.steps // L) * L)
+    warm = max(args.warmup, L)
+    warm = ((warm + L - 1) // L) * L
+    ms, clk = h.time_steps(step, steps, warm)
+    # per-phase times: events around each call of a cycle, averaged over cycles
+    cycles = max(1, min(50, steps // L))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(cycles * L)]
+    h.barrier()
+    for i in range(cycles * L):
+        ev[i][0].record(h.stream)
+        step(i)
+        ev[i][1].record(h.stream)
+    h.barrier()
+    phase_ms = [statistics.mean(ev[c * L + p][0].elapsed_time(ev[c * L + p][1]) for c in range(cycles))
+                for p in range(L)]
+    (ms,) = max_over_ranks([ms], h.world)
+    if h.rank != 0:
+        return h.finish(None)
+    S = B * HV * V * K * 4
+    state_traffic = (1 + 1 / L) * S
+    ring_append = B * (HV * V * 2 + H * K * 2 + HV * 4)
+    ring_read_mean = B * (HV * V * 2 + H * K * 2 + HV * 4) * (L - 1) / 2
+    io = packed_io_bytes(B, H, HV, K, V)
+    gbs = h.world * state_traffic / (ms * 1e-3) / 1e9
+    line = base_line(
+        h, gbs, ms, steps, warm,
+        f"gdn buffered output-only decode: B={B} H={H} HV={HV} K=V={K}, L={L}, bf16 rings, "
+        f"fp32 checkpoint state, all phases timed", {"B": B, "H": H, "HV": HV, "K": K, "V": V, "L": L,
+        "state_bytes_per_step_mean": state_traffic,
+        "packed_equivalent_state_GBs": round(2 * S / (ms * 1e-3) / 1e9, 2)}, steps)
+    line["roofline"] = roofline(state_traffic + ring_append + ring_read_mean + io, ms, "buffered",
+                                f"buffered_B{B}_L{L}")
+    line["phase_us"] = [round(p * 1e3, 2) for p in phase_ms]
+    line["flush_over_nonflush"] = (round(phase_ms[-1] / statistics.mean(phase_ms[:-1]), 3)
+                                   if L > 1 else None)
+    line["clocks"] = clk
+    return h.finish(line)
+
+
+def fused_workload(T, heads, D, seed, device, layout="DS"):
+    import numpy as np
+    import torch
+    import gdn_synth as syn
+    num_slots = T + 8
+    dim = heads * D
+    ins = syn.fused_inputs(T, heads, D, num_slots, seed)
+    bf = lambda bits: torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+    state = torch.empty((num_slots, heads, D, D), dtype=torch.float32, device=device)
+    syn.fill_normal_(state, seed, syn.Tag.STATE, 0, 1.0)
+    cs = bf(ins["conv_state"])
+    if layout == "SD":
+        cs = cs.transpose(1, 2).contiguous().transpose(1, 2)
+    return dict(x=bf(ins["x"]), conv_w=torch.from_numpy(ins["conv_w"]).to(device), conv_state=cs,
+                raw_g=bf(ins["raw_g"]), raw_beta=bf(ins["raw_beta"]),
+                A_log=torch.from_numpy(ins["A_log"]).to(device),
+                dt_bias=torch.from_numpy(ins["dt_bias"]).to(device), state=state,
+                idx=torch.arange(1, T + 1, dtype=torch.int32, device=device),
+                out_gate=bf(ins["out_gate"]), norm_w=torch.from_numpy(ins["norm_w"]).to(device),
+                out=torch.empty((T, heads, D), dtype=torch.bfloat16, device=device), dim=dim)
+
+
+def run_fused(args):
+    """Fused KDA decode (conv update -> per-key-decay delta step -> gated RMSNorm), 96 heads of
+    128, T tokens, T+8 slots, slot 0 the NULL slot."""
+    import ssm_recurrent_decode_gb300 as gdn
+    h = Harness(args)
+    gdn.lib()
+    T, heads, D = args.T, 96, 128
+    w = fused_workload(T, heads, D, seed=555 + h.rank, device=h.dev, layout=args.layout)
+    sid = h.stream.cuda_stream
+
+    def step(_):
+        gdn.gdn_decode_fused(w["x"], w["conv_w"], w["conv_state"], w["raw_g"], w["raw_beta"],
+                             w["A_log"], w["dt_bias"], w["state"], w["idx"], w["out_gate"],
+                             w["norm_w"], w["out"], pad_slot_id=0, gate_kind="kda",
+                             kda_gate_form=0, gate_act="silu", stream=sid)
+
+    ms, clk = h.time_steps(step, args.steps, args.warmup)
+    (ms,) = max_over_ranks([ms], h.world)
+    if h.rank != 0:
+        return h.finish(None)
+    dim = w["dim"]
+    state_bytes = 2 * T * heads * D * D * 4
+    io = (T * 3 * dim * 2            # x
+          + 2 * T * 3 * dim * 3 * 2  # conv state read + write
+          + 3 * dim * 4 * 4          # conv weights
+          + T * dim * 2 * 2          # raw_g, out_gate
+          + T * heads * 2 + heads * 4 + dim * 4 + D * 4 + T * 4
+          + T * dim * 2)             # out
+    gbs = h.world * state_bytes / (ms * 1e-3) / 1e9
+    line = base_line(
+        h, gbs, ms, args.steps, args.warmup,
+        f"fused KDA decode: T={T} tokens, {heads} heads x {D}, conv width 4 ({args.layout} conv "
+        f"state), per-key decay bounded at -5, gated RMSNorm with silu",
+        {"T": T, "heads": heads, "head_dim": D, "state_bytes_per_step": state_bytes,
+         "l2": ("state larger than L2: no flush" if state_bytes / 2 > 129e6 else
+                "state fits in L2: figure is L2-assisted")}, args.steps)
+    line["roofline"] = roofline(state_bytes + io, ms, "fused", f"fused_T{T}")
+    line["clocks"] = clk
+    return h.finish(line)
+
+
+def stack_decode(layers=48, B=256, H=16, HV=48, K=128, V=128, steps=1000, seed=2024, pairs=8,
+                 heads_per_pair=2, device=None, verbose=False):
+    """The stacked decode under CUDA graphs: `layers` independent state pools, one graph that
+    draws fresh seeded inputs for every layer on the device (keyed by seed, layer and a device step
+    counter), and one graph of `layers` decode calls, replayed `steps` times. Afterwards the fp64
+    oracle replays `pairs` sampled (layer, slot) pairs, on `heads_per_pair` q/k heads each (all
+    their value heads), through every step and the drift of the GPU state against it is measured.
+    Returns a dict of timings and errors."""
+    import torch
+    import gdn_synth as syn
+    import oracle
+    import ssm_recurrent_decode_gb300 as gdn
+    dev = device or torch.device("cuda", torch.cuda.current_device())
+    r = syn.GdnRecipe()
+    G = HV // H
+    width = 2 * H * K + HV * V
+    ctr = torch.zeros(1, dtype=torch.int32, device=dev)
+    L = []
+    for l in range(layers):
+        w = packed_workload(B, H, HV, K, V, seed, dev, layer=l)
+        L.append(w)
+
+    def gen():
+        for l, w in enumerate(L):
+            syn.fill_normal_(w["x"], seed, syn.Tag.QKV, 0, r.qkv_std, l, step_ptr=ctr)
+            syn.fill_normal_(w["a"], seed, syn.Tag.A, 0, r.a_std, l, step_ptr=ctr)
+            syn.fill_normal_(w["b"], seed, syn.Tag.B, 0, r.b_std, l, step_ptr=ctr)
+        syn.add_i32_(ctr, 1)
+
+    views = [gdn.split_mixed_qkv(w["x"], H, HV, K, V) for w in L]
+
+    def decode():
+        sid = torch.cuda.current_stream(dev).cuda_stream
+        for (q, k, v), w in zip(views, L):
+            gdn.gdn_decode_step_indexed(q, k, v, w["state"], w["out"], w["idx"], H=H, a=w["a"],
+                                        b=w["b"], A_log=w["A_log"], dt_bias=w["dt_bias"], stream=sid)
+
+    # one eager pass loads every kernel before capture; then the pools are reset to step 0
+    gen()
+    decode()
+    torch.cuda.synchronize(dev)
+    for l, w in enumerate(L):
+        syn.fill_normal_(w["state"], seed, syn.Tag.STATE, 0, r.state_std, l)
+    ctr.zero_()
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    g_gen, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_gen, stream=s):
+        gen()
+    with torch.cuda.graph(g_dec, stream=s):
+        decode()
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        w0.record(s)
+        for i in range(steps):
+            g_gen.replay()
+            ev[i][0].record(s)
+            g_dec.replay()
+            ev[i][1].record(s)
+        w1.record(s)
+    torch.cuda.synchronize(dev)
+    dec_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = w0.elapsed_time(w1)
+
+    # sampled (layer, slot) pairs, replayed by the oracle from the initial tiles
+    rng = np.random.default_rng(seed)
+    picks = []
+    for _ in range(pairs):
+        l = int(rng.integers(layers)); b = int(rng.integers(B)); h0 = int(rng.integers(H - heads_per_pair + 1))
+        picks.append((l, b, h0))
+    drift, out_err = 0.0, 0.0
+    for l, b, h0 in picks:
+        slot = int(L[l]["idx"][b].item())
+        hvs = list(range(h0 * G, (h0 + heads_per_pair) * G))
+        S = np.stack([syn.state_tile_values(seed, HV, V, K, slot, hv, r.state_std, l) for hv in hvs])[None].astype(np.float64)
+        A_log = syn.normal_f32(seed, syn.Tag.A_LOG, 0, (HV,), r.A_log_std, l).astype(np.float64)[hvs]
+        dt_bias = syn.normal_f32(seed, syn.Tag.DT_BIAS, 0, (HV,), r.dt_bias_std, l).astype(np.float64)[hvs]
+        f64 = lambda x: syn.bf16_bits_to_f32(syn.f32_to_bf16_bits(x)).astype(np.float64)
+        for step in range(steps):
+            x = f64(syn.normal_f32(seed, syn.Tag.QKV, step, (width,), r.qkv_std, l, start=b * width))
+            av = f64(syn.normal_f32(seed, syn.Tag.A, step, (HV,), r.a_std, l, start=b * HV))[hvs]
+            bv = f64(syn.normal_f32(seed, syn.Tag.B, step, (HV,), r.b_std, l, start=b * HV))[hvs]
+            q = x[:H * K].reshape(H, K)[h0:h0 + heads_per_pair][None]
+            k = x[H * K:2 * H * K].reshape(H, K)[h0:h0 + heads_per_pair][None]
+            v = x[2 * H * K:].reshape(HV, V)[hvs][None]
+            g, beta = oracle.gdn_gates(av[None], bv[None], A_log, dt_bias)
+            o, _ = oracle.delta_step(q, k, v, g, beta, S, scale=K ** -0.5)
+        got_S = L[l]["state"][slot, hvs[0]:hvs[-1] + 1].cpu().numpy()
+        drift = max(drift, float(np.max(np.abs(got_S - S[0]) / np.maximum(1.0, np.abs(S[0])))))
+        got_o = L[l]["out"][b, 0, hvs[0]:hvs[-1] + 1].float().cpu().numpy()
+        out_err = max(out_err, float(np.max(np.abs(got_o - o[0]) / np.maximum(1.0, np.abs(o[0])))))
+        if verbose:
+            print(f"pair layer={l} slot={slot} heads={h0}..{h0 + heads_per_pair - 1}: drift so far {drift:.3g}")
+    return {"dec_ms_per_step": statistics.mean(dec_ms), "dec_ms_median": statistics.median(dec_ms),
+            "total_ms_per_step": total_ms / steps, "drift": drift, "last_out_err": out_err,
+            "picks": picks, "state_bytes_per_step": 2 * layers * B * HV * V * K * 4}
+
+
+def run_stack(args):
+    h = Harness(args)
+    import ssm_recurrent_decode_gb300 as gdn
+    gdn.lib()
+    layers, B, H, HV, K, V = args.layers, 256, 16, 48, 128, 128
+    steps = args.steps
+    res = stack_decode(layers, B, H, HV, K, V, steps=steps, device=h.dev, pairs=args.pairs)
+    ms = res["dec_ms_median"]
+    (ms,) = max_over_ranks([ms], h.world)
+    if h.rank != 0:
+        return h.finish(None)
+    state_bytes = res["state_bytes_per_step"]
+    gbs = h.world * state_bytes / (ms * 1e-3) / 1e9
+    line = base_line(
+        h, gbs, ms, steps, 1,
+        f"{layers}-layer stacked gdn decode under CUDA graphs: B={B} H={H} HV={HV} K=V={K}, an "
+        f"fp32 state pool per layer ({layers * B * HV * V * K * 4 / 1e9:.1f} GB), fresh device-drawn "
+        f"bf16 inputs every step", {"layers": layers, "B": B, "H": H, "HV": HV, "K": K, "V": V,
+                                     "state_bytes_per_step": state_bytes}, steps * layers)
+    line["per_layer_us"] = round(ms * 1e3 / layers, 3)
+    line["with_input_generation_ms_per_step"] = round(res["total_ms_per_step"], 4)
+    line["drift_vs_oracle"] = {"max_rel_state_err": res["drift"], "last_step_out_err": res["last_out_err"],
+                               "pairs": [list(p) for p in res["picks"]], "steps": steps,
+                               "bar": 1e-4}
+    line["roofline"] = roofline(state_bytes / layers + packed_io_bytes(B, H, HV, K, V),
+                                ms / layers, "step", f"packed_HV{HV}_B{B}")
+    return h.finish(line)
 
 
 def main(argv=None):
@@ -373,15 +657,21 @@ def main(argv=None):
     p.add_argument("--steps", type=int, default=10000)
     p.add_argument("--warmup", type=int, default=50)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=["packed"], default="packed")
+    p.add_argument("--workload", choices=["packed", "buffered", "fused", "stack"], default="packed")
     p.add_argument("--B", type=int, default=256)
+    p.add_argument("--L", type=int, default=16)
+    p.add_argument("--T", type=int, default=128)
+    p.add_argument("--layout", choices=["DS", "SD"], default="DS")
+    p.add_argument("--layers", type=int, default=48)
+    p.add_argument("--pairs", type=int, default=8)
     p.add_argument("--cpu-budget", type=float, default=10.0)
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
     if args.impl == "reference":
         return run_reference(args)
-    return run_packed(args)
+    return {"packed": run_packed, "buffered": run_buffered, "fused": run_fused,
+            "stack": run_stack}[args.workload](args)
 
 
 if __name__ == "__main__":
