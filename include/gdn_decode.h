@@ -66,6 +66,8 @@ typedef enum gdn_status {
 /* Bits OR-ed into *err_flags by the kernels. */
 #define GDN_DEVERR_BAD_INDEX 0x1      /* a slot index outside [0, num_slots) that is not the pad id */
 #define GDN_DEVERR_BAD_WRITE_POS 0x2  /* a ring cursor outside [0, L) */
+#define GDN_DEVERR_TIMEOUT 0x4        /* a bounded wait inside a pipelined kernel gave up; the CTA
+                                         stopped early and its remaining rows were not computed */
 
 /* Arguments of one decode step (all entry points but gdn_decode_fused). */
 typedef struct gdn_step_args {
@@ -105,7 +107,13 @@ typedef struct gdn_ring_args {
     void *k_cache;            /* [num_slots, H, L, K] normalised-key records */
     float *g_cache;           /* [num_slots, HV, L] log-decay records */
     const int32_t *write_pos; /* [B] cursor of each row, 0 <= write_pos[b] < L; read only */
+    int32_t kernel;           /* GDN_KERNEL_AUTO (0): the pipelined kernel when it applies, else the
+                                 per-tile kernel; GDN_KERNEL_TILE (1) / GDN_KERNEL_PIPE (2) force one
+                                 (PIPE needs K == V == 128 and 16-byte aligned rows: GDN_ERR_SHAPE or
+                                 GDN_ERR_ALIGN otherwise) */
 } gdn_ring_args;
+
+typedef enum gdn_kernel { GDN_KERNEL_AUTO = 0, GDN_KERNEL_TILE = 1, GDN_KERNEL_PIPE = 2 } gdn_kernel;
 
 typedef enum gdn_fused_gate {
     GDN_FUSED_GATE_KDA = 0,   /* one log-decay per key channel, bounded below by lower_bound */
@@ -200,7 +208,7 @@ const char *gdn_strerror(int status);
 /* ABI checks for bindings: sizeof of the args structs (which: 0 step, 1 ring, 2 fused). */
 size_t gdn_abi_struct_size(int which);
 
-/* Library ABI version (incremented on any change of the structs above). */
+/* Library ABI version (incremented on any change of the structs above; currently 2). */
 int gdn_abi_version(void);
 
 #ifdef __cplusplus

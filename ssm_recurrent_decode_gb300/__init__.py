@@ -25,15 +25,17 @@ __all__ = [
     "lib", "build", "GdnError", "GdnStepArgs", "GdnRingArgs", "GdnFusedArgs",
     "gdn_decode_step", "gdn_decode_step_indexed", "gdn_decode_buffered", "gdn_decode_fused",
     "gdn_strerror", "split_mixed_qkv", "fused_recurrent_gated_delta_rule_packed_decode",
-    "GDN_F32", "GDN_BF16", "GDN_DEVERR_BAD_INDEX", "GDN_DEVERR_BAD_WRITE_POS", "EXPORTS",
+    "GDN_F32", "GDN_BF16", "GDN_DEVERR_BAD_INDEX", "GDN_DEVERR_BAD_WRITE_POS", "GDN_DEVERR_TIMEOUT",
+    "EXPORTS",
 ]
 
 GDN_F32, GDN_BF16 = 0, 1
 GDN_GATE_RAW, GDN_GATE_DIRECT = 0, 1
 GDN_FUSED_GATE_KDA, GDN_FUSED_GATE_GDN = 0, 1
 GDN_ACT_SILU, GDN_ACT_SIGMOID = 0, 1
-GDN_DEVERR_BAD_INDEX, GDN_DEVERR_BAD_WRITE_POS = 0x1, 0x2
-ABI_VERSION = 1
+GDN_DEVERR_BAD_INDEX, GDN_DEVERR_BAD_WRITE_POS, GDN_DEVERR_TIMEOUT = 0x1, 0x2, 0x4
+GDN_KERNEL = {"auto": 0, "tile": 1, "pipe": 2}
+ABI_VERSION = 2
 
 # every function the header declares
 EXPORTS = ("gdn_decode_step", "gdn_decode_step_indexed", "gdn_decode_buffered", "gdn_decode_fused",
@@ -54,7 +56,7 @@ class GdnStepArgs(ctypes.Structure):
 
 class GdnRingArgs(ctypes.Structure):
     _fields_ = [("L", _i32), ("ring_dtype", _i32), ("d_cache", _vp), ("k_cache", _vp),
-                ("g_cache", _vp), ("write_pos", _vp)]
+                ("g_cache", _vp), ("write_pos", _vp), ("kernel", _i32)]
 
 
 class GdnFusedArgs(ctypes.Structure):
@@ -253,10 +255,12 @@ def gdn_decode_step_indexed(q, k, v, state, out, cache_indices, *, pad_slot_id=-
 def gdn_decode_buffered(q, k, v, state, out, d_cache, k_cache, g_cache, write_pos, *,
                         cache_indices=None, pad_slot_id=-1, H=None, a=None, b=None, A_log=None,
                         dt_bias=None, g=None, beta=None, scale=None, use_qk_l2norm=True,
-                        err_flags=None, stream=None):
+                        err_flags=None, kernel="auto", stream=None):
     """Buffered output-only decode. state holds the checkpoints; d_cache [num_slots, HV, L, V],
     k_cache [num_slots, H, L, K] (both fp32 or both bf16), g_cache [num_slots, HV, L] fp32;
-    write_pos int32 [B] is read, never advanced (the caller moves it to (p+1) % L)."""
+    write_pos int32 [B] is read, never advanced (the caller moves it to (p+1) % L).
+    kernel: "auto" (the persistent pipelined kernel when K == V == 128 and rows are 16-byte
+    aligned, else the per-tile kernel), "tile" or "pipe" to force one."""
     torch = _torch()
     s = _step_args(q, k, v, state, out, H=H, a=a, b=b, A_log=A_log, dt_bias=dt_bias, g=g,
                    beta=beta, scale=scale, use_qk_l2norm=use_qk_l2norm, err_flags=err_flags)
@@ -274,6 +278,7 @@ def gdn_decode_buffered(q, k, v, state, out, d_cache, k_cache, g_cache, write_po
     r.d_cache, r.k_cache = _ptr(d_cache, "d_cache"), _ptr(k_cache, "k_cache")
     r.g_cache = _ptr(g_cache, "g_cache", torch.float32)
     r.write_pos = _ptr(_dense(write_pos, "write_pos"), "write_pos", torch.int32)
+    r.kernel = GDN_KERNEL[kernel]
     idx = None if cache_indices is None else _ptr(_dense(cache_indices, "cache_indices"),
                                                   "cache_indices", torch.int32)
     _check("gdn_decode_buffered",

@@ -9,7 +9,7 @@
 
 namespace {
 
-constexpr int kAbiVersion = 1;
+constexpr int kAbiVersion = 2;
 
 bool k_supported(int K) { return K == 16 || K == 32 || K == 64 || K == 128; }
 bool dtype_ok(int d) { return d == GDN_F32 || d == GDN_BF16; }
@@ -90,13 +90,39 @@ int gdn_decode_buffered(const gdn_step_args *args, const int32_t *cache_indices,
     if (!aligned(ring->k_cache, 4 * dtype_size(ring->ring_dtype)) ||
         !aligned(ring->d_cache, dtype_size(ring->ring_dtype)) || !aligned(ring->g_cache, 4))
         return GDN_ERR_ALIGN;
-    if (gdn::buffered_smem_bytes(ring->L, args->V, args->K) > 200 * 1024) return GDN_ERR_SHAPE;
+    if (ring->kernel < GDN_KERNEL_AUTO || ring->kernel > GDN_KERNEL_PIPE) return GDN_ERR_ARG;
+    const bool tile_ok = gdn::buffered_smem_bytes(ring->L, args->V, args->K) <= 200 * 1024;
+    bool pipe_ok = args->K == 128 && args->V == 128;
+    const size_t es = dtype_size(args->in_dtype);
+    const bool pipe_aligned =
+        aligned(args->q, 16) && aligned(args->k, 16) && aligned(args->v, 16) &&
+        (args->q_stride * (int64_t)es) % 16 == 0 && (args->k_stride * (int64_t)es) % 16 == 0 &&
+        (args->v_stride * (int64_t)es) % 16 == 0 && aligned(ring->d_cache, 16) && aligned(ring->k_cache, 16);
+    if (pipe_ok) {
+        int dev = 0, max_smem = 0;
+        pipe_ok = cudaGetDevice(&dev) == cudaSuccess &&
+                  cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess &&
+                  gdn::buffered_pipe_fits(ring->L, args->in_dtype, ring->ring_dtype, max_smem);
+    }
+    bool use_pipe;
+    if (ring->kernel == GDN_KERNEL_PIPE) {
+        if (!pipe_ok) return GDN_ERR_SHAPE;
+        if (!pipe_aligned) return GDN_ERR_ALIGN;
+        use_pipe = true;
+    } else if (ring->kernel == GDN_KERNEL_TILE) {
+        if (!tile_ok) return GDN_ERR_SHAPE;
+        use_pipe = false;
+    } else {
+        use_pipe = pipe_ok && pipe_aligned;
+        if (!use_pipe && !tile_ok) return GDN_ERR_SHAPE;
+    }
     gdn::StepLaunch p = make_step(args, cache_indices, pad_slot_id);
     p.L = ring->L;
     p.d_cache = ring->d_cache;
     p.k_cache = ring->k_cache;
     p.g_cache = ring->g_cache;
     p.write_pos = ring->write_pos;
+    if (use_pipe) return gdn::launch_buffered_pipe(p, ring->ring_dtype, reinterpret_cast<cudaStream_t>(stream));
     return gdn::launch_buffered(p, ring->ring_dtype, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -1,0 +1,381 @@
+// buffered_pipe.cu -- the buffered, output-only decode as a persistent, warp-specialised kernel
+// for K = V = 128 (the shapes of every workload on the source pages).
+//
+// Same arithmetic as buffered_kernel.cu (low-rank replay of the ring records; the flush step at
+// write_pos == L-1 folds them into the checkpoint and writes it back), organised so that HBM
+// streams continuously:
+//   - one CTA per SM, 16 consumer warps and 1 producer warp;
+//   - the producer walks the CTA's tiles ahead of the consumers and, for each, moves the 64 KB
+//     checkpoint tile, the q/k/v rows and the tile's ring records (p delta rows, p key rows) into
+//     a shared-memory stage with 1-D bulk copies (cp.async.bulk) that complete on the stage's
+//     "full" mbarrier, and writes the tile's scalars (slot, cursor, gate inputs, the records'
+//     log-decays) beside them;
+//   - NST stages (2 or 3, as many as fit) keep up to NST tiles in flight per SM while the
+//     consumers compute, so the tile loads of the next tiles overlap the current tile's
+//     arithmetic and write-back;
+//   - consumers copy the tile from shared memory into registers (8 rows x 4 columns per lane),
+//     release the stage on its "empty" mbarrier once everything in it has been read, and write the
+//     flushed state from registers with streaming stores.
+// Every wait is bounded: a wait that runs past its limit sets GDN_DEVERR_TIMEOUT, raises a
+// CTA-wide abort flag and ends the CTA's loop; the producer then waits (bounded) for the copies
+// it issued, so no copy is in flight when the CTA exits.
+//
+// Source: "Microbenchmark: buffered output-only GDN decode (ReplaySSM Part A)" (module docstring,
+// _bench_cfg / run_replay); the step of "Optimization Log: Qwen3.5-27B Dense on B200", Kernel 4.
+#include "gdn_launch.h"
+#include "gdn_pipe.cuh"
+#include "gdn_tile.cuh"
+
+namespace gdn {
+
+constexpr int kPipeCW = 16;                           // consumer warps
+constexpr int kPipeThreads = (kPipeCW + 1) * 32;      // plus one producer warp
+constexpr int kPipeLMax = 64;
+constexpr long long kWaitLimit = 1LL << 31;           // SM clock cycles, about one second
+
+// Per-stage scalars: written by the producer (status .. gr), scratch of the consumers (c ..).
+struct PipeMeta {
+    int status;                 // 0 run, 1 pad row, 2 bad slot index, 3 bad cursor
+    int slot, p;
+    float ga, gb, A_log, dt_bias;   // raw a, b and the head's parameters (or g, beta direct)
+    float gr[kPipeLMax];        // log-decays of records j < p
+    float c[kPipeLMax];         // c_j = exp(g_{j+1} + ... + g_p)
+    float alpha[kPipeLMax];     // c_j (k_j . k)
+    float gamma[kPipeLMax];     // c_j (k_j . q)
+};
+
+__host__ __device__ inline uint32_t round16(uint32_t x) { return (x + 15u) & ~15u; }
+
+// Byte offsets inside one stage: S tile, q, k, v rows, delta records, key records, scalars.
+struct PipeLayout {
+    uint32_t q, k, v, d, kr, meta, stage;
+    __host__ __device__ PipeLayout(int L, uint32_t es, uint32_t rs)
+    {
+        q = 128u * 128u * 4u;
+        k = q + round16(128u * es);
+        v = k + round16(128u * es);
+        d = v + round16(128u * es);
+        kr = d + round16((uint32_t)(L - 1) * 128u * rs);
+        meta = kr + round16((uint32_t)(L - 1) * 128u * rs);
+        stage = (meta + (uint32_t)sizeof(PipeMeta) + 127u) & ~127u;
+    }
+};
+
+template <typename Tring> __device__ __forceinline__ Tring ring_out(float x);
+template <> __device__ __forceinline__ float ring_out<float>(float x) { return x; }
+template <> __device__ __forceinline__ bf16 ring_out<bf16>(float x) { return __float2bfloat16_rn(x); }
+
+__device__ __forceinline__ float ring_in(float x) { return x; }
+__device__ __forceinline__ float ring_in(bf16 x) { return __bfloat162float(x); }
+
+// eight consecutive ring values (one warp's rows) from shared memory
+__device__ __forceinline__ void load8(const float *p, float (&o)[8])
+{
+    const float4 a = *reinterpret_cast<const float4 *>(p), b = *reinterpret_cast<const float4 *>(p + 4);
+    o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w; o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+}
+__device__ __forceinline__ void load8(const bf16 *p, float (&o)[8])
+{
+    const uint4 r = *reinterpret_cast<const uint4 *>(p);
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        o[2 * i] = __uint_as_float(w[i] << 16);
+        o[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+template <typename Tin, typename Tring>
+__global__ void __launch_bounds__(kPipeThreads, 1) buffered_pipe_kernel(const __grid_constant__ StepLaunch P)
+{
+    constexpr int K = 128, V = 128;
+    using TL = Tile<128, 8, kPipeCW>;
+    extern __shared__ __align__(128) unsigned char sm[];
+    __shared__ int abort_flag;
+    __shared__ int zero_flag;
+
+    const gdn_step_args &a = P.a;
+    const int HV = a.HV, L = P.L, NST = P.nst, G = P.G;
+    const int ntiles = a.B * HV;
+    const PipeLayout lay(L, sizeof(Tin), sizeof(Tring));
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + (size_t)NST * lay.stage);
+    uint64_t *empty = full + NST;
+    uint64_t *scr = empty + NST;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(&full[s], 32);
+            mbar_init(&empty[s], kPipeCW);
+            mbar_init(&scr[s], kPipeCW);
+        }
+        abort_flag = 0;
+        zero_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == kPipeCW) {
+        // ---------------------------------------------------------------- producer warp
+        const uint64_t pol = policy_evict_first();
+        int n = 0;
+        for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++n) {
+            const int st = n % NST;
+            const uint32_t ph = (uint32_t)(n / NST) & 1u;
+            if (n >= NST && !mbar_wait(&empty[st], ph ^ 1u, &abort_flag, kWaitLimit)) {
+                if (lane == 0) {
+                    *(volatile int *)&abort_flag = 1;
+                    raise_flag(a.err_flags, GDN_DEVERR_TIMEOUT);
+                }
+                break;
+            }
+            unsigned char *stage = sm + (size_t)st * lay.stage;
+            PipeMeta *meta = reinterpret_cast<PipeMeta *>(stage + lay.meta);
+            const int b = tile / HV, hv = tile - b * HV, h = hv / G;
+            int slot = b, status = 0;
+            if (P.idx) {
+                slot = P.idx[b];
+                if (slot == P.pad) status = 1;
+                else if (slot < 0 || slot >= a.num_slots) status = 2;
+            }
+            int p = P.write_pos[b];
+            if (status == 0 && (p < 0 || p >= L)) status = 3;
+            if (status != 0) p = 0;
+            const float *gring = P.g_cache + ((size_t)slot * HV + hv) * L;
+            for (int j = lane; j < p; j += 32) meta->gr[j] = gring[j];
+            if (lane == 0) {
+                meta->status = status;
+                meta->slot = slot;
+                meta->p = p;
+                if (status == 0) {
+                    const size_t gi = (size_t)b * HV + hv;
+                    if (a.gate_mode == GDN_GATE_RAW) {
+                        meta->ga = to_f32(static_cast<const Tin *>(a.a)[gi]);
+                        meta->gb = to_f32(static_cast<const Tin *>(a.b)[gi]);
+                        meta->A_log = a.A_log[hv];
+                        meta->dt_bias = a.dt_bias[hv];
+                    } else {
+                        meta->ga = a.g[gi];
+                        meta->gb = a.beta[gi];
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) {
+                const uint32_t es = sizeof(Tin), rs = sizeof(Tring);
+                const uint32_t bytes = status == 0 ? 128u * 128u * 4u + 3u * 128u * es + 2u * (uint32_t)p * 128u * rs : 0u;
+                fence_proxy_async();
+                mbar_arrive_expect_tx(&full[st], bytes);
+                if (status == 0) {
+                    const float *S = a.state + ((size_t)slot * HV + hv) * (size_t)(V * K);
+                    bulk_g2s_hint(stage, S, 128u * 128u * 4u, &full[st], pol);
+                    bulk_g2s(stage + lay.q, static_cast<const Tin *>(a.q) + (size_t)b * a.q_stride + (size_t)h * K, 128u * es, &full[st]);
+                    bulk_g2s(stage + lay.k, static_cast<const Tin *>(a.k) + (size_t)b * a.k_stride + (size_t)h * K, 128u * es, &full[st]);
+                    bulk_g2s(stage + lay.v, static_cast<const Tin *>(a.v) + (size_t)b * a.v_stride + (size_t)hv * V, 128u * es, &full[st]);
+                    if (p > 0) {
+                        const Tring *dr = static_cast<const Tring *>(P.d_cache) + ((size_t)slot * HV + hv) * L * V;
+                        const Tring *kr = static_cast<const Tring *>(P.k_cache) + ((size_t)slot * a.H + h) * L * K;
+                        bulk_g2s(stage + lay.d, dr, (uint32_t)p * 128u * rs, &full[st]);
+                        bulk_g2s(stage + lay.kr, kr, (uint32_t)p * 128u * rs, &full[st]);
+                    }
+                }
+            } else {
+                mbar_arrive(&full[st]);
+            }
+        }
+        if (*(volatile int *)&abort_flag) {
+            // let every copy issued for the stages still in flight land before the CTA exits
+            for (int back = 1; back <= NST && n - back >= 0; ++back) {
+                const int m = n - back;
+                mbar_wait(&full[m % NST], (uint32_t)(m / NST) & 1u, &zero_flag, kWaitLimit);
+            }
+        }
+        return;
+    }
+
+    // -------------------------------------------------------------------- consumer warps
+    TL t;
+    t.init(warp);
+    const int tid = threadIdx.x;   // 0 .. 511
+    int n = 0;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++n) {
+        const int st = n % NST;
+        const uint32_t ph = (uint32_t)(n / NST) & 1u;
+        if (!mbar_wait(&full[st], ph, &abort_flag, kWaitLimit)) {
+            if (lane == 0) {
+                *(volatile int *)&abort_flag = 1;
+                raise_flag(a.err_flags, GDN_DEVERR_TIMEOUT);
+            }
+            break;
+        }
+        const unsigned char *stage = sm + (size_t)st * lay.stage;
+        PipeMeta *meta = reinterpret_cast<PipeMeta *>(sm + (size_t)st * lay.stage + lay.meta);
+        const int status = meta->status, slot = meta->slot, p = meta->p;
+        const int b = tile / HV, hv = tile - b * HV;
+        const size_t out_base = ((size_t)b * HV + hv) * V;
+        if (status != 0) {
+            if (status >= 2 && tid == 0)
+                raise_flag(a.err_flags, status == 2 ? GDN_DEVERR_BAD_INDEX : GDN_DEVERR_BAD_WRITE_POS);
+            if (tid < V) store_out(a.out, a.out_dtype, out_base + tid, 0.f);
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&scr[st]);
+                mbar_arrive(&empty[st]);
+            }
+            continue;
+        }
+        const bool flush = p == L - 1;
+        const Tin *qs = reinterpret_cast<const Tin *>(stage + lay.q);
+        const Tin *ks = reinterpret_cast<const Tin *>(stage + lay.k);
+        const Tin *vs = reinterpret_cast<const Tin *>(stage + lay.v);
+        const Tring *ds = reinterpret_cast<const Tring *>(stage + lay.d);
+        const Tring *krs = reinterpret_cast<const Tring *>(stage + lay.kr);
+        const float *Ss = reinterpret_cast<const float *>(stage);
+
+        const float4 kh = l2_normalise4<32>(load4(ks + t.col), a.use_qk_l2norm != 0, 1.f);
+        const float4 qh = l2_normalise4<32>(load4(qs + t.col), a.use_qk_l2norm != 0, P.scale);
+        const float kq = group_sum<32>(dot4(kh, qh));
+        float g, beta;
+        if (a.gate_mode == GDN_GATE_RAW) {
+            g = -expf(meta->A_log) * softplus_f(meta->ga + meta->dt_bias);
+            beta = sigmoid_f(meta->gb);
+        } else {
+            g = meta->ga;
+            beta = meta->gb;
+        }
+        // record scalars, one warp per record
+        for (int j = warp; j < p; j += kPipeCW) {
+            const float4 kj = load4(krs + (size_t)j * K + t.col);
+            const float dk = group_sum<32>(dot4(kj, kh));
+            const float dq = group_sum<32>(dot4(kj, qh));
+            if (lane == 0) {
+                float acc = g;
+                for (int i = j + 1; i < p; ++i) acc += meta->gr[i];
+                const float c = expf(acc);
+                meta->c[j] = c;
+                meta->alpha[j] = c * dk;
+                meta->gamma[j] = c * dq;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&scr[st]);
+
+        float gsum = g;
+        for (int i = 0; i < p; ++i) gsum += meta->gr[i];
+        const float Gam = expf(gsum);
+
+        // tile into registers, the two dots
+#pragma unroll
+        for (int i = 0; i < TL::R; ++i)
+            t.s[i] = *reinterpret_cast<const float4 *>(Ss + (size_t)t.row(0, i) * K + t.col);
+        const int r_own = t.row(0, t.owned_chunk(0));
+        const float vv = t.holds_k_dot() ? to_f32(vs[r_own]) : 0.f;
+        float x[TL::N];
+        t.partial_dots(scale4(kh, Gam), scale4(qh, Gam), x);
+        t.reduce_scatter(x);
+
+        if (!mbar_wait(&scr[st], ph, &abort_flag, kWaitLimit)) {
+            if (lane == 0) {
+                *(volatile int *)&abort_flag = 1;
+                raise_flag(a.err_flags, GDN_DEVERR_TIMEOUT);
+            }
+            break;
+        }
+        // ring corrections: lower lanes on u, upper lanes on o
+        {
+            const float *coef = t.holds_k_dot() ? meta->alpha : meta->gamma;
+            float acc = x[0];
+            for (int j = 0; j < p; ++j) acc = fmaf(ring_in(ds[(size_t)j * V + r_own]), coef[j], acc);
+            x[0] = acc;
+        }
+        float dv[TL::M];
+        dv[0] = beta * (vv - x[0]);
+        const float dq = t.delta_for_q(dv[0]);
+        Tring *dring = static_cast<Tring *>(P.d_cache) + ((size_t)slot * HV + hv) * L * V;
+        if (t.writer()) {
+            if (t.holds_k_dot())
+                dring[(size_t)p * V + r_own] = ring_out<Tring>(dv[0]);
+            else
+                store_out(a.out, a.out_dtype, out_base + r_own, fmaf(dq, kq, x[0]));
+        }
+        if (flush) {
+#pragma unroll
+            for (int i = 0; i < TL::R; ++i) t.s[i] = axpby4(Gam, t.s[i], t.delta_of(dv, i), kh);
+            const int row0 = t.row(0, 0);   // this warp's 8 consecutive rows
+            for (int j = 0; j < p; ++j) {
+                const float cj = meta->c[j];
+                const float4 kj = scale4(load4(krs + (size_t)j * K + t.col), cj);
+                float dj[8];
+                load8(ds + (size_t)j * V + row0, dj);
+#pragma unroll
+                for (int i = 0; i < TL::R; ++i) {
+                    t.s[i].x = fmaf(dj[i], kj.x, t.s[i].x);
+                    t.s[i].y = fmaf(dj[i], kj.y, t.s[i].y);
+                    t.s[i].z = fmaf(dj[i], kj.z, t.s[i].z);
+                    t.s[i].w = fmaf(dj[i], kj.w, t.s[i].w);
+                }
+            }
+        }
+        // everything of this stage has been read
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+
+        if (flush) {
+            float *S = a.state + ((size_t)slot * HV + hv) * (size_t)(V * K);
+#pragma unroll
+            for (int i = 0; i < TL::R; ++i) st_stream(S + (size_t)t.row(0, i) * K + t.col, t.s[i]);
+        }
+        // this step's key record (first value head of the group) and log-decay record
+        if (hv % G == 0 && warp == 0) {
+            Tring *dst = static_cast<Tring *>(P.k_cache) + (((size_t)slot * a.H + hv / G) * L + p) * K + t.col;
+            dst[0] = ring_out<Tring>(kh.x);
+            dst[1] = ring_out<Tring>(kh.y);
+            dst[2] = ring_out<Tring>(kh.z);
+            dst[3] = ring_out<Tring>(kh.w);
+        }
+        if (tid == 0) P.g_cache[((size_t)slot * HV + hv) * L + p] = g;
+    }
+}
+
+// dynamic shared memory of the pipelined kernel for NST stages
+static size_t pipe_smem(const PipeLayout &lay, int nst) { return (size_t)nst * lay.stage + 3 * nst * sizeof(uint64_t); }
+
+template <typename Tin, typename Tring>
+static int launch_pipe_t(const StepLaunch &p0, cudaStream_t stream)
+{
+    StepLaunch p = p0;
+    const PipeLayout lay(p.L, sizeof(Tin), sizeof(Tring));
+    int dev = 0, sms = 0, max_smem = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        return GDN_ERR_LAUNCH;
+    const size_t budget = (size_t)max_smem - 1024;   // room for the kernel's static shared memory
+    int nst = 3;
+    while (nst >= 2 && pipe_smem(lay, nst) > budget) --nst;
+    if (nst < 2) return GDN_ERR_SHAPE;
+    p.nst = nst;
+    const size_t smem = pipe_smem(lay, nst);
+    auto kern = buffered_pipe_kernel<Tin, Tring>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return GDN_ERR_LAUNCH;
+    const int tiles = p.a.B * p.a.HV;
+    const int grid = tiles < sms ? tiles : sms;
+    kern<<<grid, kPipeThreads, smem, stream>>>(p);
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
+}
+
+bool buffered_pipe_fits(int L, int in_dtype, int ring_dtype, int max_smem)
+{
+    const PipeLayout lay(L, in_dtype == GDN_BF16 ? 2 : 4, ring_dtype == GDN_BF16 ? 2 : 4);
+    return pipe_smem(lay, 2) + 1024 <= (size_t)max_smem;
+}
+
+int launch_buffered_pipe(const StepLaunch &p, int ring_dtype, cudaStream_t stream)
+{
+    if (p.a.in_dtype == GDN_BF16)
+        return ring_dtype == GDN_BF16 ? launch_pipe_t<bf16, bf16>(p, stream) : launch_pipe_t<bf16, float>(p, stream);
+    return ring_dtype == GDN_BF16 ? launch_pipe_t<float, bf16>(p, stream) : launch_pipe_t<float, float>(p, stream);
+}
+
+}  // namespace gdn

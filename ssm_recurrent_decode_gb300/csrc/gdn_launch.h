@@ -22,6 +22,7 @@ struct StepLaunch {
     void *k_cache;
     float *g_cache;
     const int32_t *write_pos;
+    int32_t nst;              // pipelined kernel: shared-memory stages
 };
 
 struct FusedLaunch {
@@ -37,5 +38,10 @@ int launch_fused(const FusedLaunch &p, cudaStream_t stream);
 
 // Dynamic shared memory the buffered kernel needs for ring length L, value dim V and key dim K.
 size_t buffered_smem_bytes(int L, int V, int K);
+
+// The persistent, warp-specialised buffered kernel (K = V = 128, 16-byte aligned rows).
+int launch_buffered_pipe(const StepLaunch &p, int ring_dtype, cudaStream_t stream);
+// Whether its two-stage shared-memory footprint fits in max_smem bytes per CTA.
+bool buffered_pipe_fits(int L, int in_dtype, int ring_dtype, int max_smem);
 
 }  // namespace gdn

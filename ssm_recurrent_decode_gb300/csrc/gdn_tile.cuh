@@ -26,25 +26,26 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
-template <int K>
+template <int K, int R_ = 16, int NW = kWarps>
 struct Tile {
     static_assert(K == 16 || K == 32 || K == 64 || K == 128, "K must be 16, 32, 64 or 128");
     static constexpr int LPR = K / 4;               // lanes per state row
     static constexpr int RPI = 32 / LPR;            // rows per warp instruction
-    static constexpr int R = 16;                    // 16-byte vectors per thread per pass
+    static constexpr int R = R_;                    // 16-byte vectors per thread per pass
     static constexpr int N = 2 * R;                 // partial dots per thread (R for S.k, R for S.q)
-    static constexpr int M = N / LPR;               // fully reduced dots per lane
+    static constexpr int DUP = N >= LPR ? 1 : LPR / N;  // lanes left holding the same reduced dot
+    static constexpr int M = N >= LPR ? N / LPR : 1;    // fully reduced dots per lane
     static constexpr int HALF = LPR / 2;            // lanes [0, HALF) of a row group end with S.k
     static constexpr int ROWS_WARP = R * RPI;
-    static constexpr int ROWS_PASS = kWarps * ROWS_WARP;
+    static constexpr int ROWS_PASS = NW * ROWS_WARP;
 
     int lane, warp, sub, grp, col;
     float4 s[R];
 
-    __device__ __forceinline__ void init()
+    __device__ __forceinline__ void init(int warp_index = threadIdx.x >> 5)
     {
         lane = threadIdx.x & 31;
-        warp = threadIdx.x >> 5;
+        warp = warp_index;
         sub = lane % LPR;
         grp = lane / LPR;
         col = sub * 4;
@@ -57,8 +58,10 @@ struct Tile {
     }
 
     // chunk index whose reduced dot this lane holds in slot m (see reduce_scatter)
-    __device__ __forceinline__ int owned_chunk(int m) const { return (sub % HALF) * M + m; }
+    __device__ __forceinline__ int owned_chunk(int m) const { return ((sub % HALF) / DUP) * M + m; }
     __device__ __forceinline__ bool holds_k_dot() const { return sub < HALF; }
+    // one lane of each group of DUP identical lanes writes the row's results
+    __device__ __forceinline__ bool writer() const { return (sub % DUP) == 0; }
 
     __device__ __forceinline__ void load(const float *tile, int V, int row0)
     {
@@ -80,27 +83,38 @@ struct Tile {
     }
 
     // Butterfly reduce-scatter over the LPR lanes of a row group: at offset o a lane keeps one
-    // half of its values and adds the partner's copy of that half. After log2(LPR) steps lane
-    // `sub` holds the complete sums of indices sub*M .. sub*M + M-1 in x[0 .. M). That is
-    // N - N/LPR shuffles per lane instead of N * log2(LPR) for N separate reductions.
-    __device__ __forceinline__ void reduce_scatter(float (&x)[N]) const
+    // half of its values and adds the partner's copy of that half. After the halving steps lane
+    // `sub` holds the complete sums of indices (sub/DUP)*M .. (sub/DUP)*M + M-1 in x[0 .. M);
+    // when there are fewer values than lanes (DUP > 1) the last steps are plain butterflies and
+    // DUP neighbouring lanes end with the same sums. That is about N shuffles per lane instead of
+    // N * log2(LPR) for N separate reductions.
+    __device__ __forceinline__ void reduce_scatter(float (&x)[N]) const { rs_step<LPR / 2, N>(x); }
+
+    // one butterfly step at lane offset O with NN live values (compile-time, fully unrolled)
+    template <int O, int NN>
+    __device__ __forceinline__ void rs_step(float (&x)[N]) const
     {
+        if constexpr (O >= 1) {
+            if constexpr (NN > 1) {
+                const bool upper = (lane & O) != 0;
 #pragma unroll
-        for (int o = LPR / 2, n = N; o >= 1; o >>= 1, n >>= 1) {
-            const bool upper = (lane & o) != 0;
-#pragma unroll
-            for (int j = 0; j < n / 2; ++j) {
-                const float send = upper ? x[j] : x[j + n / 2];
-                const float keep = upper ? x[j + n / 2] : x[j];
-                x[j] = keep + __shfl_xor_sync(kFull, send, o);
+                for (int j = 0; j < NN / 2; ++j) {
+                    const float send = upper ? x[j] : x[j + NN / 2];
+                    const float keep = upper ? x[j + NN / 2] : x[j];
+                    x[j] = keep + __shfl_xor_sync(kFull, send, O);
+                }
+                rs_step<O / 2, NN / 2>(x);
+            } else {
+                x[0] += __shfl_xor_sync(kFull, x[0], O);
+                rs_step<O / 2, 1>(x);
             }
         }
     }
 
-    // delta of chunk i (the value sits on lane grp*LPR + i/M, slot i%M)
+    // delta of chunk i (the value sits on lane grp*LPR + (i/M)*DUP, slot i%M)
     __device__ __forceinline__ float delta_of(const float (&dv)[M], int i) const
     {
-        return __shfl_sync(kFull, dv[i % M], (lane & ~(LPR - 1)) + i / M);
+        return __shfl_sync(kFull, dv[i % M], (lane & ~(LPR - 1)) + (i / M) * DUP);
     }
 
     // upper lanes receive the delta of the lower lane that owns the same chunk

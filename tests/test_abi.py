@@ -119,6 +119,10 @@ def test_buffered_ring_checks():
     assert L.gdn_decode_buffered(ctypes.byref(s), None, -1, None, None) == -1
     r.ring_dtype = 3
     assert L.gdn_decode_buffered(ctypes.byref(s), None, -1, ctypes.byref(r), None) == -3
+    r.ring_dtype = gdn.GDN_BF16
+    r.d_cache, r.k_cache, r.g_cache, r.write_pos = (1 << 41), (1 << 42), (1 << 43), (1 << 44)
+    r.kernel = 7
+    assert L.gdn_decode_buffered(ctypes.byref(s), None, -1, ctypes.byref(r), None) == -6
 
 
 def test_fused_checks():

@@ -24,7 +24,7 @@ def _cuda():
 
 
 def _run_buffered(B, H, HV, K, V, L, dtype, ring, seed, steps, *, start_pos=None, indexed=False,
-                  out_dtype=None, pad_rows=()):
+                  out_dtype=None, pad_rows=(), kernel="auto"):
     out_dtype = out_dtype or dtype
     num_slots = B + 2 if indexed else B
     S64 = host_state(num_slots, HV, V, K, seed)
@@ -50,7 +50,8 @@ def _run_buffered(B, H, HV, K, V, L, dtype, ring, seed, steps, *, start_pos=None
         q, k, v = c.views()
         gdn.gdn_decode_buffered(q, k, v, state, out, d_cache, k_cache, g_cache,
                                 torch.from_numpy(wp).cuda(), cache_indices=idx, pad_slot_id=-1,
-                                H=H, a=c.a, b=c.b, A_log=c.A_log, dt_bias=c.dt_bias, err_flags=err)
+                                H=H, a=c.a, b=c.b, A_log=c.A_log, dt_bias=c.dt_bias, err_flags=err,
+                                kernel=kernel)
         mixed, a, b, A_log, dt_bias = c.oracle_args()
         qo, ko, vo = oracle.split_packed(mixed, H, HV, K, V)
         g, beta = oracle.gdn_gates(a, b, A_log, dt_bias)
@@ -77,22 +78,40 @@ def test_exact_ring_tiny_two_cycles(L):
     assert max(w.values()) <= 1e-5, w
 
 
-@pytest.mark.parametrize("K,G", [(32, 1), (64, 3), (128, 2)])
-def test_exact_ring_shapes_mixed_phases(K, G):
+@pytest.mark.parametrize("K,G,kernel", [(32, 1, "auto"), (64, 3, "auto"), (128, 2, "tile"),
+                                        (128, 2, "pipe"), (128, 3, "pipe")])
+def test_exact_ring_shapes_mixed_phases(K, G, kernel):
     """Rows at different cursors in one call (each row's own phase), records of one q/k head
-    shared by G value heads."""
+    shared by G value heads; at K = V = 128 both the per-tile and the pipelined kernel."""
     H = 2
     w = _run_buffered(3, H, H * G, K, K, 5, "f32", "f32", seed=K + G, steps=7, start_pos=[0, 2, 4],
-                      indexed=True)
+                      indexed=True, kernel=kernel)
     assert max(w.values()) <= 1e-5, w
 
 
+@pytest.mark.parametrize("kernel", ["tile", "pipe"])
 @pytest.mark.parametrize("L", [8, 16])
-def test_bf16_ring_packed_shapes(L):
+def test_bf16_ring_packed_shapes(L, kernel):
     """The packed decode shapes (H=16, HV=32, K=V=128) with bf16 inputs, outputs and records over
     one full cycle plus one step."""
-    w = _run_buffered(4, 16, 32, 128, 128, L, "bf16", "bf16", seed=50 + L, steps=L + 1, indexed=True)
+    w = _run_buffered(4, 16, 32, 128, 128, L, "bf16", "bf16", seed=50 + L, steps=L + 1, indexed=True,
+                      kernel=kernel)
     assert w["out"] <= 2e-2 and w["state"] <= 2e-2 and w["ring"] <= 2e-2, w
+
+
+def test_pipelined_kernel_many_tiles_per_cta():
+    """1536 tiles: every CTA of the persistent kernel walks about ten tiles through its
+    shared-memory stages, with rows at mixed cursors and a pad row."""
+    B = 48
+    w = _run_buffered(B, 16, 32, 128, 128, 8, "bf16", "bf16", seed=91, steps=9, indexed=True,
+                      start_pos=[(3 * r) % 8 for r in range(B)], pad_rows=(5,), kernel="pipe")
+    assert w["out"] <= 2e-2 and w["state"] <= 2e-2 and w["ring"] <= 2e-2, w
+
+
+def test_pipelined_kernel_exact_ring_fp32_inputs():
+    w = _run_buffered(6, 4, 8, 128, 128, 4, "f32", "f32", seed=92, steps=9, indexed=True,
+                      start_pos=[0, 1, 2, 3, 0, 1], kernel="pipe")
+    assert max(w.values()) <= 1e-5, w
 
 
 def test_pad_rows_are_skipped():
