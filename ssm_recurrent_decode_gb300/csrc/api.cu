@@ -92,12 +92,13 @@ int gdn_decode_buffered(const gdn_step_args *args, const int32_t *cache_indices,
         return GDN_ERR_ALIGN;
     if (ring->kernel < GDN_KERNEL_AUTO || ring->kernel > GDN_KERNEL_PIPE) return GDN_ERR_ARG;
     const bool tile_ok = gdn::buffered_smem_bytes(ring->L, args->V, args->K) <= 200 * 1024;
-    bool pipe_ok = args->K == 128 && args->V == 128;
+    bool pipe_ok = args->K == 128 && args->V == 128 && (ring->L == 1 || ring->L % 4 == 0);
     const size_t es = dtype_size(args->in_dtype);
     const bool pipe_aligned =
         aligned(args->q, 16) && aligned(args->k, 16) && aligned(args->v, 16) &&
         (args->q_stride * (int64_t)es) % 16 == 0 && (args->k_stride * (int64_t)es) % 16 == 0 &&
-        (args->v_stride * (int64_t)es) % 16 == 0 && aligned(ring->d_cache, 16) && aligned(ring->k_cache, 16);
+        (args->v_stride * (int64_t)es) % 16 == 0 && aligned(ring->d_cache, 16) && aligned(ring->k_cache, 16) &&
+        aligned(ring->g_cache, 16);
     if (pipe_ok) {
         int dev = 0, max_smem = 0;
         pipe_ok = cudaGetDevice(&dev) == cudaSuccess &&

@@ -33,12 +33,13 @@ constexpr int kPipeThreads = (kPipeCW + 1) * 32;      // plus one producer warp
 constexpr int kPipeLMax = 64;
 constexpr long long kWaitLimit = 1LL << 31;           // SM clock cycles, about one second
 
-// Per-stage scalars: written by the producer (status .. gr), scratch of the consumers (c ..).
+// Per-stage scalars. gr is filled by a bulk copy of the tile's log-decay records (first, so that
+// it is 16-byte aligned); status .. beta by the producer; c, alpha, gamma are consumer scratch.
 struct PipeMeta {
+    float gr[kPipeLMax];        // log-decays of records j < p
     int status;                 // 0 run, 1 pad row, 2 bad slot index, 3 bad cursor
     int slot, p;
-    float ga, gb, A_log, dt_bias;   // raw a, b and the head's parameters (or g, beta direct)
-    float gr[kPipeLMax];        // log-decays of records j < p
+    float g, beta;              // this step's log-decay and beta
     float c[kPipeLMax];         // c_j = exp(g_{j+1} + ... + g_p)
     float alpha[kPipeLMax];     // c_j (k_j . k)
     float gamma[kPipeLMax];     // c_j (k_j . q)
@@ -117,56 +118,67 @@ __global__ void __launch_bounds__(kPipeThreads, 1) buffered_pipe_kernel(const __
 
     if (warp == kPipeCW) {
         // ---------------------------------------------------------------- producer warp
+        // Tile scalars are fetched 32 tiles at a time (lane i for the i-th next tile), so the
+        // producer pays one global round trip per 32 tiles; per tile it only waits for a free
+        // stage, writes the scalars and issues the bulk copies.
         const uint64_t pol = policy_evict_first();
+        const uint32_t es = sizeof(Tin), rs = sizeof(Tring);
         int n = 0;
-        for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++n) {
-            const int st = n % NST;
-            const uint32_t ph = (uint32_t)(n / NST) & 1u;
-            if (n >= NST && !mbar_wait(&empty[st], ph ^ 1u, &abort_flag, kWaitLimit)) {
-                if (lane == 0) {
-                    *(volatile int *)&abort_flag = 1;
-                    raise_flag(a.err_flags, GDN_DEVERR_TIMEOUT);
+        bool stop = false;
+        for (int base = blockIdx.x; base < ntiles && !stop; base += 32 * gridDim.x) {
+            const int my_tile = base + lane * gridDim.x;
+            int my_slot = 0, my_status = 1, my_p = 0;
+            float my_g = 0.f, my_beta = 0.f;
+            if (my_tile < ntiles) {
+                const int b = my_tile / HV, hv = my_tile - b * HV;
+                my_slot = b;
+                my_status = 0;
+                if (P.idx) {
+                    my_slot = P.idx[b];
+                    if (my_slot == P.pad) my_status = 1;
+                    else if (my_slot < 0 || my_slot >= a.num_slots) my_status = 2;
                 }
-                break;
+                my_p = P.write_pos[b];
+                if (my_status == 0 && (my_p < 0 || my_p >= L)) my_status = 3;
+                if (my_status != 0) my_p = 0;
+                step_gates<Tin>(a, b, hv, my_g, my_beta);
             }
-            unsigned char *stage = sm + (size_t)st * lay.stage;
-            PipeMeta *meta = reinterpret_cast<PipeMeta *>(stage + lay.meta);
-            const int b = tile / HV, hv = tile - b * HV, h = hv / G;
-            int slot = b, status = 0;
-            if (P.idx) {
-                slot = P.idx[b];
-                if (slot == P.pad) status = 1;
-                else if (slot < 0 || slot >= a.num_slots) status = 2;
-            }
-            int p = P.write_pos[b];
-            if (status == 0 && (p < 0 || p >= L)) status = 3;
-            if (status != 0) p = 0;
-            const float *gring = P.g_cache + ((size_t)slot * HV + hv) * L;
-            for (int j = lane; j < p; j += 32) meta->gr[j] = gring[j];
-            if (lane == 0) {
+            for (int i = 0; i < 32; ++i) {
+                const int tile = base + i * gridDim.x;
+                if (tile >= ntiles) break;
+                const int st = n % NST;
+                const uint32_t ph = (uint32_t)(n / NST) & 1u;
+                if (n >= NST && !mbar_wait(&empty[st], ph ^ 1u, &abort_flag, kWaitLimit)) {
+                    if (lane == 0) {
+                        *(volatile int *)&abort_flag = 1;
+                        raise_flag(a.err_flags, GDN_DEVERR_TIMEOUT);
+                    }
+                    stop = true;
+                    break;
+                }
+                const int slot = __shfl_sync(kFull, my_slot, i);
+                const int status = __shfl_sync(kFull, my_status, i);
+                const int p = __shfl_sync(kFull, my_p, i);
+                const float g = __shfl_sync(kFull, my_g, i);
+                const float beta = __shfl_sync(kFull, my_beta, i);
+                ++n;
+                if (lane != 0) {
+                    mbar_arrive(&full[st]);
+                    continue;
+                }
+                unsigned char *stage = sm + (size_t)st * lay.stage;
+                PipeMeta *meta = reinterpret_cast<PipeMeta *>(stage + lay.meta);
                 meta->status = status;
                 meta->slot = slot;
                 meta->p = p;
-                if (status == 0) {
-                    const size_t gi = (size_t)b * HV + hv;
-                    if (a.gate_mode == GDN_GATE_RAW) {
-                        meta->ga = to_f32(static_cast<const Tin *>(a.a)[gi]);
-                        meta->gb = to_f32(static_cast<const Tin *>(a.b)[gi]);
-                        meta->A_log = a.A_log[hv];
-                        meta->dt_bias = a.dt_bias[hv];
-                    } else {
-                        meta->ga = a.g[gi];
-                        meta->gb = a.beta[gi];
-                    }
-                }
-            }
-            __syncwarp();
-            if (lane == 0) {
-                const uint32_t es = sizeof(Tin), rs = sizeof(Tring);
-                const uint32_t bytes = status == 0 ? 128u * 128u * 4u + 3u * 128u * es + 2u * (uint32_t)p * 128u * rs : 0u;
+                meta->g = g;
+                meta->beta = beta;
+                const uint32_t gbytes = p > 0 ? round16((uint32_t)p * 4u) : 0u;
+                const uint32_t bytes = status == 0 ? 128u * 128u * 4u + 3u * 128u * es + 2u * (uint32_t)p * 128u * rs + gbytes : 0u;
                 fence_proxy_async();
                 mbar_arrive_expect_tx(&full[st], bytes);
                 if (status == 0) {
+                    const int b = tile / HV, hv = tile - b * HV, h = hv / G;
                     const float *S = a.state + ((size_t)slot * HV + hv) * (size_t)(V * K);
                     bulk_g2s_hint(stage, S, 128u * 128u * 4u, &full[st], pol);
                     bulk_g2s(stage + lay.q, static_cast<const Tin *>(a.q) + (size_t)b * a.q_stride + (size_t)h * K, 128u * es, &full[st]);
@@ -177,10 +189,9 @@ __global__ void __launch_bounds__(kPipeThreads, 1) buffered_pipe_kernel(const __
                         const Tring *kr = static_cast<const Tring *>(P.k_cache) + ((size_t)slot * a.H + h) * L * K;
                         bulk_g2s(stage + lay.d, dr, (uint32_t)p * 128u * rs, &full[st]);
                         bulk_g2s(stage + lay.kr, kr, (uint32_t)p * 128u * rs, &full[st]);
+                        bulk_g2s(meta->gr, P.g_cache + ((size_t)slot * HV + hv) * L, gbytes, &full[st]);
                     }
                 }
-            } else {
-                mbar_arrive(&full[st]);
             }
         }
         if (*(volatile int *)&abort_flag) {
@@ -235,14 +246,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1) buffered_pipe_kernel(const __
         const float4 kh = l2_normalise4<32>(load4(ks + t.col), a.use_qk_l2norm != 0, 1.f);
         const float4 qh = l2_normalise4<32>(load4(qs + t.col), a.use_qk_l2norm != 0, P.scale);
         const float kq = group_sum<32>(dot4(kh, qh));
-        float g, beta;
-        if (a.gate_mode == GDN_GATE_RAW) {
-            g = -expf(meta->A_log) * softplus_f(meta->ga + meta->dt_bias);
-            beta = sigmoid_f(meta->gb);
-        } else {
-            g = meta->ga;
-            beta = meta->gb;
-        }
+        const float g = meta->g, beta = meta->beta;
         // record scalars, one warp per record
         for (int j = warp; j < p; j += kPipeCW) {
             const float4 kj = load4(krs + (size_t)j * K + t.col);

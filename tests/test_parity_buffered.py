@@ -84,7 +84,7 @@ def test_exact_ring_shapes_mixed_phases(K, G, kernel):
     """Rows at different cursors in one call (each row's own phase), records of one q/k head
     shared by G value heads; at K = V = 128 both the per-tile and the pipelined kernel."""
     H = 2
-    w = _run_buffered(3, H, H * G, K, K, 5, "f32", "f32", seed=K + G, steps=7, start_pos=[0, 2, 4],
+    w = _run_buffered(3, H, H * G, K, K, 4, "f32", "f32", seed=K + G, steps=7, start_pos=[0, 1, 3],
                       indexed=True, kernel=kernel)
     assert max(w.values()) <= 1e-5, w
 
