@@ -4,7 +4,7 @@
 // Same arithmetic as buffered_kernel.cu (low-rank replay of the ring records; the flush step at
 // write_pos == L-1 folds them into the checkpoint and writes it back), organised so that HBM
 // streams continuously:
-//   - one CTA per SM, 16 consumer warps and 1 producer warp;
+//   - one CTA per SM: two groups of 8 consumer warps that take alternate tiles, and 1 producer warp;
 //   - the producer walks the CTA's tiles ahead of the consumers and, for each, moves the 64 KB
 //     checkpoint tile, the q/k/v rows and the tile's ring records (p delta rows, p key rows) into
 //     a shared-memory stage with 1-D bulk copies (cp.async.bulk) that complete on the stage's
@@ -13,9 +13,9 @@
 //   - NST stages (2 or 3, as many as fit) keep up to NST tiles in flight per SM while the
 //     consumers compute, so the tile loads of the next tiles overlap the current tile's
 //     arithmetic and write-back;
-//   - consumers copy the tile from shared memory into registers (8 rows x 4 columns per lane),
-//     release the stage on its "empty" mbarrier once everything in it has been read, and write the
-//     flushed state from registers with streaming stores.
+//   - consumers take both dot products straight from the staged tile (16 rows x 4 columns per
+//     lane); a flush step re-reads it eight rows at a time, folds the records in and writes the
+//     new checkpoint with streaming stores; then the stage is released on its "empty" mbarrier.
 // Every wait is bounded: a wait that runs past its limit sets GDN_DEVERR_TIMEOUT, raises a
 // CTA-wide abort flag and ends the CTA's loop; the producer then waits (bounded) for the copies
 // it issued, so no copy is in flight when the CTA exits.
@@ -28,7 +28,9 @@
 
 namespace gdn {
 
-constexpr int kPipeCW = 16;                           // consumer warps
+constexpr int kPipeGW = 8;                            // warps of one consumer group
+constexpr int kPipeGroups = 2;                        // consumer groups, alternating tiles
+constexpr int kPipeCW = kPipeGW * kPipeGroups;        // consumer warps
 constexpr int kPipeThreads = (kPipeCW + 1) * 32;      // plus one producer warp
 constexpr int kPipeLMax = 64;
 constexpr long long kWaitLimit = 1LL << 31;           // SM clock cycles, about one second
@@ -69,7 +71,7 @@ template <> __device__ __forceinline__ bf16 ring_out<bf16>(float x) { return __f
 __device__ __forceinline__ float ring_in(float x) { return x; }
 __device__ __forceinline__ float ring_in(bf16 x) { return __bfloat162float(x); }
 
-// eight consecutive ring values (one warp's rows) from shared memory
+// eight consecutive ring values (rows of one warp) from shared memory
 __device__ __forceinline__ void load8(const float *p, float (&o)[8])
 {
     const float4 a = *reinterpret_cast<const float4 *>(p), b = *reinterpret_cast<const float4 *>(p + 4);
@@ -90,7 +92,7 @@ template <typename Tin, typename Tring>
 __global__ void __launch_bounds__(kPipeThreads, 1) buffered_pipe_kernel(const __grid_constant__ StepLaunch P)
 {
     constexpr int K = 128, V = 128;
-    using TL = Tile<128, 8, kPipeCW>;
+    using TL = Tile<128, 16, kPipeGW>;
     extern __shared__ __align__(128) unsigned char sm[];
     __shared__ int abort_flag;
     __shared__ int zero_flag;
@@ -107,8 +109,8 @@ __global__ void __launch_bounds__(kPipeThreads, 1) buffered_pipe_kernel(const __
     if (threadIdx.x == 0) {
         for (int s = 0; s < NST; ++s) {
             mbar_init(&full[s], 32);
-            mbar_init(&empty[s], kPipeCW);
-            mbar_init(&scr[s], kPipeCW);
+            mbar_init(&empty[s], kPipeGW);
+            mbar_init(&scr[s], kPipeGW);
         }
         abort_flag = 0;
         zero_flag = 0;
@@ -205,11 +207,13 @@ __global__ void __launch_bounds__(kPipeThreads, 1) buffered_pipe_kernel(const __
     }
 
     // -------------------------------------------------------------------- consumer warps
+    // Two groups of eight warps take alternate tiles, so two tiles are in their arithmetic at once.
+    const int group = warp / kPipeGW, gwarp = warp - group * kPipeGW;
     TL t;
-    t.init(warp);
-    const int tid = threadIdx.x;   // 0 .. 511
-    int n = 0;
-    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++n) {
+    t.init(gwarp);
+    const int tid = threadIdx.x - group * kPipeGW * 32;   // 0 .. 255 within the group
+    int n = group;
+    for (int tile = blockIdx.x + group * gridDim.x; tile < ntiles; tile += kPipeGroups * gridDim.x, n += kPipeGroups) {
         const int st = n % NST;
         const uint32_t ph = (uint32_t)(n / NST) & 1u;
         if (!mbar_wait(&full[st], ph, &abort_flag, kWaitLimit)) {
@@ -248,7 +252,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1) buffered_pipe_kernel(const __
         const float kq = group_sum<32>(dot4(kh, qh));
         const float g = meta->g, beta = meta->beta;
         // record scalars, one warp per record
-        for (int j = warp; j < p; j += kPipeCW) {
+        for (int j = gwarp; j < p; j += kPipeGW) {
             const float4 kj = load4(krs + (size_t)j * K + t.col);
             const float dk = group_sum<32>(dot4(kj, kh));
             const float dq = group_sum<32>(dot4(kj, qh));
@@ -268,14 +272,20 @@ __global__ void __launch_bounds__(kPipeThreads, 1) buffered_pipe_kernel(const __
         for (int i = 0; i < p; ++i) gsum += meta->gr[i];
         const float Gam = expf(gsum);
 
-        // tile into registers, the two dots
-#pragma unroll
-        for (int i = 0; i < TL::R; ++i)
-            t.s[i] = *reinterpret_cast<const float4 *>(Ss + (size_t)t.row(0, i) * K + t.col);
+        // the two dots, straight from the staged tile (16 rows x 4 columns per lane)
+        const int row0 = t.row(0, 0);   // this warp's TL::R consecutive rows
         const int r_own = t.row(0, t.owned_chunk(0));
         const float vv = t.holds_k_dot() ? to_f32(vs[r_own]) : 0.f;
         float x[TL::N];
-        t.partial_dots(scale4(kh, Gam), scale4(qh, Gam), x);
+        {
+            const float4 gk = scale4(kh, Gam), gq = scale4(qh, Gam);
+#pragma unroll
+            for (int i = 0; i < TL::R; ++i) {
+                const float4 srow = *reinterpret_cast<const float4 *>(Ss + (size_t)(row0 + i) * K + t.col);
+                x[i] = dot4(srow, gk);
+                x[TL::R + i] = dot4(srow, gq);
+            }
+        }
         t.reduce_scatter(x);
 
         if (!mbar_wait(&scr[st], ph, &abort_flag, kWaitLimit)) {
@@ -303,34 +313,38 @@ __global__ void __launch_bounds__(kPipeThreads, 1) buffered_pipe_kernel(const __
                 store_out(a.out, a.out_dtype, out_base + r_own, fmaf(dq, kq, x[0]));
         }
         if (flush) {
+            // S = Gamma S_c + delta k^T + sum_j d_j (c_j k_j)^T, eight rows at a time
+            float *S = a.state + ((size_t)slot * HV + hv) * (size_t)(V * K);
 #pragma unroll
-            for (int i = 0; i < TL::R; ++i) t.s[i] = axpby4(Gam, t.s[i], t.delta_of(dv, i), kh);
-            const int row0 = t.row(0, 0);   // this warp's 8 consecutive rows
-            for (int j = 0; j < p; ++j) {
-                const float cj = meta->c[j];
-                const float4 kj = scale4(load4(krs + (size_t)j * K + t.col), cj);
-                float dj[8];
-                load8(ds + (size_t)j * V + row0, dj);
+            for (int i8 = 0; i8 < TL::R; i8 += 8) {
+                float4 acc[8];
 #pragma unroll
-                for (int i = 0; i < TL::R; ++i) {
-                    t.s[i].x = fmaf(dj[i], kj.x, t.s[i].x);
-                    t.s[i].y = fmaf(dj[i], kj.y, t.s[i].y);
-                    t.s[i].z = fmaf(dj[i], kj.z, t.s[i].z);
-                    t.s[i].w = fmaf(dj[i], kj.w, t.s[i].w);
+                for (int i = 0; i < 8; ++i) {
+                    const float4 srow = *reinterpret_cast<const float4 *>(Ss + (size_t)(row0 + i8 + i) * K + t.col);
+                    acc[i] = axpby4(Gam, srow, t.delta_of(dv, i8 + i), kh);
                 }
+                for (int j = 0; j < p; ++j) {
+                    const float4 kj = scale4(load4(krs + (size_t)j * K + t.col), meta->c[j]);
+                    float dj[8];
+                    load8(ds + (size_t)j * V + row0 + i8, dj);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        acc[i].x = fmaf(dj[i], kj.x, acc[i].x);
+                        acc[i].y = fmaf(dj[i], kj.y, acc[i].y);
+                        acc[i].z = fmaf(dj[i], kj.z, acc[i].z);
+                        acc[i].w = fmaf(dj[i], kj.w, acc[i].w);
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) st_stream(S + (size_t)(row0 + i8 + i) * K + t.col, acc[i]);
             }
         }
         // everything of this stage has been read
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[st]);
 
-        if (flush) {
-            float *S = a.state + ((size_t)slot * HV + hv) * (size_t)(V * K);
-#pragma unroll
-            for (int i = 0; i < TL::R; ++i) st_stream(S + (size_t)t.row(0, i) * K + t.col, t.s[i]);
-        }
         // this step's key record (first value head of the group) and log-decay record
-        if (hv % G == 0 && warp == 0) {
+        if (hv % G == 0 && gwarp == 0) {
             Tring *dst = static_cast<Tring *>(P.k_cache) + (((size_t)slot * a.H + hv / G) * L + p) * K + t.col;
             dst[0] = ring_out<Tring>(kh.x);
             dst[1] = ring_out<Tring>(kh.y);
