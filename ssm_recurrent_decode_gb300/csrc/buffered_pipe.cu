@@ -216,7 +216,12 @@ __global__ void __launch_bounds__(kPipeThreads, 1) buffered_pipe_kernel(const __
     for (int tile = blockIdx.x + group * gridDim.x; tile < ntiles; tile += kPipeGroups * gridDim.x, n += kPipeGroups) {
         const int st = n % NST;
         const uint32_t ph = (uint32_t)(n / NST) & 1u;
-        if (!mbar_wait(&full[st], ph, &abort_flag, kWaitLimit)) {
+        // A stage's uses alternate between the groups, so this group may reach tile n while the
+        // other group still holds tile n - NST on the same stage. A parity wait can only tell
+        // apart a phase from the one before it, so first wait for that earlier use to be released
+        // (after which the stage's barriers are at most one phase away from tile n's).
+        if ((n >= NST && !mbar_wait(&empty[st], ph ^ 1u, &abort_flag, kWaitLimit)) ||
+            !mbar_wait(&full[st], ph, &abort_flag, kWaitLimit)) {
             if (lane == 0) {
                 *(volatile int *)&abort_flag = 1;
                 raise_flag(a.err_flags, GDN_DEVERR_TIMEOUT);
