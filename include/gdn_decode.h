@@ -156,6 +156,9 @@ typedef struct gdn_fused_args {
     int32_t gate_act;         /* gdn_act applied to out_gate */
     void *out;                /* bf16 [T, heads, head_dim] */
     int32_t *err_flags;       /* optional */
+    int32_t kernel;           /* GDN_KERNEL_AUTO: the pipelined kernel when head_dim == 128, the conv
+                                 state is in the DS or SD layout and rows are 16-byte aligned, else
+                                 the per-tile kernel; GDN_KERNEL_TILE / GDN_KERNEL_PIPE force one */
 } gdn_fused_args;
 
 /*
@@ -208,7 +211,7 @@ const char *gdn_strerror(int status);
 /* ABI checks for bindings: sizeof of the args structs (which: 0 step, 1 ring, 2 fused). */
 size_t gdn_abi_struct_size(int which);
 
-/* Library ABI version (incremented on any change of the structs above; currently 2). */
+/* Library ABI version (incremented on any change of the structs above; currently 3). */
 int gdn_abi_version(void);
 
 #ifdef __cplusplus

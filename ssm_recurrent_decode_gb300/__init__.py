@@ -35,7 +35,7 @@ GDN_FUSED_GATE_KDA, GDN_FUSED_GATE_GDN = 0, 1
 GDN_ACT_SILU, GDN_ACT_SIGMOID = 0, 1
 GDN_DEVERR_BAD_INDEX, GDN_DEVERR_BAD_WRITE_POS, GDN_DEVERR_TIMEOUT = 0x1, 0x2, 0x4
 GDN_KERNEL = {"auto": 0, "tile": 1, "pipe": 2}
-ABI_VERSION = 2
+ABI_VERSION = 3
 
 # every function the header declares
 EXPORTS = ("gdn_decode_step", "gdn_decode_step_indexed", "gdn_decode_buffered", "gdn_decode_fused",
@@ -68,7 +68,7 @@ class GdnFusedArgs(ctypes.Structure):
                 ("lower_bound", _f32), ("scale", _f32), ("use_qk_l2norm", _i32),
                 ("state", _vp), ("state_indices", _vp), ("pad_slot_id", _i32),
                 ("out_gate", _vp), ("norm_w", _vp), ("norm_eps", _f32), ("gate_act", _i32),
-                ("out", _vp), ("err_flags", _vp)]
+                ("out", _vp), ("err_flags", _vp), ("kernel", _i32)]
 
 
 class GdnError(RuntimeError):
@@ -290,8 +290,10 @@ def gdn_decode_buffered(q, k, v, state, out, d_cache, k_cache, g_cache, write_po
 def gdn_decode_fused(x, conv_w, conv_state, raw_g, raw_beta, A_log, dt_bias, state, state_indices,
                      out_gate, norm_w, out, *, conv_b=None, pad_slot_id=0, gate_kind="kda",
                      kda_gate_form=0, lower_bound=-5.0, scale=None, use_qk_l2norm=True,
-                     norm_eps=1e-5, gate_act="silu", err_flags=None, stream=None):
+                     norm_eps=1e-5, gate_act="silu", err_flags=None, kernel="auto", stream=None):
     """Fused decode: conv update -> delta step -> gated RMSNorm, one launch.
+    kernel: "auto" (the persistent pipelined kernel when head_dim is 128, the conv state is in the
+    DS or SD layout and rows are 16-byte aligned), "tile" or "pipe" to force one.
     x bf16 [T, 3*dim]; conv_w fp32 [3*dim, 4]; conv_state bf16 with logical shape
     [num_slots, 3*dim, 3] (any strides: the "DS" layout is the plain tensor, the "SD" layout a
     transposed view of [num_slots, 3, 3*dim]); raw_g bf16 [T, heads, D] (kda) or [T, heads] (gdn);
@@ -331,6 +333,7 @@ def gdn_decode_fused(x, conv_w, conv_state, raw_g, raw_beta, A_log, dt_bias, sta
     f.gate_act = {"silu": GDN_ACT_SILU, "sigmoid": GDN_ACT_SIGMOID}[gate_act]
     f.out = _ptr(_dense(out, "out"), "out", torch.bfloat16)
     f.err_flags = _ptr(err_flags, "err_flags", torch.int32)
+    f.kernel = GDN_KERNEL[kernel]
     _check("gdn_decode_fused", lib().gdn_decode_fused(ctypes.byref(f), _stream(stream)))
     return out
 

@@ -9,7 +9,7 @@
 
 namespace {
 
-constexpr int kAbiVersion = 2;
+constexpr int kAbiVersion = 3;
 
 bool k_supported(int K) { return K == 16 || K == 32 || K == 64 || K == 128; }
 bool dtype_ok(int d) { return d == GDN_F32 || d == GDN_BF16; }
@@ -148,10 +148,33 @@ int gdn_decode_fused(const gdn_fused_args *a, gdn_stream_t stream)
     if (!aligned(a->conv_w, 16) || !aligned(a->state, 16) || !aligned(a->A_log, 4) ||
         !aligned(a->dt_bias, 4) || !aligned(a->norm_w, 4) || (a->conv_b && !aligned(a->conv_b, 4)))
         return GDN_ERR_ALIGN;
+    if (a->kernel < GDN_KERNEL_AUTO || a->kernel > GDN_KERNEL_PIPE) return GDN_ERR_ARG;
     gdn::FusedLaunch p;
     std::memset(&p, 0, sizeof(p));
     p.a = *a;
     p.scale = a->scale != 0.f ? a->scale : 1.0f / std::sqrt((float)a->head_dim);
+    // the pipelined kernel: head_dim 128, conv state in the DS ([slot][chan][tap]) or SD
+    // ([slot][tap][chan]) layout, every bulk-copied row 16-byte aligned
+    const bool ds = a->cs_stride_chan == 3 && a->cs_stride_tap == 1;
+    const bool sd = a->cs_stride_chan == 1 && a->cs_stride_tap == 3 * dim;
+    bool pipe_ok = a->head_dim == 128 && (ds || sd);
+    const bool pipe_aligned = aligned(a->x, 16) && a->x_stride % 8 == 0 && aligned(a->conv_state, 16) &&
+                              a->cs_stride_slot % 8 == 0 && aligned(a->raw_g, 16) && aligned(a->out_gate, 16) &&
+                              aligned(a->dt_bias, 16) && aligned(a->state, 16);
+    if (pipe_ok) {
+        int dev = 0, max_smem = 0;
+        pipe_ok = cudaGetDevice(&dev) == cudaSuccess &&
+                  cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess &&
+                  gdn::fused_pipe_fits(max_smem);
+    }
+    bool use_pipe = pipe_ok && pipe_aligned;
+    if (a->kernel == GDN_KERNEL_PIPE) {
+        if (!pipe_ok) return GDN_ERR_SHAPE;
+        if (!pipe_aligned) return GDN_ERR_ALIGN;
+    } else if (a->kernel == GDN_KERNEL_TILE) {
+        use_pipe = false;
+    }
+    if (use_pipe) return gdn::launch_fused_pipe(p, sd, reinterpret_cast<cudaStream_t>(stream));
     return gdn::launch_fused(p, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -44,4 +44,9 @@ int launch_buffered_pipe(const StepLaunch &p, int ring_dtype, cudaStream_t strea
 // Whether its two-stage shared-memory footprint fits in max_smem bytes per CTA.
 bool buffered_pipe_fits(int L, int in_dtype, int ring_dtype, int max_smem);
 
+// The persistent, warp-specialised fused kernel (head_dim 128; conv state in the DS layout, or in
+// the SD layout when sd is true).
+int launch_fused_pipe(const FusedLaunch &p, bool sd, cudaStream_t stream);
+bool fused_pipe_fits(int max_smem);
+
 }  // namespace gdn

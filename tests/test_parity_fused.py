@@ -24,7 +24,7 @@ def f64(bits):
 
 
 def _run_fused(T, heads, D, *, layout="DS", gate_kind="kda", form=0, act="silu", seed=0,
-               pad_rows=(), steps=1, sample_rows=None):
+               pad_rows=(), steps=1, sample_rows=None, kernel="auto"):
     dim = heads * D
     num_slots = T + 8
     ins = syn.fused_inputs(T, heads, D, num_slots, seed)
@@ -60,7 +60,7 @@ def _run_fused(T, heads, D, *, layout="DS", gate_kind="kda", form=0, act="silu",
                              bits_to_torch_bf16(raw_g_bits), bits_to_torch_bf16(ins["raw_beta"]),
                              A_log, dtb, state, idx, bits_to_torch_bf16(gate_bits), norm_w, out,
                              pad_slot_id=0, gate_kind=gate_kind, kda_gate_form=form, gate_act=act,
-                             err_flags=err)
+                             err_flags=err, kernel=kernel)
         rows = np.arange(T) if sample_rows is None else np.asarray(sample_rows)
         if sample_rows is not None:
             # only the sampled rows' slots are followed by the oracle
@@ -89,16 +89,19 @@ def _run_fused(T, heads, D, *, layout="DS", gate_kind="kda", form=0, act="silu",
     return worst
 
 
+@pytest.mark.parametrize("kernel", ["tile", "pipe"])
 @pytest.mark.parametrize("layout", ["DS", "SD"])
 @pytest.mark.parametrize("T", [1, 8])
-def test_kda_config_shapes(layout, T):
+def test_kda_config_shapes(layout, T, kernel):
     """The fused KDA decode shapes: 96 heads x 128, conv width 4, lower bound -5, silu gate."""
-    w = _run_fused(T, 96, 128, layout=layout, seed=T)
+    w = _run_fused(T, 96, 128, layout=layout, seed=T, kernel=kernel)
     assert w["out"] <= 2e-2 and w["state"] <= 1e-5, w
 
 
-def test_kda_32_tokens_sampled_rows():
-    w = _run_fused(32, 96, 128, seed=32, sample_rows=[0, 7, 19, 31])
+@pytest.mark.parametrize("kernel", ["tile", "pipe"])
+def test_kda_32_tokens_sampled_rows(kernel):
+    """3072 tiles: the pipelined kernel walks about twenty per CTA through its stages."""
+    w = _run_fused(32, 96, 128, seed=32, sample_rows=[0, 7, 19, 31], kernel=kernel, steps=2)
     assert w["out"] <= 2e-2 and w["state"] <= 1e-5, w
 
 
@@ -107,14 +110,17 @@ def test_kda_32_tokens_sampled_rows():
 def test_gate_readings_and_activations(form, act):
     w = _run_fused(4, 6, 64, form=form, act=act, seed=3 + form, steps=3)
     assert w["out"] <= 2e-2 and w["state"] <= 1e-5, w
+    w = _run_fused(4, 6, 128, form=form, act=act, seed=13 + form, steps=3, kernel="pipe")
+    assert w["out"] <= 2e-2 and w["state"] <= 1e-5, w
 
 
-@pytest.mark.parametrize("D", [16, 32])
+@pytest.mark.parametrize("D", [16, 32, 128])
 def test_gdn_gate_and_small_heads(D):
     w = _run_fused(5, 4, D, gate_kind="gdn", seed=D, steps=2, layout="SD")
     assert w["out"] <= 2e-2 and w["state"] <= 1e-5, w
 
 
-def test_null_slot_rows_are_skipped():
-    w = _run_fused(6, 4, 64, seed=9, pad_rows=(0, 4), steps=2)
+@pytest.mark.parametrize("D,kernel", [(64, "auto"), (128, "pipe")])
+def test_null_slot_rows_are_skipped(D, kernel):
+    w = _run_fused(6, 4, D, seed=9, pad_rows=(0, 4), steps=2, kernel=kernel)
     assert w["out"] <= 2e-2 and w["state"] <= 1e-5, w
