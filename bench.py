@@ -69,8 +69,8 @@ KERNEL_FILES = {
              "ssm_recurrent_decode_gb300/csrc/gdn_common.cuh"],
     "buffered": ["ssm_recurrent_decode_gb300/csrc/buffered_pipe.cu", "ssm_recurrent_decode_gb300/csrc/gdn_pipe.cuh",
                  "ssm_recurrent_decode_gb300/csrc/gdn_tile.cuh", "ssm_recurrent_decode_gb300/csrc/gdn_common.cuh"],
-    "fused": ["ssm_recurrent_decode_gb300/csrc/fused_kernel.cu", "ssm_recurrent_decode_gb300/csrc/gdn_tile.cuh",
-              "ssm_recurrent_decode_gb300/csrc/gdn_common.cuh"],
+    "fused": ["ssm_recurrent_decode_gb300/csrc/fused_pipe.cu", "ssm_recurrent_decode_gb300/csrc/gdn_pipe.cuh",
+              "ssm_recurrent_decode_gb300/csrc/gdn_tile.cuh", "ssm_recurrent_decode_gb300/csrc/gdn_common.cuh"],
 }
 
 
