@@ -100,7 +100,7 @@ def _declare(L):
     L.oracle_sigmoid.argtypes = [c_size, _D, _D]
     L.oracle_delta_step.restype = c_int
     L.oracle_delta_step.argtypes = [c_int] * 6 + [_D, _D, _D, _D, c_int, _D, c_dbl, c_int,
-                                                  c_dbl, _I32, ctypes.c_int32, _D, _D]
+                                                  c_dbl, _I32, ctypes.c_int32, c_int, _D, _D]
     L.oracle_gdn_buffered.restype = c_int
     L.oracle_gdn_buffered.argtypes = ([c_int] * 6 + [_D, _D, _D, _D, _D, c_dbl, c_int, c_dbl,
                                        _I32, ctypes.c_int32, c_int, c_int, _D, _D, _D, _I32,
@@ -167,10 +167,10 @@ def sigmoid(x):
 
 
 def delta_step(q, k, v, g, beta, state, *, scale, use_qk_l2norm=True, idx=None, pad_slot=-1,
-               l2_eps=L2_EPS):
+               l2_eps=L2_EPS, state_bf16=False):
     """One decode step. q, k: [B, H, K]; v: [B, HV, V]; g: [B, HV] or [B, HV, K] (per key);
-    beta: [B, HV]; state: [num_slots, HV, V, K] float64, updated in place.
-    Returns (out [B, HV, V], number of out-of-range rows)."""
+    beta: [B, HV]; state: [num_slots, HV, V, K] float64, updated in place (and rounded to bf16
+    after the update when state_bf16). Returns (out [B, HV, V], number of out-of-range rows)."""
     _check_inplace(state)
     q, k, v, g, beta = _f64(q), _f64(k), _f64(v), _f64(g), _f64(beta)
     B, H, K = q.shape
@@ -183,7 +183,7 @@ def delta_step(q, k, v, g, beta, state, *, scale, use_qk_l2norm=True, idx=None, 
     out = np.empty((B, HV, V))
     bad = lib().oracle_delta_step(B, H, HV, K, V, num_slots, _p(q), _p(k), _p(v), _p(g), per_key,
                                   _p(beta), float(scale), int(bool(use_qk_l2norm)), float(l2_eps),
-                                  _pi(idx), int(pad_slot), _p(state), _p(out))
+                                  _pi(idx), int(pad_slot), int(bool(state_bf16)), _p(state), _p(out))
     return out, bad
 
 
@@ -198,13 +198,13 @@ def split_packed(mixed_qkv, H, HV, K, V):
 
 
 def gdn_step_packed(mixed_qkv, a, b, A_log, dt_bias, state, *, H, HV, K, V, scale=None,
-                    use_qk_l2norm=True, idx=None, pad_slot=-1):
+                    use_qk_l2norm=True, idx=None, pad_slot=-1, state_bf16=False):
     """The packed GDN decode step with the raw gate inputs; returns (out, bad)."""
     q, k, v = split_packed(mixed_qkv, H, HV, K, V)
     g, beta = gdn_gates(a, b, A_log, dt_bias)
     scale = K ** -0.5 if scale is None else scale
     return delta_step(q, k, v, g, beta, state, scale=scale, use_qk_l2norm=use_qk_l2norm, idx=idx,
-                      pad_slot=pad_slot)
+                      pad_slot=pad_slot, state_bf16=state_bf16)
 
 
 def gdn_buffered(q, k, v, g, beta, state, d_cache, k_cache, g_cache, write_pos, *, L,

@@ -137,12 +137,15 @@ static long slot_of(int b, const int32_t *idx, int32_t pad_slot, int num_slots)
  *   q/k head of value head hv is hv / (HV / H). With use_qk_l2norm, k_hat = k / sqrt(|k|^2 + l2_eps)
  *   and q_hat = scale * q / sqrt(|q|^2 + l2_eps); otherwise q_hat = scale * q.
  *   A pad row (idx[b] == pad_slot) and a row with an out-of-range slot leave the state as it is and
- *   get out = 0. Returns the number of out-of-range rows. */
+ *   get out = 0. Returns the number of out-of-range rows.
+ *   state_bf16 != 0: the state is stored in bf16 ("Optimization Log", Kernel 4: a 32 KB bf16 state
+ *   per head). The step runs on the stored values as above, out comes from the updated state before
+ *   storage, and the updated state is then rounded to bf16 (nearest, ties to even). */
 int oracle_delta_step(int B, int H, int HV, int K, int V, int num_slots,
                       const double *q, const double *k, const double *v,
                       const double *g, int g_per_key, const double *beta,
                       double scale, int use_qk_l2norm, double l2_eps,
-                      const int32_t *idx, int32_t pad_slot, double *state, double *out)
+                      const int32_t *idx, int32_t pad_slot, int state_bf16, double *state, double *out)
 {
     int G = HV / H, bad = 0;
     double *kh = malloc(sizeof(double) * K), *qh = malloc(sizeof(double) * K);
@@ -159,9 +162,11 @@ int oracle_delta_step(int B, int H, int HV, int K, int V, int num_slots,
             l2_normalise(K, k + ((size_t)b * H + h) * K, l2_eps, 1.0, use_qk_l2norm, kh);
             l2_normalise(K, q + ((size_t)b * H + h) * K, l2_eps, scale, use_qk_l2norm, qh);
             const double *gl = g_per_key ? g + ((size_t)b * HV + hv) * K : g + (size_t)b * HV + hv;
-            delta_rule_tile(K, V, state + ((size_t)s * HV + hv) * V * K, kh, qh,
-                            v + ((size_t)b * HV + hv) * V, gl, g_per_key, beta[(size_t)b * HV + hv],
-                            u, d, out + ((size_t)b * HV + hv) * V);
+            double *S = state + ((size_t)s * HV + hv) * V * K;
+            delta_rule_tile(K, V, S, kh, qh, v + ((size_t)b * HV + hv) * V, gl, g_per_key,
+                            beta[(size_t)b * HV + hv], u, d, out + ((size_t)b * HV + hv) * V);
+            if (state_bf16)
+                for (size_t e = 0; e < (size_t)V * K; ++e) S[e] = oracle_round_bf16(S[e]);
         }
     }
     free(kh); free(qh); free(u); free(d);

@@ -44,6 +44,10 @@ MUTANTS = [
     ("per-key decay index", "decay_log[kk] : decay_log[0]", "decay_log[0] : decay_log[0]"),
     ("bf16 rounding by truncation", "return ldexp(nearbyint(ldexp(m, 8)), e - 8);",
      "return ldexp(trunc(ldexp(m, 8)), e - 8);"),
+    ("bf16 state not rounded", "for (size_t e = 0; e < (size_t)V * K; ++e) S[e] = oracle_round_bf16(S[e]);", ";"),
+    ("bf16 state rounded before the output",
+     "            delta_rule_tile(K, V, S, kh, qh, v + ((size_t)b * HV + hv) * V, gl, g_per_key,\n                            beta[(size_t)b * HV + hv], u, d, out + ((size_t)b * HV + hv) * V);\n            if (state_bf16)\n                for (size_t e = 0; e < (size_t)V * K; ++e) S[e] = oracle_round_bf16(S[e]);",
+     "            delta_rule_tile(K, V, S, kh, qh, v + ((size_t)b * HV + hv) * V, gl, g_per_key,\n                            beta[(size_t)b * HV + hv], u, d, out + ((size_t)b * HV + hv) * V);\n            if (state_bf16) {\n                for (size_t e = 0; e < (size_t)V * K; ++e) S[e] = oracle_round_bf16(S[e]);\n                for (int vv = 0; vv < V; ++vv) { double acc = 0.0; for (int kk = 0; kk < K; ++kk) acc += S[(size_t)vv * K + kk] * qh[kk]; out[((size_t)b * HV + hv) * V + vv] = acc; }\n            }"),
 ]
 
 

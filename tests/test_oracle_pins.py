@@ -254,6 +254,33 @@ def check_closed_matrix_form(B=2, H=2, HV=4, K=16, V=16):
             assert rel_err(out2[b, hv], want2 @ qq) < 1e-13
 
 
+def check_bf16_state_storage():
+    """bf16 state storage: the step runs on the stored values, out comes from the updated state
+    before storage, and the stored state is the update rounded to bf16 -- checked against the
+    closed matrix form (numpy) rounded with torch's own bf16 conversion."""
+    B, H, HV, K, V = 2, 2, 4, 16, 16
+    q, k, v, g, beta = tiny_step_inputs(seed=19, B=B, H=H, HV=HV, K=K, V=V)
+    S0 = torch.from_numpy(tiny_state(seed=19)).to(torch.bfloat16).to(torch.float64).numpy()
+    S = S0.copy()
+    out, _ = oracle.delta_step(q, k, v, g, beta, S, scale=0.25, state_bf16=True)
+    kh = l2n(k); qh = 0.25 * l2n(q)
+    I = np.eye(K)
+    for b in range(B):
+        for hv in range(HV):
+            kk = kh[b, hv // 2]
+            want = math.exp(g[b, hv]) * S0[b, hv] @ (I - beta[b, hv] * np.outer(kk, kk)) \
+                + beta[b, hv] * np.outer(v[b, hv], kk)
+            assert rel_err(out[b, hv], want @ qh[b, hv // 2]) < 1e-13
+            stored = torch.from_numpy(want).to(torch.bfloat16).to(torch.float64).numpy()
+            # the fp64 update and the closed form agree to ~1e-15, so only values within that of a
+            # bf16 rounding midpoint could round apart; none is expected at these inputs
+            assert np.array_equal(S[b, hv], stored)
+
+
+def test_bf16_state_storage():
+    check_bf16_state_storage()
+
+
 def check_gqa_duplication():
     """G > 1 equals G = 1 with each q/k head repeated for its G value heads."""
     B, H, HV, K, V = 2, 2, 6, 16, 16
@@ -520,5 +547,5 @@ ALL_CHECKS = [
     check_indices_permute_and_pad, check_buffered_equals_looped,
     check_buffered_ring_records_and_lowrank, check_gdn_gates, check_kda_gate_reading,
     check_conv_update_is_causal_convolution, check_gated_rmsnorm, check_bf16_rounding,
-    check_fused_per_key_gate_reduces_to_scalar,
+    check_fused_per_key_gate_reduces_to_scalar, check_bf16_state_storage,
 ]
