@@ -312,7 +312,7 @@ def base_line(h, value, ms, steps, warmup, workload, config, kernel_launches):
 # ------------------------------------------------------------------------------------------------
 # workloads
 # ------------------------------------------------------------------------------------------------
-def packed_workload(B, H, HV, K, V, seed, device, layer=0):
+def packed_workload(B, H, HV, K, V, seed, device, layer=0, state_dtype="f32"):
     import torch
     import gdn_synth as syn
     width = 2 * H * K + HV * V
@@ -321,7 +321,8 @@ def packed_workload(B, H, HV, K, V, seed, device, layer=0):
     b = torch.empty((B, HV), dtype=torch.bfloat16, device=device)
     A_log = torch.empty(HV, dtype=torch.float32, device=device)
     dt_bias = torch.empty(HV, dtype=torch.float32, device=device)
-    state = torch.empty((B, HV, V, K), dtype=torch.float32, device=device)
+    state = torch.empty((B, HV, V, K), dtype=torch.bfloat16 if state_dtype == "bf16" else torch.float32,
+                        device=device)
     r = syn.GdnRecipe()
     syn.fill_normal_(x, seed, syn.Tag.QKV, 0, r.qkv_std, layer)
     syn.fill_normal_(a, seed, syn.Tag.A, 0, r.a_std, layer)
@@ -364,9 +365,10 @@ def run_packed(args):
     torch = h.torch
     gdn.lib()
     B, H, HV, K, V = args.B, 16, 32, 128, 128
-    w = packed_workload(B, H, HV, K, V, seed=1234 + h.rank, device=h.dev)
+    sbytes = 2 if args.state_dtype == "bf16" else 4
+    w = packed_workload(B, H, HV, K, V, seed=1234 + h.rank, device=h.dev, state_dtype=args.state_dtype)
     import gdn_synth as syn
-    n_pools = pool_count(B * HV * V * K * 4, h.dev)
+    n_pools = pool_count(B * HV * V * K * sbytes, h.dev)
     pools = [w["state"]]
     for p in range(1, n_pools):
         s = torch.empty_like(w["state"])
@@ -401,20 +403,22 @@ def run_packed(args):
     if h.rank != 0:
         return h.finish(None)
 
-    state_bytes = 2 * B * HV * V * K * 4
+    state_bytes = 2 * B * HV * V * K * sbytes
     gbs = h.world * state_bytes / (ms * 1e-3) / 1e9
     peak, _ = hbm_peak()
     line = base_line(
         h, gbs, ms, args.steps, args.warmup,
         f"gdn packed decode over a slot pool: B={B} H={H} HV={HV} K=V={K}, bf16 mixed_qkv/a/b/out, "
-        f"fp32 state [{B},{HV},{V},{K}], permuted int32 cache indices",
-        {"B": B, "H": H, "HV": HV, "K": K, "V": V, "input_dtype": "bf16", "state_dtype": "f32",
+        f"{args.state_dtype} state [{B},{HV},{V},{K}], permuted int32 cache indices",
+        {"B": B, "H": H, "HV": HV, "K": K, "V": V, "input_dtype": "bf16", "state_dtype": args.state_dtype,
          "state_bytes_per_step": state_bytes, "state_pools": n_pools,
-         "l2": ("state larger than L2 (1.07 GB vs 129 MB at B=256): no flush between steps"
-                if n_pools == 1 else f"{n_pools} state pools rotated, 4x the L2 size per pass")},
+         "l2": (f"state of {state_bytes / 2 / 1e9:.2f} GB read per step, larger than the L2: no flush "
+                f"between steps" if n_pools == 1 else
+                f"{n_pools} state pools rotated, at least 4x the L2 size per pass")},
         args.steps)
     line["pct_of_peak"] = round(100 * gbs / h.world / peak, 2)
-    line["roofline"] = roofline(state_bytes + packed_io_bytes(B, H, HV, K, V), ms, "step", f"packed_B{B}")
+    line["roofline"] = roofline(state_bytes + packed_io_bytes(B, H, HV, K, V), ms, "step",
+                                f"packed_B{B}" + ("_bf16state" if args.state_dtype == "bf16" else ""))
     line["cpu_baseline"] = cpu_baseline(H, HV, K, V, seed=7, budget_s=args.cpu_budget)
     line["e2e"] = {"value": round(h.world * state_bytes / (ms_e2e * 1e-3) / 1e9, 2), "unit": "GB/s",
                    "us_per_step": round(ms_e2e * 1e3, 3), "h2d_bytes_per_step": h2d,
@@ -695,6 +699,7 @@ def main(argv=None):
     p.add_argument("--L", type=int, default=16)
     p.add_argument("--T", type=int, default=128)
     p.add_argument("--layout", choices=["DS", "SD"], default="DS")
+    p.add_argument("--state-dtype", choices=["f32", "bf16"], default="f32")
     p.add_argument("--layers", type=int, default=48)
     p.add_argument("--pairs", type=int, default=8)
     p.add_argument("--cpu-budget", type=float, default=10.0)

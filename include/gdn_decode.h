@@ -94,9 +94,14 @@ typedef struct gdn_step_args {
     const float *beta;    /* DIRECT: [B, HV] */
     float scale;          /* multiplies q after normalisation; 0 selects K^-1/2 */
     int32_t use_qk_l2norm;/* 1: normalise q and k in the kernel (as above); 0: use them as given */
-    float *state;         /* [num_slots, HV, V, K] fp32, read and written in place */
+    void *state;          /* [num_slots, HV, V, K] in state_dtype, read and written in place */
     void *out;            /* [B, HV, V] out_dtype (the [B, 1, HV, V] decode output) */
     int32_t *err_flags;   /* optional, may be NULL: GDN_DEVERR_* bits are OR-ed in */
+    int32_t state_dtype;  /* GDN_F32 (default), or GDN_BF16: the state is stored in bf16 and the
+                             step computes in fp32; out comes from the updated state before it is
+                             rounded (nearest even) for storage. bf16 storage is supported by
+                             gdn_decode_step and gdn_decode_step_indexed; gdn_decode_buffered
+                             returns GDN_ERR_DTYPE for it. */
 } gdn_step_args;
 
 /* Ring of the buffered (output-only) decode; see gdn_decode_buffered. */
@@ -165,7 +170,8 @@ typedef struct gdn_fused_args {
  * gdn_decode_step -- one decode step, row b on slot b (num_slots >= B).
  * Source: "Optimization Log: Qwen3.5-27B Dense on B200", Kernel 4 Math block; q/k treatment as
  * in "Microbenchmark: buffered output-only GDN decode", _bench_cfg (run_packed).
- * HBM traffic: the state tile is read once and written once (2*B*HV*V*K*4 bytes per call).
+ * HBM traffic: the state tile is read once and written once (2*B*HV*V*K*4 bytes per call, or
+ * 2*B*HV*V*K*2 with a bf16 state).
  */
 int gdn_decode_step(const gdn_step_args *args, gdn_stream_t stream);
 
@@ -211,7 +217,7 @@ const char *gdn_strerror(int status);
 /* ABI checks for bindings: sizeof of the args structs (which: 0 step, 1 ring, 2 fused). */
 size_t gdn_abi_struct_size(int which);
 
-/* Library ABI version (incremented on any change of the structs above; currently 3). */
+/* Library ABI version (incremented on any change of the structs above; currently 4). */
 int gdn_abi_version(void);
 
 #ifdef __cplusplus

@@ -35,7 +35,7 @@ GDN_FUSED_GATE_KDA, GDN_FUSED_GATE_GDN = 0, 1
 GDN_ACT_SILU, GDN_ACT_SIGMOID = 0, 1
 GDN_DEVERR_BAD_INDEX, GDN_DEVERR_BAD_WRITE_POS, GDN_DEVERR_TIMEOUT = 0x1, 0x2, 0x4
 GDN_KERNEL = {"auto": 0, "tile": 1, "pipe": 2}
-ABI_VERSION = 3
+ABI_VERSION = 4
 
 # every function the header declares
 EXPORTS = ("gdn_decode_step", "gdn_decode_step_indexed", "gdn_decode_buffered", "gdn_decode_fused",
@@ -51,7 +51,7 @@ class GdnStepArgs(ctypes.Structure):
                 ("q_stride", _i64), ("k_stride", _i64), ("v_stride", _i64),
                 ("gate_mode", _i32), ("a", _vp), ("b", _vp), ("A_log", _vp), ("dt_bias", _vp),
                 ("g", _vp), ("beta", _vp), ("scale", _f32), ("use_qk_l2norm", _i32),
-                ("state", _vp), ("out", _vp), ("err_flags", _vp)]
+                ("state", _vp), ("out", _vp), ("err_flags", _vp), ("state_dtype", _i32)]
 
 
 class GdnRingArgs(ctypes.Structure):
@@ -212,7 +212,8 @@ def _step_args(q, k, v, state, out, *, H, a, b, A_log, dt_bias, g, beta, scale, 
         s.dt_bias = _ptr(_dense(dt_bias, "dt_bias"), "dt_bias", torch.float32)
     s.scale = 0.0 if scale is None else float(scale)
     s.use_qk_l2norm = int(bool(use_qk_l2norm))
-    s.state = _ptr(state, "state", torch.float32)
+    s.state = _ptr(state, "state")
+    s.state_dtype = _dtype_code(state)
     s.out = _ptr(out, "out")
     s.err_flags = _ptr(err_flags, "err_flags", torch.int32)
     return s
@@ -230,8 +231,8 @@ def gdn_decode_step(q, k, v, state, out, *, H=None, a=None, b=None, A_log=None, 
                     g=None, beta=None, scale=None, use_qk_l2norm=True, err_flags=None, stream=None):
     """One decode step, row b on slot b. q, k: [B, H*K] (or [B, H, K]) row views; v: [B, HV*V];
     gates either raw (a, b [B, HV] in the dtype of q; A_log, dt_bias [HV] fp32) or direct
-    (g, beta [B, HV] fp32); state [num_slots, HV, V, K] fp32 updated in place; out [B, HV, V]
-    (or [B, 1, HV, V]) fp32 or bf16."""
+    (g, beta [B, HV] fp32); state [num_slots, HV, V, K] fp32 (or bf16: stored in bf16, computed in
+    fp32) updated in place; out [B, HV, V] (or [B, 1, HV, V]) fp32 or bf16."""
     s = _step_args(q, k, v, state, out, H=H, a=a, b=b, A_log=A_log, dt_bias=dt_bias, g=g,
                    beta=beta, scale=scale, use_qk_l2norm=use_qk_l2norm, err_flags=err_flags)
     _check("gdn_decode_step", lib().gdn_decode_step(ctypes.byref(s), _stream(stream)))

@@ -9,7 +9,7 @@
 
 namespace {
 
-constexpr int kAbiVersion = 3;
+constexpr int kAbiVersion = 4;
 
 bool k_supported(int K) { return K == 16 || K == 32 || K == 64 || K == 128; }
 bool dtype_ok(int d) { return d == GDN_F32 || d == GDN_BF16; }
@@ -25,7 +25,7 @@ int check_step(const gdn_step_args *a, bool indexed)
     if (!k_supported(a->K) || a->V < 1 || a->V > 1024) return GDN_ERR_SHAPE;
     if ((int64_t)a->B * a->HV > INT32_MAX) return GDN_ERR_SHAPE;
     if (!indexed && a->num_slots < a->B) return GDN_ERR_SHAPE;
-    if (!dtype_ok(a->in_dtype) || !dtype_ok(a->out_dtype)) return GDN_ERR_DTYPE;
+    if (!dtype_ok(a->in_dtype) || !dtype_ok(a->out_dtype) || !dtype_ok(a->state_dtype)) return GDN_ERR_DTYPE;
     if (a->gate_mode != GDN_GATE_RAW && a->gate_mode != GDN_GATE_DIRECT) return GDN_ERR_ARG;
     if (a->B == 0) return GDN_OK;
     if (!a->q || !a->k || !a->v || !a->state || !a->out) return GDN_ERR_NULL;
@@ -82,6 +82,7 @@ int gdn_decode_buffered(const gdn_step_args *args, const int32_t *cache_indices,
 {
     int rc = check_step(args, cache_indices != nullptr);
     if (rc != GDN_OK) return rc;
+    if (args->state_dtype != GDN_F32) return GDN_ERR_DTYPE;
     if (!ring) return GDN_ERR_NULL;
     if (ring->L < 1 || ring->L > 64) return GDN_ERR_ARG;
     if (!dtype_ok(ring->ring_dtype)) return GDN_ERR_DTYPE;

@@ -65,7 +65,7 @@ __global__ void __launch_bounds__(kThreads, 2) buffered_kernel(const __grid_cons
         return;
     }
     const bool flush = p == L - 1;
-    float *S = a.state + ((size_t)slot * HV + hv) * (size_t)V * K;
+    float *S = static_cast<float *>(a.state) + ((size_t)slot * HV + hv) * (size_t)V * K;
 
     TL t;
     t.init();

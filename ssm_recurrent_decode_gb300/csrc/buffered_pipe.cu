@@ -181,7 +181,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1) buffered_pipe_kernel(const __
                 mbar_arrive_expect_tx(&full[st], bytes);
                 if (status == 0) {
                     const int b = tile / HV, hv = tile - b * HV, h = hv / G;
-                    const float *S = a.state + ((size_t)slot * HV + hv) * (size_t)(V * K);
+                    const float *S = static_cast<const float *>(a.state) + ((size_t)slot * HV + hv) * (size_t)(V * K);
                     bulk_g2s_hint(stage, S, 128u * 128u * 4u, &full[st], pol);
                     bulk_g2s(stage + lay.q, static_cast<const Tin *>(a.q) + (size_t)b * a.q_stride + (size_t)h * K, 128u * es, &full[st]);
                     bulk_g2s(stage + lay.k, static_cast<const Tin *>(a.k) + (size_t)b * a.k_stride + (size_t)h * K, 128u * es, &full[st]);
@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1) buffered_pipe_kernel(const __
         }
         if (flush) {
             // S = Gamma S_c + delta k^T + sum_j d_j (c_j k_j)^T, eight rows at a time
-            float *S = a.state + ((size_t)slot * HV + hv) * (size_t)(V * K);
+            float *S = static_cast<float *>(a.state) + ((size_t)slot * HV + hv) * (size_t)(V * K);
 #pragma unroll
             for (int i8 = 0; i8 < TL::R; i8 += 8) {
                 float4 acc[8];

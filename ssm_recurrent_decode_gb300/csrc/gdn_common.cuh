@@ -54,6 +54,23 @@ template <> __device__ __forceinline__ void store4<bf16>(bf16 *p, float4 v)
 __device__ __forceinline__ float4 ld_stream(const float *p) { return __ldcs(reinterpret_cast<const float4 *>(p)); }
 __device__ __forceinline__ void st_stream(float *p, float4 v) { __stcs(reinterpret_cast<float4 *>(p), v); }
 
+// bf16 state storage: four consecutive values as one 8-byte access, widened to / rounded from fp32
+__device__ __forceinline__ float4 ld_stream(const bf16 *p)
+{
+    const uint2 raw = __ldcs(reinterpret_cast<const uint2 *>(p));
+    return make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
+                       __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u));
+}
+__device__ __forceinline__ void st_stream(bf16 *p, float4 v)
+{
+    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+    uint2 raw;
+    raw.x = *reinterpret_cast<uint32_t *>(&lo);
+    raw.y = *reinterpret_cast<uint32_t *>(&hi);
+    __stcs(reinterpret_cast<uint2 *>(p), raw);
+}
+
 // ---------------------------------------------------------------------------------------------
 // small vector arithmetic
 // ---------------------------------------------------------------------------------------------

@@ -63,7 +63,8 @@ struct Tile {
     // one lane of each group of DUP identical lanes writes the row's results
     __device__ __forceinline__ bool writer() const { return (sub % DUP) == 0; }
 
-    __device__ __forceinline__ void load(const float *tile, int V, int row0)
+    template <typename TS>
+    __device__ __forceinline__ void load(const TS *tile, int V, int row0)
     {
 #pragma unroll
         for (int i = 0; i < R; ++i) {
@@ -123,8 +124,9 @@ struct Tile {
         return __shfl_up_sync(kFull, dm, HALF);
     }
 
-    // S' = S * dec + delta k^T, written back with streaming stores
-    __device__ __forceinline__ void update_store(float *tile, int V, int row0, float4 dec,
+    // S' = S * dec + delta k^T, written back with streaming stores (rounded for a bf16 state)
+    template <typename TS>
+    __device__ __forceinline__ void update_store(TS *tile, int V, int row0, float4 dec,
                                                  float4 kh, const float (&dv)[M])
     {
 #pragma unroll

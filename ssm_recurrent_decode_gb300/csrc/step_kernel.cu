@@ -1,6 +1,9 @@
 // step_kernel.cu -- the packed / indexed single-token decode step (gdn_decode_step and
 // gdn_decode_step_indexed).
 //
+// The state is fp32, or bf16 when it is stored in bf16 (8-byte accesses of four values, fp32
+// arithmetic, the updated tile rounded to nearest even as it is stored).
+//
 // Grid: one CTA per (row b, value head hv), blockIdx.x = b * HV + hv, so the G value heads that
 // share a q/k head sit next to each other and find its q/k in L2. Each CTA streams its 64 KB
 // (K = V = 128) fp32 tile in with 16-byte loads, takes S.(Dk) and S.(Dq) from registers, and
@@ -17,7 +20,7 @@
 
 namespace gdn {
 
-template <int K, typename Tin>
+template <int K, typename Tin, typename TS>
 __global__ void __launch_bounds__(kThreads, 2) step_kernel(const __grid_constant__ StepLaunch P)
 {
     using TL = Tile<K>;
@@ -36,7 +39,7 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const __grid_constant
             return;
         }
     }
-    float *S = a.state + ((size_t)slot * HV + hv) * (size_t)V * K;
+    TS *S = static_cast<TS *>(a.state) + ((size_t)slot * HV + hv) * (size_t)V * K;
 
     TL t;
     t.init();
@@ -82,29 +85,31 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const __grid_constant
     }
 }
 
-template <int K, typename Tin>
+template <int K, typename Tin, typename TS>
 static int launch_step_t(const StepLaunch &p, cudaStream_t stream)
 {
     const unsigned tiles = (unsigned)p.a.B * (unsigned)p.a.HV;
-    step_kernel<K, Tin><<<tiles, kThreads, 0, stream>>>(p);
+    step_kernel<K, Tin, TS><<<tiles, kThreads, 0, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
 }
 
-template <typename Tin>
+template <typename Tin, typename TS>
 static int launch_step_k(const StepLaunch &p, cudaStream_t stream)
 {
     switch (p.a.K) {
-    case 16: return launch_step_t<16, Tin>(p, stream);
-    case 32: return launch_step_t<32, Tin>(p, stream);
-    case 64: return launch_step_t<64, Tin>(p, stream);
-    case 128: return launch_step_t<128, Tin>(p, stream);
+    case 16: return launch_step_t<16, Tin, TS>(p, stream);
+    case 32: return launch_step_t<32, Tin, TS>(p, stream);
+    case 64: return launch_step_t<64, Tin, TS>(p, stream);
+    case 128: return launch_step_t<128, Tin, TS>(p, stream);
     default: return GDN_ERR_SHAPE;
     }
 }
 
 int launch_step(const StepLaunch &p, cudaStream_t stream)
 {
-    return p.a.in_dtype == GDN_BF16 ? launch_step_k<bf16>(p, stream) : launch_step_k<float>(p, stream);
+    if (p.a.state_dtype == GDN_BF16)
+        return p.a.in_dtype == GDN_BF16 ? launch_step_k<bf16, bf16>(p, stream) : launch_step_k<float, bf16>(p, stream);
+    return p.a.in_dtype == GDN_BF16 ? launch_step_k<bf16, float>(p, stream) : launch_step_k<float, float>(p, stream);
 }
 
 }  // namespace gdn
