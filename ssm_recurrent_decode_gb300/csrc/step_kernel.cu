@@ -85,11 +85,119 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const __grid_constant
     }
 }
 
+__device__ __forceinline__ float4 widen_bf16x4(uint2 raw)
+{
+    return make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
+                       __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u));
+}
+
+// bf16 state, one row pass (V <= rows per pass): each CTA takes two consecutive tiles and issues
+// both tiles' loads before computing either, so a CTA keeps as many bytes in flight as with an
+// fp32 tile. The rows stay in registers as packed bf16 (8 bytes per four values) and are widened
+// to fp32 where they are used; the update is rounded to nearest even as it is stored.
+template <int K, typename Tin>
+__global__ void __launch_bounds__(kThreads, 2) step_kernel_bf16_pair(const __grid_constant__ StepLaunch P)
+{
+    using TL = Tile<K>;
+    const gdn_step_args &a = P.a;
+    const int HV = a.HV, V = a.V;
+    const int ntiles = a.B * HV;
+    TL t;
+    t.init();
+    uint2 raw[2][TL::R];
+    bf16 *S[2];
+    bool run[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int tile = blockIdx.x * 2 + u;
+        run[u] = false;
+        S[u] = nullptr;
+        if (tile < ntiles) {
+            const int b = tile / HV, hv = tile - b * HV;
+            int slot = b;
+            bool skip = false;
+            if (P.idx) {
+                slot = P.idx[b];
+                const bool pad = slot == P.pad;
+                if (pad || slot < 0 || slot >= a.num_slots) {
+                    if (!pad && threadIdx.x == 0) raise_flag(a.err_flags, GDN_DEVERR_BAD_INDEX);
+                    const size_t out_base = ((size_t)b * HV + hv) * V;
+                    for (int r = threadIdx.x; r < V; r += kThreads) store_out(a.out, a.out_dtype, out_base + r, 0.f);
+                    skip = true;
+                }
+            }
+            if (!skip) {
+                run[u] = true;
+                S[u] = static_cast<bf16 *>(a.state) + ((size_t)slot * HV + hv) * (size_t)V * K;
+            }
+        }
+        if (run[u]) {
+#pragma unroll
+            for (int i = 0; i < TL::R; ++i) {
+                const int r = t.row(0, i);
+                raw[u][i] = r < V ? __ldcs(reinterpret_cast<const uint2 *>(S[u] + (size_t)r * K + t.col))
+                                  : make_uint2(0u, 0u);
+            }
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        if (!run[u]) continue;   // uniform over the CTA
+        const int tile = blockIdx.x * 2 + u;
+        const int b = tile / HV, hv = tile - b * HV, h = hv / P.G;
+        const size_t out_base = ((size_t)b * HV + hv) * V;
+        const Tin *qp = static_cast<const Tin *>(a.q) + (size_t)b * a.q_stride + (size_t)h * K;
+        const Tin *kp = static_cast<const Tin *>(a.k) + (size_t)b * a.k_stride + (size_t)h * K;
+        const Tin *vp = static_cast<const Tin *>(a.v) + (size_t)b * a.v_stride + (size_t)hv * V;
+        const float4 q4 = load4(qp + t.col), k4 = load4(kp + t.col);
+        float g, beta;
+        step_gates<Tin>(a, b, hv, g, beta);
+        const float4 kh = l2_normalise4<TL::LPR>(k4, a.use_qk_l2norm != 0, 1.f);
+        const float4 qh = l2_normalise4<TL::LPR>(q4, a.use_qk_l2norm != 0, P.scale);
+        const float kq = group_sum<TL::LPR>(dot4(kh, qh));
+        const float e = expf(g);
+        const float4 dec = make_float4(e, e, e, e);
+        const float4 kd = scale4(kh, e), qd = scale4(qh, e);
+        float vv[TL::M];
+#pragma unroll
+        for (int m = 0; m < TL::M; ++m) {
+            const int r = t.row(0, t.owned_chunk(m));
+            vv[m] = (t.holds_k_dot() && r < V) ? to_f32(vp[r]) : 0.f;
+        }
+        float x[TL::N];
+#pragma unroll
+        for (int i = 0; i < TL::R; ++i) {
+            const float4 sv = widen_bf16x4(raw[u][i]);
+            x[i] = dot4(sv, kd);
+            x[TL::R + i] = dot4(sv, qd);
+        }
+        t.reduce_scatter(x);
+        float dv[TL::M];
+#pragma unroll
+        for (int m = 0; m < TL::M; ++m) dv[m] = beta * (vv[m] - x[m]);
+#pragma unroll
+        for (int m = 0; m < TL::M; ++m) {
+            const float dq = t.delta_for_q(dv[m]);
+            const int r = t.row(0, t.owned_chunk(m));
+            if (!t.holds_k_dot() && r < V) store_out(a.out, a.out_dtype, out_base + r, fmaf(dq, kq, x[m]));
+        }
+#pragma unroll
+        for (int i = 0; i < TL::R; ++i) {
+            const float d = t.delta_of(dv, i);
+            const int r = t.row(0, i);
+            if (r < V) st_stream(S[u] + (size_t)r * K + t.col, decay_update4(dec, widen_bf16x4(raw[u][i]), d, kh));
+        }
+    }
+}
+
 template <int K, typename Tin, typename TS>
 static int launch_step_t(const StepLaunch &p, cudaStream_t stream)
 {
     const unsigned tiles = (unsigned)p.a.B * (unsigned)p.a.HV;
-    step_kernel<K, Tin, TS><<<tiles, kThreads, 0, stream>>>(p);
+    if (sizeof(TS) == 2 && K >= 64 && p.a.V <= Tile<K>::ROWS_PASS)
+        step_kernel_bf16_pair<K, Tin><<<(tiles + 1) / 2, kThreads, 0, stream>>>(p);
+    else
+        step_kernel<K, Tin, TS><<<tiles, kThreads, 0, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
 }
 
