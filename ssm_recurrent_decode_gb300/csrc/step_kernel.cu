@@ -20,22 +20,29 @@
 
 namespace gdn {
 
-template <int K, typename Tin, typename TS>
-__global__ void __launch_bounds__(kThreads, 2) step_kernel(const __grid_constant__ StepLaunch P)
+// R rows per warp: R = 16 for the bulk of the work (a CTA owns a whole tile, looping over row
+// passes when V is larger than 128); R = 8, 4 or 2 split a tile's rows over `splits` CTAs for small
+// batches, which have too few tiles to fill the GPU. Row dots are complete within a row, so the
+// split needs no exchange between CTAs; each CTA normalises q and k itself.
+template <int K, typename Tin, typename TS, int R>
+__global__ void __launch_bounds__(kThreads, R >= 16 ? 2 : 4) step_kernel(const __grid_constant__ StepLaunch P, int splits)
 {
-    using TL = Tile<K>;
+    using TL = Tile<K, R>;
     const gdn_step_args &a = P.a;
     const int HV = a.HV, V = a.V;
-    const int b = blockIdx.x / HV, hv = blockIdx.x - b * HV, h = hv / P.G;
+    const int tile = blockIdx.x / splits, blk = blockIdx.x - tile * splits;
+    const int b = tile / HV, hv = tile - b * HV, h = hv / P.G;
     const size_t out_base = ((size_t)b * HV + hv) * V;
+    const int first_row = blk * TL::ROWS_PASS, row_step = splits * TL::ROWS_PASS;
 
     int slot = b;
     if (P.idx) {
         slot = P.idx[b];
         const bool pad = slot == P.pad;
         if (pad || slot < 0 || slot >= a.num_slots) {   // uniform over the CTA
-            if (!pad && threadIdx.x == 0) raise_flag(a.err_flags, GDN_DEVERR_BAD_INDEX);
-            for (int r = threadIdx.x; r < V; r += kThreads) store_out(a.out, a.out_dtype, out_base + r, 0.f);
+            if (!pad && blk == 0 && threadIdx.x == 0) raise_flag(a.err_flags, GDN_DEVERR_BAD_INDEX);
+            for (int r = threadIdx.x; r < V; r += kThreads)
+                if ((r / TL::ROWS_PASS) % splits == blk) store_out(a.out, a.out_dtype, out_base + r, 0.f);
             return;
         }
     }
@@ -43,7 +50,7 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const __grid_constant
 
     TL t;
     t.init();
-    t.load(S, V, 0);   // the tile's loads go out first; everything below overlaps them
+    t.load(S, V, first_row);   // the tile's loads go out first; everything below overlaps them
 
     const Tin *qp = static_cast<const Tin *>(a.q) + (size_t)b * a.q_stride + (size_t)h * K;
     const Tin *kp = static_cast<const Tin *>(a.k) + (size_t)b * a.k_stride + (size_t)h * K;
@@ -59,8 +66,8 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const __grid_constant
     const float4 dec = make_float4(e, e, e, e);
     const float4 kd = scale4(kh, e), qd = scale4(qh, e);
 
-    for (int row0 = 0; row0 < V; row0 += TL::ROWS_PASS) {
-        if (row0) t.load(S, V, row0);
+    for (int row0 = first_row; row0 < V; row0 += row_step) {
+        if (row0 != first_row) t.load(S, V, row0);
         float vv[TL::M];
 #pragma unroll
         for (int m = 0; m < TL::M; ++m) {
@@ -79,7 +86,7 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const __grid_constant
         for (int m = 0; m < TL::M; ++m) {
             const float dq = t.delta_for_q(dv[m]);
             const int r = t.row(row0, t.owned_chunk(m));
-            if (!t.holds_k_dot() && r < V) store_out(a.out, a.out_dtype, out_base + r, fmaf(dq, kq, x[m]));
+            if (!t.holds_k_dot() && t.writer() && r < V) store_out(a.out, a.out_dtype, out_base + r, fmaf(dq, kq, x[m]));
         }
         t.update_store(S, V, row0, dec, kh, dv);
     }
@@ -105,13 +112,13 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel_bf16_pair(const __gri
     TL t;
     t.init();
     uint2 raw[2][TL::R];
-    bf16 *S[2];
+    int slots[2];
     bool run[2];
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
         const int tile = blockIdx.x * 2 + u;
         run[u] = false;
-        S[u] = nullptr;
+        slots[u] = 0;
         if (tile < ntiles) {
             const int b = tile / HV, hv = tile - b * HV;
             int slot = b;
@@ -128,15 +135,14 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel_bf16_pair(const __gri
             }
             if (!skip) {
                 run[u] = true;
-                S[u] = static_cast<bf16 *>(a.state) + ((size_t)slot * HV + hv) * (size_t)V * K;
-            }
-        }
-        if (run[u]) {
+                slots[u] = slot;
+                const bf16 *S = static_cast<const bf16 *>(a.state) + ((size_t)slot * HV + hv) * (size_t)V * K;
 #pragma unroll
-            for (int i = 0; i < TL::R; ++i) {
-                const int r = t.row(0, i);
-                raw[u][i] = r < V ? __ldcs(reinterpret_cast<const uint2 *>(S[u] + (size_t)r * K + t.col))
-                                  : make_uint2(0u, 0u);
+                for (int i = 0; i < TL::R; ++i) {
+                    const int r = t.row(0, i);
+                    raw[u][i] = r < V ? __ldcs(reinterpret_cast<const uint2 *>(S + (size_t)r * K + t.col))
+                                      : make_uint2(0u, 0u);
+                }
             }
         }
     }
@@ -181,23 +187,55 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel_bf16_pair(const __gri
             const int r = t.row(0, t.owned_chunk(m));
             if (!t.holds_k_dot() && r < V) store_out(a.out, a.out_dtype, out_base + r, fmaf(dq, kq, x[m]));
         }
+        bf16 *S = static_cast<bf16 *>(a.state) + ((size_t)slots[u] * HV + hv) * (size_t)V * K;
 #pragma unroll
         for (int i = 0; i < TL::R; ++i) {
             const float d = t.delta_of(dv, i);
             const int r = t.row(0, i);
-            if (r < V) st_stream(S[u] + (size_t)r * K + t.col, decay_update4(dec, widen_bf16x4(raw[u][i]), d, kh));
+            if (r < V) st_stream(S + (size_t)r * K + t.col, decay_update4(dec, widen_bf16x4(raw[u][i]), d, kh));
         }
     }
+}
+
+static int sm_count()
+{
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    return sms;
+}
+
+template <int K, typename Tin, typename TS, int R>
+static void launch_rows(const StepLaunch &p, unsigned tiles, cudaStream_t stream)
+{
+    const int splits = R >= 16 ? 1 : (p.a.V + Tile<K, R>::ROWS_PASS - 1) / Tile<K, R>::ROWS_PASS;
+    step_kernel<K, Tin, TS, R><<<tiles * (unsigned)splits, kThreads, 0, stream>>>(p, splits);
 }
 
 template <int K, typename Tin, typename TS>
 static int launch_step_t(const StepLaunch &p, cudaStream_t stream)
 {
     const unsigned tiles = (unsigned)p.a.B * (unsigned)p.a.HV;
-    if (sizeof(TS) == 2 && K >= 64 && p.a.V <= Tile<K>::ROWS_PASS)
-        step_kernel_bf16_pair<K, Tin><<<(tiles + 1) / 2, kThreads, 0, stream>>>(p);
-    else
-        step_kernel<K, Tin, TS><<<tiles, kThreads, 0, stream>>>(p);
+    // Enough CTAs to cover every SM about four times over: whole tiles when the batch allows it,
+    // otherwise the fewest row splits that get there (at most 8 per tile at V = 128).
+    const unsigned target = 4u * (unsigned)(sm_count() > 0 ? sm_count() : 152);
+    auto ctas = [&](int rows_pass) { return tiles * (unsigned)((p.a.V + rows_pass - 1) / rows_pass); };
+    if (tiles >= target) {
+        bool paired = false;
+        if constexpr (sizeof(TS) == 2 && K >= 64) {
+            if (p.a.V <= Tile<K>::ROWS_PASS) {
+                step_kernel_bf16_pair<K, Tin><<<(tiles + 1) / 2, kThreads, 0, stream>>>(p);
+                paired = true;
+            }
+        }
+        if (!paired) launch_rows<K, Tin, TS, 16>(p, tiles, stream);
+    } else if (ctas(Tile<K, 8>::ROWS_PASS) >= target) {
+        launch_rows<K, Tin, TS, 8>(p, tiles, stream);
+    } else if (ctas(Tile<K, 4>::ROWS_PASS) >= target) {
+        launch_rows<K, Tin, TS, 4>(p, tiles, stream);
+    } else {
+        launch_rows<K, Tin, TS, 2>(p, tiles, stream);
+    }
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
 }
 

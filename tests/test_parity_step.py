@@ -94,9 +94,23 @@ def test_shapes_fp32(K, G):
 
 
 def test_ragged_multi_pass_rows():
-    """V = 200 at K = 128 needs two row passes, the second one ragged."""
+    """V = 200 at K = 128 with few tiles: the rows are split over 13 CTAs per tile, the last ragged."""
     wo, ws, _ = _run(2, 1, 2, 128, 200, "f32", "f32", seed=5, steps=2)
     assert wo <= TOL_F32 and ws <= TOL_F32
+
+
+def test_ragged_multi_pass_rows_whole_tiles():
+    """V = 200 at K = 128 with 640 tiles: one CTA per tile, two row passes, the second ragged."""
+    wo, ws, _ = _run(160, 2, 4, 128, 200, "f32", "f32", seed=6, steps=1)
+    assert wo <= TOL_F32 and ws <= TOL_F32
+
+
+@pytest.mark.parametrize("B", [1, 4, 16, 64])
+def test_row_split_batches(B):
+    """Small batches split each tile's rows over several CTAs (8 at B = 1, 2 at B = 16); the
+    results do not depend on the split."""
+    wo, ws, flags = _run(B, 16, 32, 128, 128, "bf16", "f32", seed=300 + B, steps=2)
+    assert wo <= TOL_F32 and ws <= TOL_F32 and flags == 0, (B, wo, ws)
 
 
 @pytest.mark.parametrize("out_dtype", ["bf16", "f32"])
