@@ -283,6 +283,39 @@ class Harness:
             clocks.mark(t0, t1)
         return e0.elapsed_time(e1) / steps, (clocks.stop() if clocks else None)
 
+    def time_graph(self, step, steps, warmup, per_graph):
+        """Warm up eagerly, capture `per_graph` calls of step(i) into one CUDA graph, and time
+        replays of it (CUDA events on the replay stream, barrier + synchronize on both sides).
+        Returns (ms per step, steps timed, clocks record). Replaying a graph takes the host's
+        per-call cost out of the measurement, which otherwise dominates at small batches."""
+        torch = self.torch
+        for i in range(warmup):
+            step(i)
+        self.barrier()
+        s = torch.cuda.Stream(self.dev)
+        s.wait_stream(torch.cuda.current_stream(self.dev))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for i in range(per_graph):
+                step(i)
+        reps = max(1, steps // per_graph)
+        with torch.cuda.stream(s):
+            g.replay()
+        clocks = ClockSampler(self.dev.index)
+        clocks.start()
+        self.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.time()
+        with torch.cuda.stream(s):
+            e0.record(s)
+            for _ in range(reps):
+                g.replay()
+            e1.record(s)
+        self.barrier()
+        t1 = time.time()
+        clocks.mark(t0, t1)
+        return e0.elapsed_time(e1) / (reps * per_graph), reps * per_graph, clocks.stop()
+
     def finish(self, line):
         if self.rank == 0 and line is not None:
             print(json.dumps(line), flush=True)
@@ -375,13 +408,15 @@ def run_packed(args):
         syn.fill_normal_(s, 1234 + h.rank, syn.Tag.STATE, 0, 1.0, layer=p)
         pools.append(s)
     q, k, v = gdn.split_mixed_qkv(w["x"], H, HV, K, V)
-    sid = h.stream.cuda_stream
+    calls = [gdn.gdn_decode_step_indexed(q, k, v, pool, w["out"], w["idx"], H=H, a=w["a"], b=w["b"],
+                                         A_log=w["A_log"], dt_bias=w["dt_bias"], prepare=True)
+             for pool in pools]
 
     def step(i):
-        gdn.gdn_decode_step_indexed(q, k, v, pools[i % n_pools], w["out"], w["idx"], H=H, a=w["a"],
-                                    b=w["b"], A_log=w["A_log"], dt_bias=w["dt_bias"], stream=sid)
+        calls[i % n_pools]()
 
-    ms, clk = h.time_steps(step, args.steps, args.warmup)
+    per_graph = max(64, n_pools)
+    ms, steps, clk = h.time_graph(step, args.steps, args.warmup, per_graph)
 
     # end to end through the public API: pinned host inputs in, output back to pinned host memory
     hx = w["x"].cpu().pin_memory()
@@ -395,7 +430,7 @@ def run_packed(args):
         step(i)
         hout.copy_(w["out"], non_blocking=True)
 
-    e2e_steps = max(1, min(args.steps, 2000))
+    e2e_steps = max(1, min(steps, 2000))
     ms_e2e, _ = h.time_steps(e2e_step, e2e_steps, 3, sample_clocks=False)
     h2d = (hx.numel() + ha.numel() + hb.numel()) * 2
     d2h = hout.numel() * 2
@@ -407,15 +442,16 @@ def run_packed(args):
     gbs = h.world * state_bytes / (ms * 1e-3) / 1e9
     peak, _ = hbm_peak()
     line = base_line(
-        h, gbs, ms, args.steps, args.warmup,
+        h, gbs, ms, steps, args.warmup,
         f"gdn packed decode over a slot pool: B={B} H={H} HV={HV} K=V={K}, bf16 mixed_qkv/a/b/out, "
         f"{args.state_dtype} state [{B},{HV},{V},{K}], permuted int32 cache indices",
         {"B": B, "H": H, "HV": HV, "K": K, "V": V, "input_dtype": "bf16", "state_dtype": args.state_dtype,
          "state_bytes_per_step": state_bytes, "state_pools": n_pools,
          "l2": (f"state of {state_bytes / 2 / 1e9:.2f} GB read per step, larger than the L2: no flush "
                 f"between steps" if n_pools == 1 else
-                f"{n_pools} state pools rotated, at least 4x the L2 size per pass")},
-        args.steps)
+                f"{n_pools} state pools rotated, at least 4x the L2 size per pass"),
+         "timing": f"CUDA-graph replays of {per_graph} calls; e2e: direct calls"},
+        steps)
     line["pct_of_peak"] = round(100 * gbs / h.world / peak, 2)
     line["roofline"] = roofline(state_bytes + packed_io_bytes(B, H, HV, K, V), ms, "step",
                                 f"packed_B{B}" + ("_bf16state" if args.state_dtype == "bf16" else ""))
@@ -443,24 +479,25 @@ def run_buffered(args):
     k_cache = torch.zeros((B, H, L, K), dtype=torch.bfloat16, device=h.dev)
     g_cache = torch.zeros((B, HV, L), dtype=torch.float32, device=h.dev)
     pos = [torch.full((B,), p, dtype=torch.int32, device=h.dev) for p in range(L)]
-    sid = h.stream.cuda_stream
+    calls = [gdn.gdn_decode_buffered(q, k, v, w["state"], w["out"], d_cache, k_cache, g_cache, pos[p],
+                                     cache_indices=w["idx"], H=H, a=w["a"], b=w["b"],
+                                     A_log=w["A_log"], dt_bias=w["dt_bias"], prepare=True)
+             for p in range(L)]
 
     def step(i):
-        gdn.gdn_decode_buffered(q, k, v, w["state"], w["out"], d_cache, k_cache, g_cache,
-                                pos[i % L], cache_indices=w["idx"], H=H, a=w["a"], b=w["b"],
-                                A_log=w["A_log"], dt_bias=w["dt_bias"], stream=sid)
+        calls[i % L]()
 
-    steps = max(L, (args.steps // L) * L)
     warm = max(args.warmup, L)
     warm = ((warm + L - 1) // L) * L
-    ms, clk = h.time_steps(step, steps, warm)
+    per_graph = L * max(1, 64 // L)
+    ms, steps, clk = h.time_graph(step, max(L, args.steps), warm, per_graph)
     # per-phase times: events around each call of a cycle, averaged over cycles
     cycles = max(1, min(50, steps // L))
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(cycles * L)]
     h.barrier()
     for i in range(cycles * L):
         ev[i][0].record(h.stream)
-        step(i)
+        calls[i % L](h.stream.cuda_stream)
         ev[i][1].record(h.stream)
     h.barrier()
     phase_ms = [statistics.mean(ev[c * L + p][0].elapsed_time(ev[c * L + p][1]) for c in range(cycles))
@@ -478,6 +515,7 @@ def run_buffered(args):
         h, gbs, ms, steps, warm,
         f"gdn buffered output-only decode: B={B} H={H} HV={HV} K=V={K}, L={L}, bf16 rings, "
         f"fp32 checkpoint state, all phases timed", {"B": B, "H": H, "HV": HV, "K": K, "V": V, "L": L,
+        "timing": f"CUDA-graph replays of {per_graph} calls (whole cycles); phase times: direct calls",
         "state_bytes_per_step_mean": state_traffic,
         "packed_equivalent_state_GBs": round(2 * S / (ms * 1e-3) / 1e9, 2)}, steps)
     line["roofline"] = roofline(state_traffic + ring_append + ring_read_mean + io, ms, "buffered",
@@ -526,15 +564,17 @@ def run_fused(args):
         s = h.torch.empty_like(w["state"])
         syn.fill_normal_(s, 555 + h.rank, syn.Tag.STATE, 0, 1.0, layer=p)
         pools.append(s)
-    sid = h.stream.cuda_stream
+    calls = [gdn.gdn_decode_fused(w["x"], w["conv_w"], w["conv_state"], w["raw_g"], w["raw_beta"],
+                                  w["A_log"], w["dt_bias"], pool, w["idx"], w["out_gate"],
+                                  w["norm_w"], w["out"], pad_slot_id=0, gate_kind="kda",
+                                  kda_gate_form=0, gate_act="silu", prepare=True)
+             for pool in pools]
 
     def step(i):
-        gdn.gdn_decode_fused(w["x"], w["conv_w"], w["conv_state"], w["raw_g"], w["raw_beta"],
-                             w["A_log"], w["dt_bias"], pools[i % n_pools], w["idx"], w["out_gate"],
-                             w["norm_w"], w["out"], pad_slot_id=0, gate_kind="kda",
-                             kda_gate_form=0, gate_act="silu", stream=sid)
+        calls[i % n_pools]()
 
-    ms, clk = h.time_steps(step, args.steps, args.warmup)
+    per_graph = max(64, n_pools)
+    ms, steps, clk = h.time_graph(step, args.steps, args.warmup, per_graph)
     (ms,) = max_over_ranks([ms], h.world)
     if h.rank != 0:
         return h.finish(None)
@@ -548,12 +588,13 @@ def run_fused(args):
           + T * dim * 2)             # out
     gbs = h.world * state_bytes / (ms * 1e-3) / 1e9
     line = base_line(
-        h, gbs, ms, args.steps, args.warmup,
+        h, gbs, ms, steps, args.warmup,
         f"fused KDA decode: T={T} tokens, {heads} heads x {D}, conv width 4 ({args.layout} conv "
         f"state), per-key decay bounded at -5, gated RMSNorm with silu",
         {"T": T, "heads": heads, "head_dim": D, "state_bytes_per_step": state_bytes,
          "state_pools": n_pools,
-         "l2": f"{n_pools} state pool(s) rotated, at least 4x the L2 size per pass"}, args.steps)
+         "l2": f"{n_pools} state pool(s) rotated, at least 4x the L2 size per pass",
+         "timing": f"CUDA-graph replays of {per_graph} calls"}, steps)
     line["roofline"] = roofline(state_bytes + io, ms, "fused", f"fused_T{T}")
     line["clocks"] = clk
     return h.finish(line)

@@ -24,7 +24,7 @@ from . import _build
 __all__ = [
     "lib", "build", "GdnError", "GdnStepArgs", "GdnRingArgs", "GdnFusedArgs",
     "gdn_decode_step", "gdn_decode_step_indexed", "gdn_decode_buffered", "gdn_decode_fused",
-    "gdn_strerror", "split_mixed_qkv", "fused_recurrent_gated_delta_rule_packed_decode",
+    "gdn_strerror", "split_mixed_qkv", "fused_recurrent_gated_delta_rule_packed_decode", "PreparedCall",
     "GDN_F32", "GDN_BF16", "GDN_DEVERR_BAD_INDEX", "GDN_DEVERR_BAD_WRITE_POS", "GDN_DEVERR_TIMEOUT",
     "EXPORTS",
 ]
@@ -224,39 +224,64 @@ def _check(fn: str, rc: int):
         raise GdnError(fn, rc)
 
 
+class PreparedCall:
+    """A library call whose argument structs were built once (``prepare=True`` on an entry
+    point). Calling it only launches, which takes a few microseconds of host time instead of
+    re-marshalling every tensor; that matters for small batches, where the kernels take a few
+    microseconds themselves. The tensors it was built from must stay alive with the same storage;
+    each launch reads their current contents."""
+
+    __slots__ = ("_name", "_fn", "_args", "_keep")
+
+    def __init__(self, name, fn, args, keep):
+        self._name, self._fn, self._args, self._keep = name, fn, args, keep
+
+    def __call__(self, stream=None):
+        _check(self._name, self._fn(*self._args, _stream(stream)))
+
+
+def _run_or_prepare(name, args, keep, stream, prepare, result):
+    fn = getattr(lib(), name)
+    if prepare:
+        return PreparedCall(name, fn, args, keep)
+    _check(name, fn(*args, _stream(stream)))
+    return result
+
+
 # ------------------------------------------------------------------------------------------------
 # entry points
 # ------------------------------------------------------------------------------------------------
 def gdn_decode_step(q, k, v, state, out, *, H=None, a=None, b=None, A_log=None, dt_bias=None,
-                    g=None, beta=None, scale=None, use_qk_l2norm=True, err_flags=None, stream=None):
+                    g=None, beta=None, scale=None, use_qk_l2norm=True, err_flags=None, stream=None,
+                    prepare=False):
     """One decode step, row b on slot b. q, k: [B, H*K] (or [B, H, K]) row views; v: [B, HV*V];
     gates either raw (a, b [B, HV] in the dtype of q; A_log, dt_bias [HV] fp32) or direct
     (g, beta [B, HV] fp32); state [num_slots, HV, V, K] fp32 (or bf16: stored in bf16, computed in
-    fp32) updated in place; out [B, HV, V] (or [B, 1, HV, V]) fp32 or bf16."""
+    fp32) updated in place; out [B, HV, V] (or [B, 1, HV, V]) fp32 or bf16.
+    prepare=True returns a PreparedCall instead of launching (every entry point takes it)."""
     s = _step_args(q, k, v, state, out, H=H, a=a, b=b, A_log=A_log, dt_bias=dt_bias, g=g,
                    beta=beta, scale=scale, use_qk_l2norm=use_qk_l2norm, err_flags=err_flags)
-    _check("gdn_decode_step", lib().gdn_decode_step(ctypes.byref(s), _stream(stream)))
-    return out
+    return _run_or_prepare("gdn_decode_step", (ctypes.byref(s),), (s,), stream, prepare, out)
 
 
 def gdn_decode_step_indexed(q, k, v, state, out, cache_indices, *, pad_slot_id=-1, H=None, a=None,
                             b=None, A_log=None, dt_bias=None, g=None, beta=None, scale=None,
-                            use_qk_l2norm=True, err_flags=None, stream=None):
+                            use_qk_l2norm=True, err_flags=None, stream=None, prepare=False):
     """As gdn_decode_step, with row b on slot cache_indices[b] (int32 [B] on the device); rows
     whose index is pad_slot_id are skipped (state untouched, out zeroed)."""
     torch = _torch()
     s = _step_args(q, k, v, state, out, H=H, a=a, b=b, A_log=A_log, dt_bias=dt_bias, g=g,
                    beta=beta, scale=scale, use_qk_l2norm=use_qk_l2norm, err_flags=err_flags)
     idx = _ptr(_dense(cache_indices, "cache_indices"), "cache_indices", torch.int32)
-    _check("gdn_decode_step_indexed",
-           lib().gdn_decode_step_indexed(ctypes.byref(s), idx, int(pad_slot_id), _stream(stream)))
-    return out
+    return _run_or_prepare("gdn_decode_step_indexed",
+                           (ctypes.byref(s), ctypes.c_void_p(idx), ctypes.c_int32(int(pad_slot_id))),
+                           (s,), stream, prepare, out)
 
 
 def gdn_decode_buffered(q, k, v, state, out, d_cache, k_cache, g_cache, write_pos, *,
                         cache_indices=None, pad_slot_id=-1, H=None, a=None, b=None, A_log=None,
                         dt_bias=None, g=None, beta=None, scale=None, use_qk_l2norm=True,
-                        err_flags=None, kernel="auto", stream=None):
+                        err_flags=None, kernel="auto", stream=None, prepare=False):
     """Buffered output-only decode. state holds the checkpoints; d_cache [num_slots, HV, L, V],
     k_cache [num_slots, H, L, K] (both fp32 or both bf16), g_cache [num_slots, HV, L] fp32;
     write_pos int32 [B] is read, never advanced (the caller moves it to (p+1) % L).
@@ -282,16 +307,16 @@ def gdn_decode_buffered(q, k, v, state, out, d_cache, k_cache, g_cache, write_po
     r.kernel = GDN_KERNEL[kernel]
     idx = None if cache_indices is None else _ptr(_dense(cache_indices, "cache_indices"),
                                                   "cache_indices", torch.int32)
-    _check("gdn_decode_buffered",
-           lib().gdn_decode_buffered(ctypes.byref(s), idx, int(pad_slot_id), ctypes.byref(r),
-                                     _stream(stream)))
-    return out
+    return _run_or_prepare("gdn_decode_buffered",
+                           (ctypes.byref(s), ctypes.c_void_p(idx), ctypes.c_int32(int(pad_slot_id)),
+                            ctypes.byref(r)), (s, r), stream, prepare, out)
 
 
 def gdn_decode_fused(x, conv_w, conv_state, raw_g, raw_beta, A_log, dt_bias, state, state_indices,
                      out_gate, norm_w, out, *, conv_b=None, pad_slot_id=0, gate_kind="kda",
                      kda_gate_form=0, lower_bound=-5.0, scale=None, use_qk_l2norm=True,
-                     norm_eps=1e-5, gate_act="silu", err_flags=None, kernel="auto", stream=None):
+                     norm_eps=1e-5, gate_act="silu", err_flags=None, kernel="auto", stream=None,
+                     prepare=False):
     """Fused decode: conv update -> delta step -> gated RMSNorm, one launch.
     kernel: "auto" (the persistent pipelined kernel when head_dim is 128, the conv state is in the
     DS or SD layout and rows are 16-byte aligned), "tile" or "pipe" to force one.
@@ -335,8 +360,7 @@ def gdn_decode_fused(x, conv_w, conv_state, raw_g, raw_beta, A_log, dt_bias, sta
     f.out = _ptr(_dense(out, "out"), "out", torch.bfloat16)
     f.err_flags = _ptr(err_flags, "err_flags", torch.int32)
     f.kernel = GDN_KERNEL[kernel]
-    _check("gdn_decode_fused", lib().gdn_decode_fused(ctypes.byref(f), _stream(stream)))
-    return out
+    return _run_or_prepare("gdn_decode_fused", (ctypes.byref(f),), (f,), stream, prepare, out)
 
 
 def fused_recurrent_gated_delta_rule_packed_decode(mixed_qkv, a, b, A_log, dt_bias, scale,
