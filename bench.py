@@ -418,22 +418,55 @@ def run_packed(args):
     per_graph = max(64, n_pools)
     ms, steps, clk = h.time_graph(step, args.steps, args.warmup, per_graph)
 
-    # end to end through the public API: pinned host inputs in, output back to pinned host memory
+    # End to end through the public API, with host buffers: every step copies its inputs from
+    # pinned host memory and its output back to pinned host memory. Copies run on their own
+    # streams over two sets of device buffers, so step i's compute overlaps step i+1's input copy
+    # and step i-1's output copy (events order each buffer's reuse).
     hx = w["x"].cpu().pin_memory()
     ha, hb = w["a"].cpu().pin_memory(), w["b"].cpu().pin_memory()
-    hout = torch.empty(w["out"].shape, dtype=w["out"].dtype).pin_memory()
+    hout = [torch.empty(w["out"].shape, dtype=w["out"].dtype).pin_memory() for _ in range(2)]
+    dev_in = [(w["x"], w["a"], w["b"]), tuple(torch.empty_like(t) for t in (w["x"], w["a"], w["b"]))]
+    dev_out = [w["out"], torch.empty_like(w["out"])]
+    e2e_calls = []
+    for j in range(2):
+        qj, kj, vj = gdn.split_mixed_qkv(dev_in[j][0], H, HV, K, V)
+        e2e_calls.append(gdn.gdn_decode_step_indexed(qj, kj, vj, pools[0], dev_out[j], w["idx"], H=H,
+                                                     a=dev_in[j][1], b=dev_in[j][2], A_log=w["A_log"],
+                                                     dt_bias=w["dt_bias"], prepare=True))
+    s_comp = torch.cuda.current_stream(h.dev)
+    s_in, s_out = torch.cuda.Stream(h.dev), torch.cuda.Stream(h.dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step(i):
-        w["x"].copy_(hx, non_blocking=True)
-        w["a"].copy_(ha, non_blocking=True)
-        w["b"].copy_(hb, non_blocking=True)
-        step(i)
-        hout.copy_(w["out"], non_blocking=True)
+    def e2e_run(n):
+        for i in range(n):
+            j = i % 2
+            if i >= 2:
+                s_in.wait_event(ev_done[j])        # step i-2 has consumed this input set
+            with torch.cuda.stream(s_in):
+                for d_t, h_t in zip(dev_in[j], (hx, ha, hb)):
+                    d_t.copy_(h_t, non_blocking=True)
+                ev_in[j].record(s_in)
+            s_comp.wait_event(ev_in[j])
+            if i >= 2:
+                s_comp.wait_event(ev_out[j])       # step i-2's output has been copied out
+            e2e_calls[j](s_comp.cuda_stream)
+            ev_done[j].record(s_comp)
+            s_out.wait_event(ev_done[j])
+            with torch.cuda.stream(s_out):
+                hout[j].copy_(dev_out[j], non_blocking=True)
+                ev_out[j].record(s_out)
 
-    e2e_steps = max(1, min(steps, 2000))
-    ms_e2e, _ = h.time_steps(e2e_step, e2e_steps, 3, sample_clocks=False)
+    e2e_steps = max(2, min(steps, 2000))
+    e2e_run(4)
+    h.barrier()
+    t0 = time.perf_counter()
+    e2e_run(e2e_steps)
+    h.barrier()
+    ms_e2e = (time.perf_counter() - t0) * 1e3 / e2e_steps
     h2d = (hx.numel() + ha.numel() + hb.numel()) * 2
-    d2h = hout.numel() * 2
+    d2h = hout[0].numel() * 2
     ms, ms_e2e = max_over_ranks([ms, ms_e2e], h.world)
     if h.rank != 0:
         return h.finish(None)
@@ -458,7 +491,11 @@ def run_packed(args):
     line["cpu_baseline"] = cpu_baseline(H, HV, K, V, seed=7, budget_s=args.cpu_budget)
     line["e2e"] = {"value": round(h.world * state_bytes / (ms_e2e * 1e-3) / 1e9, 2), "unit": "GB/s",
                    "us_per_step": round(ms_e2e * 1e3, 3), "h2d_bytes_per_step": h2d,
-                   "d2h_bytes_per_step": d2h}
+                   "d2h_bytes_per_step": d2h,
+                   "how": "prepared gdn_decode_step_indexed calls; per step a pinned-host -> device "
+                          "copy of mixed_qkv, a, b and a device -> pinned-host copy of out, on copy "
+                          "streams overlapping the neighbouring steps; host wall clock between "
+                          "synchronizations"}
     line["clocks"] = clk
     return h.finish(line)
 
