@@ -12,6 +12,9 @@ Readings of points the sources leave open (also listed in the design doc):
   * L2 norm is x / sqrt(sum x^2 + 1e-6); the K^-1/2 scale multiplies the normalised q;
   * the state tile is S[V, K] (key index contiguous) and u = S k, o = S q.
 
+The Mamba-1 selective-scan decode ("Triton decode kernel + MBU analysis", Kernel design) is a
+second recurrence through the same kind of boundary.
+
 Parity status: every routine is pinned by tests/test_oracle_pins.py except the KDA gate formula,
 whose two readings are pinned only to their own special values (the sources name the inputs and
 the -5 lower bound but print no formula): "parity unpinned" for that formula.
@@ -108,6 +111,8 @@ def _declare(L):
     L.oracle_conv_update.restype = c_int
     L.oracle_conv_update.argtypes = [c_int, c_int, _D, _D, _D, _D, c_int, _I32,
                                       ctypes.c_int32, _D]
+    L.oracle_mamba_decode.restype = None
+    L.oracle_mamba_decode.argtypes = [c_int, c_int, c_int, _D, _D, _D, _D, _D, _D, _D, _D, _D]
     L.oracle_gated_rmsnorm.restype = None
     L.oracle_gated_rmsnorm.argtypes = [c_int, c_int, _D, _D, _D, c_dbl, c_int, _D]
 
@@ -283,3 +288,20 @@ def fused_kda(x, conv_w, conv_state, raw_g, raw_beta, A_log, dt_bias, state, out
                       pad_slot=pad_slot)
     out = gated_rmsnorm(o, out_gate, norm_w, norm_eps, act)
     return out, bad
+
+
+def mamba_decode(x, dt, A, Bm, Cm, h, *, Dskip=None, z=None):
+    """Mamba-1 selective-scan decode step. x, dt, z: [B, D]; A: [D, N]; Bm, Cm: [B, N];
+    Dskip: [D]; h: [B, D, N] float64, updated in place. Returns y [B, D]."""
+    _check_inplace(h)
+    x, dt, A, Bm, Cm = _f64(x), _f64(dt), _f64(A), _f64(Bm), _f64(Cm)
+    B, D = x.shape
+    N = A.shape[1]
+    assert h.shape == (B, D, N)
+    Dskip = None if Dskip is None else _f64(Dskip)
+    z = None if z is None else _f64(z)
+    y = np.empty((B, D))
+    lib().oracle_mamba_decode(B, D, N, _p(x), _p(dt), _p(A), _p(Bm), _p(Cm),
+                              None if Dskip is None else _p(Dskip), None if z is None else _p(z),
+                              _p(h), _p(y))
+    return y

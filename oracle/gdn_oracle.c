@@ -281,3 +281,30 @@ void oracle_gated_rmsnorm(int rows, int D, const double *x, const double *gate, 
         }
     }
 }
+
+/* Mamba-1 selective-scan decode step ("Triton decode kernel + MBU analysis", section "Kernel
+ * design"), per (row b, channel d) with state h[b, d, 0..N):
+ *   dA = exp(dt * A[d, :]);  dB = dt * B[b, :];  h <- dA * h + dB * x;  y = sum_n C[b, n] h[n];
+ *   y += Dskip[d] * x (when Dskip is given);  y *= silu(z) (when z is given).
+ * x, dt, z, y: [B, D]; A: [D, N]; Bm, Cm: [B, N]; Dskip: [D] or NULL; z: [B, D] or NULL;
+ * h: [B, D, N], updated in place. */
+void oracle_mamba_decode(int B, int D, int N, const double *x, const double *dt, const double *A,
+                         const double *Bm, const double *Cm, const double *Dskip, const double *z,
+                         double *h, double *y)
+{
+    for (int b = 0; b < B; ++b)
+        for (int d = 0; d < D; ++d) {
+            size_t r = (size_t)b * D + d;
+            double *hr = h + r * N;
+            double acc = 0.0;
+            for (int n = 0; n < N; ++n) {
+                double dA = exp(dt[r] * A[(size_t)d * N + n]);
+                double dB = dt[r] * Bm[(size_t)b * N + n];
+                hr[n] = dA * hr[n] + dB * x[r];
+                acc += Cm[(size_t)b * N + n] * hr[n];
+            }
+            if (Dskip) acc += Dskip[d] * x[r];
+            if (z) acc *= z[r] * sigmoid(z[r]);
+            y[r] = acc;
+        }
+}

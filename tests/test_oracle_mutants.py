@@ -44,6 +44,12 @@ MUTANTS = [
     ("per-key decay index", "decay_log[kk] : decay_log[0]", "decay_log[0] : decay_log[0]"),
     ("bf16 rounding by truncation", "return ldexp(nearbyint(ldexp(m, 8)), e - 8);",
      "return ldexp(trunc(ldexp(m, 8)), e - 8);"),
+    ("mamba decay sign", "double dA = exp(dt[r] * A[(size_t)d * N + n]);", "double dA = exp(-dt[r] * A[(size_t)d * N + n]);"),
+    ("mamba input without dt", "double dB = dt[r] * Bm[(size_t)b * N + n];", "double dB = Bm[(size_t)b * N + n];"),
+    ("mamba output from the old state", "                hr[n] = dA * hr[n] + dB * x[r];\n                acc += Cm[(size_t)b * N + n] * hr[n];",
+     "                acc += Cm[(size_t)b * N + n] * hr[n];\n                hr[n] = dA * hr[n] + dB * x[r];"),
+    ("mamba skip dropped", "if (Dskip) acc += Dskip[d] * x[r];", ";"),
+    ("mamba gate as sigmoid", "if (z) acc *= z[r] * sigmoid(z[r]);", "if (z) acc *= sigmoid(z[r]);"),
     ("bf16 state not rounded", "for (size_t e = 0; e < (size_t)V * K; ++e) S[e] = oracle_round_bf16(S[e]);", ";"),
     ("bf16 state rounded before the output",
      "            delta_rule_tile(K, V, S, kh, qh, v + ((size_t)b * HV + hv) * V, gl, g_per_key,\n                            beta[(size_t)b * HV + hv], u, d, out + ((size_t)b * HV + hv) * V);\n            if (state_bf16)\n                for (size_t e = 0; e < (size_t)V * K; ++e) S[e] = oracle_round_bf16(S[e]);",

@@ -541,6 +541,64 @@ def test_fused_per_key_gate_reduces_to_scalar():
     check_fused_per_key_gate_reduces_to_scalar()
 
 
+# --------------------------------------------------------------------------------------------
+# Mamba-1 selective-scan decode
+# --------------------------------------------------------------------------------------------
+def _mamba_inputs(B, D, N, seed):
+    rng = np.random.default_rng(seed)
+    return dict(x=rng.normal(size=(B, D)), dt=np.log1p(np.exp(rng.normal(size=(B, D)))),
+                A=-np.exp(rng.normal(size=(D, N))), Bm=rng.normal(size=(B, N)),
+                Cm=rng.normal(size=(B, N)), Dskip=rng.normal(size=D), z=rng.normal(size=(B, D)),
+                h=rng.normal(size=(B, D, N)))
+
+
+def check_mamba_constant_input_geometric_series():
+    """With dt, A, B, x fixed over T steps the recurrence is h_T = a^T h_0 + b x (1 - a^T)/(1 - a)
+    per state element (a = exp(dt A), b = dt B): a closed form of the linear recurrence."""
+    B, D, N, T = 2, 3, 5, 7
+    m = _mamba_inputs(B, D, N, 40)
+    h = m["h"].copy()
+    for _ in range(T):
+        oracle.mamba_decode(m["x"], m["dt"], m["A"], m["Bm"], m["Cm"], h)
+    a = np.exp(m["dt"][:, :, None] * m["A"][None])
+    bx = m["dt"][:, :, None] * m["Bm"][:, None, :] * m["x"][:, :, None]
+    want = a ** T * m["h"] + bx * (1 - a ** T) / (1 - a)
+    assert rel_err(h, want) < 1e-12
+
+
+def check_mamba_output_and_gates():
+    """y = C . h_new, plus D x, times silu(z); with dt = 0 the state is unchanged; A = 0 makes the
+    state accumulate dt B x; z = 0 zeroes y and a large z multiplies it by z (silu(z) -> z)."""
+    B, D, N = 2, 4, 6
+    m = _mamba_inputs(B, D, N, 41)
+    h = m["h"].copy()
+    y = oracle.mamba_decode(m["x"], m["dt"], m["A"], m["Bm"], m["Cm"], h, Dskip=m["Dskip"], z=m["z"])
+    plain = np.einsum("bn,bdn->bd", m["Cm"], h) + m["Dskip"][None] * m["x"]
+    silu = torch.nn.functional.silu(torch.from_numpy(m["z"])).numpy()
+    assert rel_err(y, plain * silu) < 1e-13
+    h0 = m["h"].copy()
+    y0 = oracle.mamba_decode(m["x"], np.zeros((B, D)), m["A"], m["Bm"], m["Cm"], h0)
+    np.testing.assert_array_equal(h0, m["h"])
+    assert rel_err(y0, np.einsum("bn,bdn->bd", m["Cm"], m["h"])) < 1e-13
+    ha = m["h"].copy()
+    oracle.mamba_decode(m["x"], m["dt"], np.zeros((D, N)), m["Bm"], m["Cm"], ha)
+    assert rel_err(ha, m["h"] + m["dt"][:, :, None] * m["Bm"][:, None, :] * m["x"][:, :, None]) < 1e-14
+    hz = m["h"].copy()
+    yz = oracle.mamba_decode(m["x"], m["dt"], m["A"], m["Bm"], m["Cm"], hz, z=np.zeros((B, D)))
+    assert np.all(yz == 0)
+    hb = m["h"].copy()
+    yb = oracle.mamba_decode(m["x"], m["dt"], m["A"], m["Bm"], m["Cm"], hb, z=np.full((B, D), 800.0))
+    assert rel_err(yb, 800.0 * np.einsum("bn,bdn->bd", m["Cm"], hb)) < 1e-13
+
+
+def test_mamba_constant_input_geometric_series():
+    check_mamba_constant_input_geometric_series()
+
+
+def test_mamba_output_and_gates():
+    check_mamba_output_and_gates()
+
+
 ALL_CHECKS = [
     check_hand_worked_step, check_invariant_no_decay_no_write, check_invariant_exact_recall,
     check_invariant_full_decay, check_closed_matrix_form, check_gqa_duplication,
@@ -548,4 +606,5 @@ ALL_CHECKS = [
     check_buffered_ring_records_and_lowrank, check_gdn_gates, check_kda_gate_reading,
     check_conv_update_is_causal_convolution, check_gated_rmsnorm, check_bf16_rounding,
     check_fused_per_key_gate_reduces_to_scalar, check_bf16_state_storage,
+    check_mamba_constant_input_geometric_series, check_mamba_output_and_gates,
 ]
