@@ -71,6 +71,7 @@ KERNEL_FILES = {
                  "ssm_recurrent_decode_gb300/csrc/gdn_tile.cuh", "ssm_recurrent_decode_gb300/csrc/gdn_common.cuh"],
     "fused": ["ssm_recurrent_decode_gb300/csrc/fused_pipe.cu", "ssm_recurrent_decode_gb300/csrc/gdn_pipe.cuh",
               "ssm_recurrent_decode_gb300/csrc/gdn_tile.cuh", "ssm_recurrent_decode_gb300/csrc/gdn_common.cuh"],
+    "mamba": ["ssm_recurrent_decode_gb300/csrc/mamba_kernel.cu", "ssm_recurrent_decode_gb300/csrc/gdn_common.cuh"],
 }
 
 
@@ -766,18 +767,62 @@ def run_stack(args):
     return h.finish(line)
 
 
+def run_mamba(args):
+    """Mamba-1 selective-scan decode ("Triton decode kernel + MBU analysis"): B rows, D channels,
+    N state entries, fp32 inputs and state. Bandwidth by the page's bytes model B*D*(20N+24)."""
+    import torch
+    import gdn_synth as syn
+    import ssm_recurrent_decode_gb300 as gdn
+    h = Harness(args)
+    gdn.lib()
+    B, D, N = args.B, args.D, args.N
+    m = syn.mamba_inputs(B, D, N, "f32", 77 + h.rank)
+    t = {k: torch.from_numpy(np.ascontiguousarray(v)).to(h.dev) for k, v in m.items()}
+    state_bytes = B * D * N * 4
+    n_pools = pool_count(state_bytes, h.dev)
+    pools = [t["h"]] + [t["h"].clone() for _ in range(n_pools - 1)]
+    y = torch.empty((B, D), dtype=torch.float32, device=h.dev)
+    calls = [gdn.mamba_selective_scan_decode(t["x"], t["dt"], t["A"], t["Bm"], t["Cm"], pool, y,
+                                             Dskip=t["Dskip"], z=t["z"], prepare=True) for pool in pools]
+
+    def step(i):
+        calls[i % n_pools]()
+
+    per_graph = max(64, n_pools)
+    ms, steps, clk = h.time_graph(step, args.steps, args.warmup, per_graph)
+    (ms,) = max_over_ranks([ms], h.world)
+    if h.rank != 0:
+        return h.finish(None)
+    page_bytes = B * D * (20 * N + 24)
+    gbs = h.world * page_bytes / (ms * 1e-3) / 1e9
+    line = base_line(
+        h, gbs, ms, steps, args.warmup,
+        f"Mamba-1 selective-scan decode: B={B} D={D} N={N}, fp32 inputs and state, with D skip and "
+        f"silu(z) gate", {"B": B, "D": D, "N": N, "bytes_model": "B*D*(20N+24)",
+                          "bytes_per_step": page_bytes, "state_pools": n_pools,
+                          "timing": f"CUDA-graph replays of {per_graph} calls",
+                          "context": "the page's Triton kernel on an A10G: 60.5 / 59.6 / 58.4 us at "
+                                     "B = 1 / 4 / 8, D = 1536, N = 16 (launch-bound)"}, steps)
+    min_bytes = 2 * B * D * N * 4 + D * N * 4 + 2 * B * N * 4 + 4 * B * D * 4 + D * 4
+    line["roofline"] = roofline(min_bytes, ms, "mamba", f"mamba_B{B}_D{D}_N{N}")
+    line["clocks"] = clk
+    return h.finish(line)
+
+
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=10000)
     p.add_argument("--warmup", type=int, default=50)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=["packed", "buffered", "fused", "stack"], default="packed")
+    p.add_argument("--workload", choices=["packed", "buffered", "fused", "stack", "mamba"], default="packed")
     p.add_argument("--B", type=int, default=256)
     p.add_argument("--L", type=int, default=16)
     p.add_argument("--T", type=int, default=128)
     p.add_argument("--layout", choices=["DS", "SD"], default="DS")
     p.add_argument("--state-dtype", choices=["f32", "bf16"], default="f32")
+    p.add_argument("--D", type=int, default=1536)
+    p.add_argument("--N", type=int, default=16)
     p.add_argument("--layers", type=int, default=48)
     p.add_argument("--pairs", type=int, default=8)
     p.add_argument("--cpu-budget", type=float, default=10.0)
@@ -787,7 +832,7 @@ def main(argv=None):
     if args.impl == "reference":
         return run_reference(args)
     return {"packed": run_packed, "buffered": run_buffered, "fused": run_fused,
-            "stack": run_stack}[args.workload](args)
+            "stack": run_stack, "mamba": run_mamba}[args.workload](args)
 
 
 if __name__ == "__main__":

@@ -36,7 +36,7 @@ import numpy as np
 __all__ = [
     "philox4x32_10", "normal_f32", "normal_at", "scale_constant",
     "f32_to_bf16_bits", "bf16_bits_to_f32", "Tag", "stream_id",
-    "packed_inputs", "fused_inputs", "state_tile_values", "permutation",
+    "packed_inputs", "fused_inputs", "state_tile_values", "permutation", "mamba_inputs",
 ]
 
 _MASK32 = np.uint64(0xFFFFFFFF)
@@ -82,6 +82,14 @@ class Tag:
     OUT_GATE = 12    # fused: output gate [T, heads, head_dim]
     G_DIRECT = 13    # direct-gate mode: g [B, HV]
     BETA_DIRECT = 14  # direct-gate mode: beta logits [B, HV]
+    M_X = 15         # Mamba decode: x [B, D]
+    M_DT = 16        # Mamba decode: dt [B, D]
+    M_A = 17         # Mamba decode: A [D, N]
+    M_B = 18         # Mamba decode: B rows [B, N]
+    M_C = 19         # Mamba decode: C rows [B, N]
+    M_D = 20         # Mamba decode: skip D [D]
+    M_Z = 21         # Mamba decode: gate z [B, D]
+    M_H = 22         # Mamba decode: state h [B, D, N]
 
 
 def stream_id(tag: int, layer: int = 0) -> int:
@@ -188,6 +196,23 @@ def fused_inputs(T: int, heads: int, head_dim: int, num_slots: int, seed: int, s
         "dt_bias": normal_f32(seed, Tag.DT_BIAS, 0, (dim,), 1.0, layer),
         "out_gate": f32_to_bf16_bits(normal_f32(seed, Tag.OUT_GATE, step, (T, heads, head_dim), 1.0, layer)),
         "norm_w": np.ones(head_dim, dtype=np.float32),
+    }
+
+
+def mamba_inputs(B: int, D: int, N: int, dtype: str, seed: int, step: int = 0) -> dict:
+    """Inputs of one Mamba-1 decode step: x, z ~ N(0,1), dt positive (0.01 + |N(0, 0.1)|),
+    B and C rows ~ N(0,1) (in `dtype`); parameters A negative (-(0.5 + |N(0,1)|)) and skip
+    D ~ N(0,1) in fp32; the fp32 state h ~ N(0,1) (drawn at step 0)."""
+    dt = np.float32(0.01) + np.abs(normal_f32(seed, Tag.M_DT, step, (B, D), 0.1))
+    return {
+        "x": _maybe_bf16(normal_f32(seed, Tag.M_X, step, (B, D), 1.0), dtype),
+        "dt": _maybe_bf16(dt, dtype),
+        "Bm": _maybe_bf16(normal_f32(seed, Tag.M_B, step, (B, N), 1.0), dtype),
+        "Cm": _maybe_bf16(normal_f32(seed, Tag.M_C, step, (B, N), 1.0), dtype),
+        "z": _maybe_bf16(normal_f32(seed, Tag.M_Z, step, (B, D), 1.0), dtype),
+        "A": -(np.float32(0.5) + np.abs(normal_f32(seed, Tag.M_A, 0, (D, N), 1.0))),
+        "Dskip": normal_f32(seed, Tag.M_D, 0, (D,), 1.0),
+        "h": normal_f32(seed, Tag.M_H, 0, (B, D, N), 1.0),
     }
 
 

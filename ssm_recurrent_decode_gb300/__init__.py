@@ -11,6 +11,7 @@ Entry points (same names as the C ABI):
   gdn_decode_step_indexed  row b on state slot cache_indices[b] (the packed decode over a pool)
   gdn_decode_buffered      output-only decode that writes the state back once every L steps
   gdn_decode_fused         conv1d update -> delta step (per-key or per-head decay) -> gated RMSNorm
+  mamba_selective_scan_decode  the Mamba-1 selective-scan decode step (a diagonal recurrence)
 plus ``fused_recurrent_gated_delta_rule_packed_decode``, the packed call with the keyword names
 of "Microbenchmark: buffered output-only GDN decode (ReplaySSM Part A)" (_bench_cfg, run_packed).
 """
@@ -25,6 +26,7 @@ __all__ = [
     "lib", "build", "GdnError", "GdnStepArgs", "GdnRingArgs", "GdnFusedArgs",
     "gdn_decode_step", "gdn_decode_step_indexed", "gdn_decode_buffered", "gdn_decode_fused",
     "gdn_strerror", "split_mixed_qkv", "fused_recurrent_gated_delta_rule_packed_decode", "PreparedCall",
+    "MambaArgs", "mamba_selective_scan_decode",
     "GDN_F32", "GDN_BF16", "GDN_DEVERR_BAD_INDEX", "GDN_DEVERR_BAD_WRITE_POS", "GDN_DEVERR_TIMEOUT",
     "EXPORTS",
 ]
@@ -39,7 +41,7 @@ ABI_VERSION = 4
 
 # every function the header declares
 EXPORTS = ("gdn_decode_step", "gdn_decode_step_indexed", "gdn_decode_buffered", "gdn_decode_fused",
-           "gdn_strerror", "gdn_abi_struct_size", "gdn_abi_version")
+           "gdn_strerror", "gdn_abi_struct_size", "gdn_abi_version", "mamba_selective_scan_decode")
 
 _i32, _i64, _f32, _vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
 
@@ -69,6 +71,12 @@ class GdnFusedArgs(ctypes.Structure):
                 ("state", _vp), ("state_indices", _vp), ("pad_slot_id", _i32),
                 ("out_gate", _vp), ("norm_w", _vp), ("norm_eps", _f32), ("gate_act", _i32),
                 ("out", _vp), ("err_flags", _vp), ("kernel", _i32)]
+
+
+class MambaArgs(ctypes.Structure):
+    _fields_ = [("B", _i32), ("D", _i32), ("N", _i32), ("in_dtype", _i32), ("out_dtype", _i32),
+                ("x", _vp), ("dt", _vp), ("A", _vp), ("Bm", _vp), ("Cm", _vp), ("Dskip", _vp),
+                ("z", _vp), ("h", _vp), ("h_out", _vp), ("y", _vp)]
 
 
 class GdnError(RuntimeError):
@@ -101,6 +109,8 @@ def lib():
             L.gdn_decode_buffered.argtypes = [ctypes.POINTER(GdnStepArgs), _vp, _i32,
                                               ctypes.POINTER(GdnRingArgs), _vp]
             L.gdn_decode_fused.argtypes = [ctypes.POINTER(GdnFusedArgs), _vp]
+            L.mamba_selective_scan_decode.argtypes = [ctypes.POINTER(MambaArgs), _vp]
+            L.mamba_selective_scan_decode.restype = ctypes.c_int
             for name in ("gdn_decode_step", "gdn_decode_step_indexed", "gdn_decode_buffered",
                          "gdn_decode_fused", "gdn_abi_version"):
                 getattr(L, name).restype = ctypes.c_int
@@ -382,3 +392,31 @@ def fused_recurrent_gated_delta_rule_packed_decode(mixed_qkv, a, b, A_log, dt_bi
                                    dt_bias=dt_bias, scale=scale,
                                    use_qk_l2norm=use_qk_l2norm_in_kernel, err_flags=err_flags,
                                    stream=stream)
+
+
+def mamba_selective_scan_decode(x, dt, A, Bm, Cm, h, y, *, Dskip=None, z=None, h_out=None,
+                                stream=None, prepare=False):
+    """Mamba-1 selective-scan decode step (declared in include/mamba_decode.h).
+    x, dt: [B, D] and Bm, Cm: [B, N] (fp32 or bf16, one dtype); A: [D, N] fp32; Dskip: [D] fp32 or
+    None; z: [B, D] or None; h: [B, D, N] fp32 state, updated in place unless h_out (same shape)
+    is given; y: [B, D] fp32 or bf16."""
+    torch = _torch()
+    B, D = x.shape
+    N = A.shape[1]
+    m = MambaArgs()
+    m.B, m.D, m.N = B, D, N
+    m.in_dtype, m.out_dtype = _dtype_code(x), _dtype_code(y)
+    for t, name in ((dt, "dt"), (Bm, "Bm"), (Cm, "Cm"), (z, "z")):
+        if t is not None and t.dtype != x.dtype:
+            raise TypeError(f"{name} must have the dtype of x")
+    if tuple(h.shape) != (B, D, N) or (h_out is not None and tuple(h_out.shape) != (B, D, N)):
+        raise ValueError(f"h (and h_out) must be [{B}, {D}, {N}]")
+    m.x, m.dt = _ptr(_dense(x, "x"), "x"), _ptr(_dense(dt, "dt"), "dt")
+    m.A = _ptr(_dense(A, "A"), "A", torch.float32)
+    m.Bm, m.Cm = _ptr(_dense(Bm, "Bm"), "Bm"), _ptr(_dense(Cm, "Cm"), "Cm")
+    m.Dskip = _ptr(None if Dskip is None else _dense(Dskip, "Dskip"), "Dskip", torch.float32)
+    m.z = _ptr(None if z is None else _dense(z, "z"), "z")
+    m.h = _ptr(_dense(h, "h"), "h", torch.float32)
+    m.h_out = _ptr(None if h_out is None else _dense(h_out, "h_out"), "h_out", torch.float32)
+    m.y = _ptr(_dense(y, "y"), "y")
+    return _run_or_prepare("mamba_selective_scan_decode", (ctypes.byref(m),), (m,), stream, prepare, y)

@@ -1,0 +1,145 @@
+// mamba_kernel.cu -- the Mamba-1 selective-scan decode step (mamba_selective_scan_decode).
+//
+// A diagonal recurrence: every (row, channel) owns an N-entry fp32 state row, updated
+// element-wise and contracted with C into one output. LPR = NP / 4 lanes share a row, each holding
+// four consecutive state entries (one 16-byte access when N is a multiple of 4), so a warp moves
+// 32 / LPR consecutive rows = 512 contiguous bytes of state; the output is a group sum over the
+// LPR lanes. B and C rows are shared by every channel of a row (L1 hits), A rows by every row of
+// a channel (L2 hits). Memory-bound: about 8 flops and an exp per 8 bytes of state.
+//
+// Source: "Triton decode kernel + MBU analysis", "Kernel design" (the math, fp32 accumulation and
+// state); that page's kernel runs one program per (row, channel) with BLOCK_N = next_pow2(N).
+#include <cmath>
+#include <cstdint>
+
+#include "gdn_common.cuh"
+#include "mamba_decode.h"
+
+namespace gdn {
+
+constexpr int kMambaThreads = 256;
+
+template <typename T> __device__ __forceinline__ float ld1(const void *p, size_t i)
+{
+    return to_f32(static_cast<const T *>(p)[i]);
+}
+
+template <int NP, typename Tin, bool VEC>
+__global__ void __launch_bounds__(kMambaThreads) mamba_decode_kernel(const __grid_constant__ mamba_decode_args P)
+{
+    constexpr int LPR = NP / 4;
+    const int N = P.N, D = P.D;
+    const long long rows = (long long)P.B * D;
+    const long long tid = (long long)blockIdx.x * kMambaThreads + threadIdx.x;
+    const long long r = tid / LPR;
+    const int sub = (int)(tid % LPR);
+    const bool live = r < rows;
+    const int b = live ? (int)(r / D) : 0, d = live ? (int)(r - (long long)b * D) : 0;
+    const int n0 = sub * 4;
+
+    float hv[4] = {0.f, 0.f, 0.f, 0.f}, av[4] = {0.f, 0.f, 0.f, 0.f};
+    float bv[4] = {0.f, 0.f, 0.f, 0.f}, cv[4] = {0.f, 0.f, 0.f, 0.f};
+    const float *hp = P.h + (size_t)r * N + n0;
+    if (live) {
+        if (VEC) {
+            const float4 h4 = ld_stream(hp);
+            const float4 a4 = *reinterpret_cast<const float4 *>(P.A + (size_t)d * N + n0);
+            const float4 b4 = load4(static_cast<const Tin *>(P.Bm) + (size_t)b * N + n0);
+            const float4 c4 = load4(static_cast<const Tin *>(P.Cm) + (size_t)b * N + n0);
+            hv[0] = h4.x; hv[1] = h4.y; hv[2] = h4.z; hv[3] = h4.w;
+            av[0] = a4.x; av[1] = a4.y; av[2] = a4.z; av[3] = a4.w;
+            bv[0] = b4.x; bv[1] = b4.y; bv[2] = b4.z; bv[3] = b4.w;
+            cv[0] = c4.x; cv[1] = c4.y; cv[2] = c4.z; cv[3] = c4.w;
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (n0 + j < N) {
+                    hv[j] = hp[j];
+                    av[j] = P.A[(size_t)d * N + n0 + j];
+                    bv[j] = ld1<Tin>(P.Bm, (size_t)b * N + n0 + j);
+                    cv[j] = ld1<Tin>(P.Cm, (size_t)b * N + n0 + j);
+                }
+            }
+        }
+    }
+    const float x = live ? ld1<Tin>(P.x, (size_t)r) : 0.f;
+    const float dt = live ? ld1<Tin>(P.dt, (size_t)r) : 0.f;
+    float y = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        hv[j] = fmaf(expf(dt * av[j]), hv[j], dt * bv[j] * x);
+        y = fmaf(cv[j], hv[j], y);
+    }
+    y = group_sum<LPR>(y);   // every lane of the group takes part, live or not
+    if (!live) return;
+    float *op = (P.h_out ? P.h_out : P.h) + (size_t)r * N + n0;
+    if (VEC) {
+        st_stream(op, make_float4(hv[0], hv[1], hv[2], hv[3]));
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (n0 + j < N) op[j] = hv[j];
+    }
+    if (sub == 0) {
+        if (P.Dskip) y = fmaf(P.Dskip[d], x, y);
+        if (P.z) {
+            const float z = ld1<Tin>(P.z, (size_t)r);
+            y *= z * sigmoid_f(z);
+        }
+        if (P.out_dtype == GDN_BF16)
+            static_cast<bf16 *>(P.y)[r] = __float2bfloat16_rn(y);
+        else
+            static_cast<float *>(P.y)[r] = y;
+    }
+}
+
+template <int NP, typename Tin>
+static int launch_mamba_np(const mamba_decode_args &p, cudaStream_t s)
+{
+    const long long threads = (long long)p.B * p.D * (NP / 4);
+    const unsigned blocks = (unsigned)((threads + kMambaThreads - 1) / kMambaThreads);
+    if (p.N == NP)
+        mamba_decode_kernel<NP, Tin, true><<<blocks, kMambaThreads, 0, s>>>(p);
+    else
+        mamba_decode_kernel<NP, Tin, false><<<blocks, kMambaThreads, 0, s>>>(p);
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
+}
+
+template <typename Tin>
+static int launch_mamba_t(const mamba_decode_args &p, cudaStream_t s)
+{
+    if (p.N <= 4) return launch_mamba_np<4, Tin>(p, s);
+    if (p.N <= 8) return launch_mamba_np<8, Tin>(p, s);
+    if (p.N <= 16) return launch_mamba_np<16, Tin>(p, s);
+    if (p.N <= 32) return launch_mamba_np<32, Tin>(p, s);
+    if (p.N <= 64) return launch_mamba_np<64, Tin>(p, s);
+    return launch_mamba_np<128, Tin>(p, s);
+}
+
+}  // namespace gdn
+
+namespace {
+bool al(const void *p, size_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+}
+
+extern "C" int mamba_selective_scan_decode(const mamba_decode_args *a, gdn_stream_t stream)
+{
+    if (!a) return GDN_ERR_NULL;
+    if (a->B < 0 || a->D < 0 || a->N < 1 || a->N > 128) return GDN_ERR_SHAPE;
+    if ((long long)a->B * a->D * 32 > 0x7FFFFFFFLL * 256) return GDN_ERR_SHAPE;
+    if ((a->in_dtype != GDN_F32 && a->in_dtype != GDN_BF16) || (a->out_dtype != GDN_F32 && a->out_dtype != GDN_BF16))
+        return GDN_ERR_DTYPE;
+    if (a->B == 0 || a->D == 0) return GDN_OK;
+    if (!a->x || !a->dt || !a->A || !a->Bm || !a->Cm || !a->h || !a->y) return GDN_ERR_NULL;
+    const size_t es = a->in_dtype == GDN_BF16 ? 2 : 4;
+    if (!al(a->x, es) || !al(a->dt, es) || !al(a->Bm, es) || !al(a->Cm, es) || (a->z && !al(a->z, es)) ||
+        !al(a->h, 4) || !al(a->A, 4) || (a->h_out && !al(a->h_out, 4)) || (a->Dskip && !al(a->Dskip, 4)) ||
+        !al(a->y, a->out_dtype == GDN_BF16 ? 2 : 4))
+        return GDN_ERR_ALIGN;
+    const bool pow2 = a->N == 4 || a->N == 8 || a->N == 16 || a->N == 32 || a->N == 64 || a->N == 128;
+    if (pow2 && (!al(a->h, 16) || !al(a->A, 16) || (a->h_out && !al(a->h_out, 16)) || !al(a->Bm, 4 * es) ||
+                 !al(a->Cm, 4 * es)))
+        return GDN_ERR_ALIGN;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return a->in_dtype == GDN_BF16 ? gdn::launch_mamba_t<gdn::bf16>(*a, s) : gdn::launch_mamba_t<float>(*a, s);
+}

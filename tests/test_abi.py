@@ -19,7 +19,7 @@ def declared_functions():
     for h in HEADERS:
         text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
         text = re.sub(r"//[^\n]*", "", text)
-        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(gdn_\w+)\s*\(", text, re.M):
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b((?:gdn|mamba)_\w+)\s*\(", text, re.M):
             names.append(m.group(1))
     return sorted(set(names))
 
