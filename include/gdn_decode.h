@@ -211,6 +211,16 @@ int gdn_decode_buffered(const gdn_step_args *args, const int32_t *cache_indices,
  */
 int gdn_decode_fused(const gdn_fused_args *args, gdn_stream_t stream);
 
+/*
+ * gdn_selftest_bounded_wait -- a check of the bounded waits inside the pipelined kernels (the
+ * pages have no counterpart; it is a library self-test). One CTA of 128 threads waits on an
+ * mbarrier; with arrive != 0 one thread arrives and the wait completes; with arrive == 0 nothing
+ * arrives, the waits give up after limit_cycles SM clock cycles, GDN_DEVERR_TIMEOUT is OR-ed into
+ * *err_flags (a device int32) and the kernel returns normally. Returns GDN_OK, GDN_ERR_NULL,
+ * GDN_ERR_ARG (limit_cycles < 1) or GDN_ERR_LAUNCH.
+ */
+int gdn_selftest_bounded_wait(int32_t *err_flags, int64_t limit_cycles, int32_t arrive, gdn_stream_t stream);
+
 /* Static text for a gdn_status code. */
 const char *gdn_strerror(int status);
 

@@ -26,7 +26,7 @@ __all__ = [
     "lib", "build", "GdnError", "GdnStepArgs", "GdnRingArgs", "GdnFusedArgs",
     "gdn_decode_step", "gdn_decode_step_indexed", "gdn_decode_buffered", "gdn_decode_fused",
     "gdn_strerror", "split_mixed_qkv", "fused_recurrent_gated_delta_rule_packed_decode", "PreparedCall",
-    "MambaArgs", "mamba_selective_scan_decode",
+    "MambaArgs", "mamba_selective_scan_decode", "gdn_selftest_bounded_wait",
     "GDN_F32", "GDN_BF16", "GDN_DEVERR_BAD_INDEX", "GDN_DEVERR_BAD_WRITE_POS", "GDN_DEVERR_TIMEOUT",
     "EXPORTS",
 ]
@@ -41,7 +41,8 @@ ABI_VERSION = 4
 
 # every function the header declares
 EXPORTS = ("gdn_decode_step", "gdn_decode_step_indexed", "gdn_decode_buffered", "gdn_decode_fused",
-           "gdn_strerror", "gdn_abi_struct_size", "gdn_abi_version", "mamba_selective_scan_decode")
+           "gdn_strerror", "gdn_abi_struct_size", "gdn_abi_version", "mamba_selective_scan_decode",
+           "gdn_selftest_bounded_wait")
 
 _i32, _i64, _f32, _vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
 
@@ -111,6 +112,8 @@ def lib():
             L.gdn_decode_fused.argtypes = [ctypes.POINTER(GdnFusedArgs), _vp]
             L.mamba_selective_scan_decode.argtypes = [ctypes.POINTER(MambaArgs), _vp]
             L.mamba_selective_scan_decode.restype = ctypes.c_int
+            L.gdn_selftest_bounded_wait.argtypes = [_vp, _i64, _i32, _vp]
+            L.gdn_selftest_bounded_wait.restype = ctypes.c_int
             for name in ("gdn_decode_step", "gdn_decode_step_indexed", "gdn_decode_buffered",
                          "gdn_decode_fused", "gdn_abi_version"):
                 getattr(L, name).restype = ctypes.c_int
@@ -420,3 +423,12 @@ def mamba_selective_scan_decode(x, dt, A, Bm, Cm, h, y, *, Dskip=None, z=None, h
     m.h_out = _ptr(None if h_out is None else _dense(h_out, "h_out"), "h_out", torch.float32)
     m.y = _ptr(_dense(y, "y"), "y")
     return _run_or_prepare("mamba_selective_scan_decode", (ctypes.byref(m),), (m,), stream, prepare, y)
+
+
+def gdn_selftest_bounded_wait(err_flags, limit_cycles, arrive, stream=None):
+    """Run the bounded-wait self-test kernel (see include/gdn_decode.h); err_flags is a CUDA int32
+    tensor of one element that receives GDN_DEVERR_TIMEOUT when the wait gives up."""
+    torch = _torch()
+    _check("gdn_selftest_bounded_wait",
+           lib().gdn_selftest_bounded_wait(_ptr(err_flags, "err_flags", torch.int32), int(limit_cycles),
+                                           int(bool(arrive)), _stream(stream)))

@@ -100,6 +100,12 @@ def test_null_args_and_null_indices():
     assert L.gdn_decode_step_indexed(ctypes.byref(s), None, -1, None) == -1
 
 
+def test_selftest_argument_checks():
+    L = gdn.lib()
+    assert L.gdn_selftest_bounded_wait(None, 1000, 0, None) == -1
+    assert L.gdn_selftest_bounded_wait(1 << 40, 0, 0, None) == -6
+
+
 def test_empty_batch_launches_nothing():
     s = _valid_args()
     s.B = 0
