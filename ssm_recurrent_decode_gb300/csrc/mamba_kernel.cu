@@ -1,10 +1,10 @@
 // mamba_kernel.cu -- the Mamba-1 selective-scan decode step (mamba_selective_scan_decode).
 //
 // A diagonal recurrence: every (row, channel) owns an N-entry fp32 state row, updated
-// element-wise and contracted with C into one output. LPR = NP / 4 lanes share a row, each holding
-// four consecutive state entries (one 16-byte access when N is a multiple of 4), so a warp moves
-// 32 / LPR consecutive rows = 512 contiguous bytes of state; the output is a group sum over the
-// LPR lanes. B and C rows are shared by every channel of a row (L1 hits), A rows by every row of
+// element-wise and contracted with C into one output. LPR = NP / 8 lanes share a row (NP / 4 when
+// N < 8), each holding eight (four) consecutive state entries as 16-byte accesses when N is a
+// power of two, so a warp moves 32 / LPR consecutive rows, 1 KB of contiguous state; the output
+// is a group sum over the LPR lanes. B and C rows are shared by every channel of a row (L1 hits), A rows by every row of
 // a channel (L2 hits). Memory-bound: about 8 flops and an exp per 8 bytes of state.
 //
 // Source: "Triton decode kernel + MBU analysis", "Kernel design" (the math, fp32 accumulation and
@@ -24,10 +24,13 @@ template <typename T> __device__ __forceinline__ float ld1(const void *p, size_t
     return to_f32(static_cast<const T *>(p)[i]);
 }
 
+// EPL state entries per lane (4, or 8 when N >= 8): fewer lanes per row means fewer repeated
+// loads of the row's scalars and a shorter group sum.
 template <int NP, typename Tin, bool VEC>
 __global__ void __launch_bounds__(kMambaThreads) mamba_decode_kernel(const __grid_constant__ mamba_decode_args P)
 {
-    constexpr int LPR = NP / 4;
+    constexpr int EPL = NP >= 8 ? 8 : 4;
+    constexpr int LPR = NP / EPL;
     const int N = P.N, D = P.D;
     const long long rows = (long long)P.B * D;
     const long long tid = (long long)blockIdx.x * kMambaThreads + threadIdx.x;
@@ -35,24 +38,28 @@ __global__ void __launch_bounds__(kMambaThreads) mamba_decode_kernel(const __gri
     const int sub = (int)(tid % LPR);
     const bool live = r < rows;
     const int b = live ? (int)(r / D) : 0, d = live ? (int)(r - (long long)b * D) : 0;
-    const int n0 = sub * 4;
+    const int n0 = sub * EPL;
 
-    float hv[4] = {0.f, 0.f, 0.f, 0.f}, av[4] = {0.f, 0.f, 0.f, 0.f};
-    float bv[4] = {0.f, 0.f, 0.f, 0.f}, cv[4] = {0.f, 0.f, 0.f, 0.f};
+    float hv[EPL], av[EPL], bv[EPL], cv[EPL];
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) hv[j] = av[j] = bv[j] = cv[j] = 0.f;
     const float *hp = P.h + (size_t)r * N + n0;
     if (live) {
         if (VEC) {
-            const float4 h4 = ld_stream(hp);
-            const float4 a4 = *reinterpret_cast<const float4 *>(P.A + (size_t)d * N + n0);
-            const float4 b4 = load4(static_cast<const Tin *>(P.Bm) + (size_t)b * N + n0);
-            const float4 c4 = load4(static_cast<const Tin *>(P.Cm) + (size_t)b * N + n0);
-            hv[0] = h4.x; hv[1] = h4.y; hv[2] = h4.z; hv[3] = h4.w;
-            av[0] = a4.x; av[1] = a4.y; av[2] = a4.z; av[3] = a4.w;
-            bv[0] = b4.x; bv[1] = b4.y; bv[2] = b4.z; bv[3] = b4.w;
-            cv[0] = c4.x; cv[1] = c4.y; cv[2] = c4.z; cv[3] = c4.w;
+#pragma unroll
+            for (int q = 0; q < EPL / 4; ++q) {
+                const float4 h4 = ld_stream(hp + 4 * q);
+                const float4 a4 = *reinterpret_cast<const float4 *>(P.A + (size_t)d * N + n0 + 4 * q);
+                const float4 b4 = load4(static_cast<const Tin *>(P.Bm) + (size_t)b * N + n0 + 4 * q);
+                const float4 c4 = load4(static_cast<const Tin *>(P.Cm) + (size_t)b * N + n0 + 4 * q);
+                hv[4 * q] = h4.x; hv[4 * q + 1] = h4.y; hv[4 * q + 2] = h4.z; hv[4 * q + 3] = h4.w;
+                av[4 * q] = a4.x; av[4 * q + 1] = a4.y; av[4 * q + 2] = a4.z; av[4 * q + 3] = a4.w;
+                bv[4 * q] = b4.x; bv[4 * q + 1] = b4.y; bv[4 * q + 2] = b4.z; bv[4 * q + 3] = b4.w;
+                cv[4 * q] = c4.x; cv[4 * q + 1] = c4.y; cv[4 * q + 2] = c4.z; cv[4 * q + 3] = c4.w;
+            }
         } else {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < EPL; ++j) {
                 if (n0 + j < N) {
                     hv[j] = hp[j];
                     av[j] = P.A[(size_t)d * N + n0 + j];
@@ -64,20 +71,25 @@ __global__ void __launch_bounds__(kMambaThreads) mamba_decode_kernel(const __gri
     }
     const float x = live ? ld1<Tin>(P.x, (size_t)r) : 0.f;
     const float dt = live ? ld1<Tin>(P.dt, (size_t)r) : 0.f;
+    const float dtx = dt * x;
     float y = 0.f;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        hv[j] = fmaf(expf(dt * av[j]), hv[j], dt * bv[j] * x);
+    for (int j = 0; j < EPL; ++j) {
+        // exp of a non-positive argument of modest size (dt * A): the fast exponential's few-ulp
+        // error is far inside the 1e-5 tolerance
+        hv[j] = fmaf(__expf(dt * av[j]), hv[j], dtx * bv[j]);
         y = fmaf(cv[j], hv[j], y);
     }
     y = group_sum<LPR>(y);   // every lane of the group takes part, live or not
     if (!live) return;
     float *op = (P.h_out ? P.h_out : P.h) + (size_t)r * N + n0;
     if (VEC) {
-        st_stream(op, make_float4(hv[0], hv[1], hv[2], hv[3]));
+#pragma unroll
+        for (int q = 0; q < EPL / 4; ++q)
+            st_stream(op + 4 * q, make_float4(hv[4 * q], hv[4 * q + 1], hv[4 * q + 2], hv[4 * q + 3]));
     } else {
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
+        for (int j = 0; j < EPL; ++j)
             if (n0 + j < N) op[j] = hv[j];
     }
     if (sub == 0) {
@@ -96,7 +108,7 @@ __global__ void __launch_bounds__(kMambaThreads) mamba_decode_kernel(const __gri
 template <int NP, typename Tin>
 static int launch_mamba_np(const mamba_decode_args &p, cudaStream_t s)
 {
-    const long long threads = (long long)p.B * p.D * (NP / 4);
+    const long long threads = (long long)p.B * p.D * (NP / (NP >= 8 ? 8 : 4));
     const unsigned blocks = (unsigned)((threads + kMambaThreads - 1) / kMambaThreads);
     if (p.N == NP)
         mamba_decode_kernel<NP, Tin, true><<<blocks, kMambaThreads, 0, s>>>(p);
