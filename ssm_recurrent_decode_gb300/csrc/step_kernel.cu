@@ -102,21 +102,24 @@ __device__ __forceinline__ float4 widen_bf16x4(uint2 raw)
 // both tiles' loads before computing either, so a CTA keeps as many bytes in flight as with an
 // fp32 tile. The rows stay in registers as packed bf16 (8 bytes per four values) and are widened
 // to fp32 where they are used; the update is rounded to nearest even as it is stored.
-template <int K, typename Tin>
-__global__ void __launch_bounds__(kThreads, 2) step_kernel_bf16_pair(const __grid_constant__ StepLaunch P)
+template <int K, typename Tin, int NT>
+__global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) step_kernel_bf16_pair(const __grid_constant__ StepLaunch P)
 {
-    using TL = Tile<K>;
+    using TL = Tile<K>;      // row geometry: 16 rows per warp
+    using TR = Tile<K, 8>;   // reduction of one 8-row chunk (same lane layout)
     const gdn_step_args &a = P.a;
     const int HV = a.HV, V = a.V;
     const int ntiles = a.B * HV;
     TL t;
     t.init();
-    uint2 raw[2][TL::R];
-    int slots[2];
-    bool run[2];
+    TR t8;
+    t8.init();
+    uint2 raw[NT][TL::R];
+    int slots[NT];
+    bool run[NT];
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-        const int tile = blockIdx.x * 2 + u;
+    for (int u = 0; u < NT; ++u) {
+        const int tile = blockIdx.x * NT + u;
         run[u] = false;
         slots[u] = 0;
         if (tile < ntiles) {
@@ -147,9 +150,9 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel_bf16_pair(const __gri
         }
     }
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
+    for (int u = 0; u < NT; ++u) {
         if (!run[u]) continue;   // uniform over the CTA
-        const int tile = blockIdx.x * 2 + u;
+        const int tile = blockIdx.x * NT + u;
         const int b = tile / HV, hv = tile - b * HV, h = hv / P.G;
         const size_t out_base = ((size_t)b * HV + hv) * V;
         const Tin *qp = static_cast<const Tin *>(a.q) + (size_t)b * a.q_stride + (size_t)h * K;
@@ -161,38 +164,37 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel_bf16_pair(const __gri
         const float4 kh = l2_normalise4<TL::LPR>(k4, a.use_qk_l2norm != 0, 1.f);
         const float4 qh = l2_normalise4<TL::LPR>(q4, a.use_qk_l2norm != 0, P.scale);
         const float kq = group_sum<TL::LPR>(dot4(kh, qh));
-        const float e = expf(g);
-        const float4 dec = make_float4(e, e, e, e);
-        const float4 kd = scale4(kh, e), qd = scale4(qh, e);
-        float vv[TL::M];
+        const float e = expf(g);   // applied to the reduced dots: u = e (S k), and e (S q)
+        // two chunks of 8 rows: 16 partial dots live at a time instead of 32
+        float dch[2];
 #pragma unroll
-        for (int m = 0; m < TL::M; ++m) {
-            const int r = t.row(0, t.owned_chunk(m));
-            vv[m] = (t.holds_k_dot() && r < V) ? to_f32(vp[r]) : 0.f;
-        }
-        float x[TL::N];
+        for (int c = 0; c < 2; ++c) {
+            float x[TR::N];
 #pragma unroll
-        for (int i = 0; i < TL::R; ++i) {
-            const float4 sv = widen_bf16x4(raw[u][i]);
-            x[i] = dot4(sv, kd);
-            x[TL::R + i] = dot4(sv, qd);
-        }
-        t.reduce_scatter(x);
-        float dv[TL::M];
-#pragma unroll
-        for (int m = 0; m < TL::M; ++m) dv[m] = beta * (vv[m] - x[m]);
-#pragma unroll
-        for (int m = 0; m < TL::M; ++m) {
-            const float dq = t.delta_for_q(dv[m]);
-            const int r = t.row(0, t.owned_chunk(m));
-            if (!t.holds_k_dot() && r < V) store_out(a.out, a.out_dtype, out_base + r, fmaf(dq, kq, x[m]));
+            for (int i = 0; i < 8; ++i) {
+                const float4 sv = widen_bf16x4(raw[u][8 * c + i]);
+                x[i] = dot4(sv, kh);
+                x[8 + i] = dot4(sv, qh);
+            }
+            t8.reduce_scatter(x);
+            const int r = t.row(0, 8 * c + t8.owned_chunk(0));
+            const float vv = (t8.holds_k_dot() && r < V) ? to_f32(vp[r]) : 0.f;
+            const float d = beta * (vv - e * x[0]);
+            const float dq = t8.delta_for_q(d);
+            if (!t8.holds_k_dot() && t8.writer() && r < V)
+                store_out(a.out, a.out_dtype, out_base + r, fmaf(dq, kq, e * x[0]));
+            dch[c] = d;
         }
         bf16 *S = static_cast<bf16 *>(a.state) + ((size_t)slots[u] * HV + hv) * (size_t)V * K;
 #pragma unroll
-        for (int i = 0; i < TL::R; ++i) {
-            const float d = t.delta_of(dv, i);
-            const int r = t.row(0, i);
-            if (r < V) st_stream(S + (size_t)r * K + t.col, decay_update4(dec, widen_bf16x4(raw[u][i]), d, kh));
+        for (int c = 0; c < 2; ++c) {
+            const float dc[1] = {dch[c]};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float d = t8.delta_of(dc, i);
+                const int r = t.row(0, 8 * c + i);
+                if (r < V) st_stream(S + (size_t)r * K + t.col, axpby4(e, widen_bf16x4(raw[u][8 * c + i]), d, kh));
+            }
         }
     }
 }
@@ -224,7 +226,7 @@ static int launch_step_t(const StepLaunch &p, cudaStream_t stream)
         bool paired = false;
         if constexpr (sizeof(TS) == 2 && K >= 64) {
             if (p.a.V <= Tile<K>::ROWS_PASS) {
-                step_kernel_bf16_pair<K, Tin><<<(tiles + 1) / 2, kThreads, 0, stream>>>(p);
+                step_kernel_bf16_pair<K, Tin, 2><<<(tiles + 1) / 2, kThreads, 0, stream>>>(p);
                 paired = true;
             }
         }
