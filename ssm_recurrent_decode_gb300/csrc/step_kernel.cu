@@ -98,12 +98,15 @@ __device__ __forceinline__ float4 widen_bf16x4(uint2 raw)
                        __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u));
 }
 
-// bf16 state, one row pass (V <= rows per pass): each CTA takes two consecutive tiles and issues
-// both tiles' loads before computing either, so a CTA keeps as many bytes in flight as with an
-// fp32 tile. The rows stay in registers as packed bf16 (8 bytes per four values) and are widened
-// to fp32 where they are used; the update is rounded to nearest even as it is stored.
+// bf16 state, one row pass (V <= rows per pass): NT tiles per CTA, whose loads are all issued
+// before any is computed; rows stay in registers as packed bf16 (8 bytes per four values), are
+// widened to fp32 where they are used, and the update is rounded to nearest even as it is stored.
+// Each tile's rows are reduced in two 8-row chunks (16 partial dots live, not 32) and the decay is
+// applied to the reduced dots, so one tile fits in 80 registers: launched with NT = 1 at three CTAs
+// per SM (92.7 us per step at B = 256, HV = 32; two tiles per CTA at two CTAs per SM: 105.4 us;
+// four CTAs per SM spill: 95.2 us).
 template <int K, typename Tin, int NT>
-__global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) step_kernel_bf16_pair(const __grid_constant__ StepLaunch P)
+__global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) step_kernel_bf16(const __grid_constant__ StepLaunch P)
 {
     using TL = Tile<K>;      // row geometry: 16 rows per warp
     using TR = Tile<K, 8>;   // reduction of one 8-row chunk (same lane layout)
@@ -226,7 +229,7 @@ static int launch_step_t(const StepLaunch &p, cudaStream_t stream)
         bool paired = false;
         if constexpr (sizeof(TS) == 2 && K >= 64) {
             if (p.a.V <= Tile<K>::ROWS_PASS) {
-                step_kernel_bf16_pair<K, Tin, 2><<<(tiles + 1) / 2, kThreads, 0, stream>>>(p);
+                step_kernel_bf16<K, Tin, 1><<<tiles, kThreads, 0, stream>>>(p);
                 paired = true;
             }
         }
