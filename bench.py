@@ -744,7 +744,7 @@ def run_stack(args):
     h = Harness(args)
     import ssm_recurrent_decode_gb300 as gdn
     gdn.lib()
-    layers, B, H, HV, K, V = args.layers, 256, 16, 48, 128, 128
+    layers, B, H, HV, K, V = args.layers, args.B, 16, 48, 128, 128
     steps = args.steps
     res = stack_decode(layers, B, H, HV, K, V, steps=steps, device=h.dev, pairs=args.pairs)
     ms = res["dec_ms_median"]
