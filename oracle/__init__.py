@@ -113,6 +113,8 @@ def _declare(L):
                                       ctypes.c_int32, _D]
     L.oracle_mamba_decode.restype = None
     L.oracle_mamba_decode.argtypes = [c_int, c_int, c_int, _D, _D, _D, _D, _D, _D, _D, _D, _D]
+    L.oracle_gemv.restype = None
+    L.oracle_gemv.argtypes = [c_int, c_int, c_int, _D, _D, _D]
     L.oracle_gated_rmsnorm.restype = None
     L.oracle_gated_rmsnorm.argtypes = [c_int, c_int, _D, _D, _D, c_dbl, c_int, _D]
 
@@ -304,4 +306,15 @@ def mamba_decode(x, dt, A, Bm, Cm, h, *, Dskip=None, z=None):
     lib().oracle_mamba_decode(B, D, N, _p(x), _p(dt), _p(A), _p(Bm), _p(Cm),
                               None if Dskip is None else _p(Dskip), None if z is None else _p(z),
                               _p(h), _p(y))
+    return y
+
+
+def gemv(x, W):
+    """y [T, N] = x [T, Kd] . W[N, Kd]^T in fp64 (the decode projection)."""
+    x, W = _f64(x), _f64(W)
+    T, Kd = x.shape
+    N = W.shape[0]
+    assert W.shape[1] == Kd
+    y = np.empty((T, N))
+    lib().oracle_gemv(T, N, Kd, _p(x), _p(W), _p(y))
     return y

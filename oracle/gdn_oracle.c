@@ -308,3 +308,16 @@ void oracle_mamba_decode(int B, int D, int N, const double *x, const double *dt,
             y[r] = acc;
         }
 }
+
+/* Projection for decode ("Optimization Log: Qwen3.5-27B Dense on B200", Kernel 3: BF16 GEMV):
+ * y[t, n] = sum_k x[t, k] W[n, k] for T rows, N outputs, Kd inputs; W stored one output row per
+ * line ([N, Kd]). */
+void oracle_gemv(int T, int N, int Kd, const double *x, const double *W, double *y)
+{
+    for (int t = 0; t < T; ++t)
+        for (int n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int k = 0; k < Kd; ++k) acc += x[(size_t)t * Kd + k] * W[(size_t)n * Kd + k];
+            y[(size_t)t * N + n] = acc;
+        }
+}

@@ -50,6 +50,8 @@ MUTANTS = [
      "                acc += Cm[(size_t)b * N + n] * hr[n];\n                hr[n] = dA * hr[n] + dB * x[r];"),
     ("mamba skip dropped", "if (Dskip) acc += Dskip[d] * x[r];", ";"),
     ("mamba gate as sigmoid", "if (z) acc *= z[r] * sigmoid(z[r]);", "if (z) acc *= sigmoid(z[r]);"),
+    ("gemv transposed weights", "acc += x[(size_t)t * Kd + k] * W[(size_t)n * Kd + k];", "acc += x[(size_t)t * Kd + k] * W[(size_t)k * N + n];"),
+    ("gemv drops the last input", "for (int k = 0; k < Kd; ++k) acc += x[(size_t)t * Kd + k]", "for (int k = 0; k < Kd - 1; ++k) acc += x[(size_t)t * Kd + k]"),
     ("bf16 state not rounded", "for (size_t e = 0; e < (size_t)V * K; ++e) S[e] = oracle_round_bf16(S[e]);", ";"),
     ("bf16 state rounded before the output",
      "            delta_rule_tile(K, V, S, kh, qh, v + ((size_t)b * HV + hv) * V, gl, g_per_key,\n                            beta[(size_t)b * HV + hv], u, d, out + ((size_t)b * HV + hv) * V);\n            if (state_bf16)\n                for (size_t e = 0; e < (size_t)V * K; ++e) S[e] = oracle_round_bf16(S[e]);",

@@ -599,6 +599,24 @@ def test_mamba_output_and_gates():
     check_mamba_output_and_gates()
 
 
+# --------------------------------------------------------------------------------------------
+# decode projection (GEMV)
+# --------------------------------------------------------------------------------------------
+def check_gemv():
+    """Against numpy's matmul (a different implementation), and two closed forms: identity
+    weights return x, and a rank-1 W = u w^T gives y = (x . w) u."""
+    rng = np.random.default_rng(50)
+    x = rng.normal(size=(3, 37)); W = rng.normal(size=(11, 37))
+    assert rel_err(oracle.gemv(x, W), x @ W.T) < 1e-13
+    np.testing.assert_array_equal(oracle.gemv(x, np.eye(37)), x)
+    u, w = rng.normal(size=5), rng.normal(size=37)
+    assert rel_err(oracle.gemv(x, np.outer(u, w)), np.outer(x @ w, u)) < 1e-13
+
+
+def test_gemv():
+    check_gemv()
+
+
 ALL_CHECKS = [
     check_hand_worked_step, check_invariant_no_decay_no_write, check_invariant_exact_recall,
     check_invariant_full_decay, check_closed_matrix_form, check_gqa_duplication,
@@ -606,5 +624,5 @@ ALL_CHECKS = [
     check_buffered_ring_records_and_lowrank, check_gdn_gates, check_kda_gate_reading,
     check_conv_update_is_causal_convolution, check_gated_rmsnorm, check_bf16_rounding,
     check_fused_per_key_gate_reduces_to_scalar, check_bf16_state_storage,
-    check_mamba_constant_input_geometric_series, check_mamba_output_and_gates,
+    check_mamba_constant_input_geometric_series, check_mamba_output_and_gates, check_gemv,
 ]
