@@ -73,6 +73,7 @@ KERNEL_FILES = {
     "fused": ["ssm_recurrent_decode_gb300/csrc/fused_pipe.cu", "ssm_recurrent_decode_gb300/csrc/gdn_pipe.cuh",
               "ssm_recurrent_decode_gb300/csrc/gdn_tile.cuh", "ssm_recurrent_decode_gb300/csrc/gdn_common.cuh"],
     "mamba": ["ssm_recurrent_decode_gb300/csrc/mamba_kernel.cu", "ssm_recurrent_decode_gb300/csrc/gdn_common.cuh"],
+    "gemv": ["ssm_recurrent_decode_gb300/csrc/gemv_kernel.cu", "ssm_recurrent_decode_gb300/csrc/gdn_common.cuh"],
 }
 
 
@@ -811,19 +812,67 @@ def run_mamba(args):
     return h.finish(line)
 
 
+def run_gemv(args):
+    """Decode projection ("Optimization Log", Kernel 3: BF16 GEMV with split-K) at one of the
+    page's shapes, synthetic bf16 weights N(0, 0.02^2); bandwidth = weight bytes per call / time."""
+    import torch
+    import gdn_synth as syn
+    import ssm_recurrent_decode_gb300 as gdn
+    h = Harness(args)
+    gdn.lib()
+    T, N, Kd = args.T, args.gemv_n, args.gemv_k
+    x = torch.empty((T, Kd), dtype=torch.bfloat16, device=h.dev)
+    syn.fill_normal_(x, 91, syn.Tag.X, 0, 1.0)
+    w_bytes = N * Kd * 2
+    n_pools = pool_count(w_bytes, h.dev)
+    Ws = []
+    for p in range(n_pools):
+        W = torch.empty((N, Kd), dtype=torch.bfloat16, device=h.dev)
+        syn.fill_normal_(W, 91, syn.Tag.CONV_W, 0, 0.02, layer=p)
+        Ws.append(W)
+    y = torch.empty((T, N), dtype=torch.bfloat16, device=h.dev)
+    ws = gdn.gemv_workspace(T, N, Kd, 0, device=h.dev)
+    splits = gdn.lib().gdn_gemv_default_splits(T, N, Kd)
+    calls = [gdn.gdn_gemv_bf16(x, W, y, workspace=ws, prepare=True) for W in Ws]
+
+    def step(i):
+        calls[i % n_pools]()
+
+    per_graph = max(64, n_pools)
+    ms, steps, clk = h.time_graph(step, args.steps, args.warmup, per_graph)
+    (ms,) = max_over_ranks([ms], h.world)
+    if h.rank != 0:
+        return h.finish(None)
+    gbs = h.world * w_bytes * ((T + 7) // 8) / (ms * 1e-3) / 1e9
+    line = base_line(
+        h, gbs, ms, steps, args.warmup,
+        f"decode projection GEMV: T={T} token rows, W [{N}, {Kd}] bf16 ({w_bytes / 1e6:.0f} MB), "
+        f"fp32 accumulation, {splits} K split(s)",
+        {"T": T, "N": N, "Kd": Kd, "splits": splits, "weight_pools": n_pools,
+         "timing": f"CUDA-graph replays of {per_graph} calls"}, steps * (2 if splits > 1 else 1))
+    line["metric"] = "decode projection weight-stream GB/s"
+    io = T * Kd * 2 + T * N * 2 + (2 * splits * T * N * 4 if splits > 1 else 0)
+    line["roofline"] = roofline(w_bytes * ((T + 7) // 8) + io, ms, "gemv", f"gemv_T{T}_N{N}_K{Kd}")
+    line["clocks"] = clk
+    return h.finish(line)
+
+
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=10000)
     p.add_argument("--warmup", type=int, default=50)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=["packed", "buffered", "fused", "stack", "mamba"], default="packed")
+    p.add_argument("--workload", choices=["packed", "buffered", "fused", "stack", "mamba", "gemv"],
+                   default="packed")
     p.add_argument("--B", type=int, default=256)
     p.add_argument("--L", type=int, default=16)
     p.add_argument("--T", type=int, default=128)
     p.add_argument("--layout", choices=["DS", "SD"], default="DS")
     p.add_argument("--state-dtype", choices=["f32", "bf16"], default="f32")
     p.add_argument("--D", type=int, default=1536)
+    p.add_argument("--gemv-n", type=int, default=17408)
+    p.add_argument("--gemv-k", type=int, default=5120)
     p.add_argument("--N", type=int, default=16)
     p.add_argument("--layers", type=int, default=48)
     p.add_argument("--pairs", type=int, default=8)
@@ -834,7 +883,7 @@ def main(argv=None):
     if args.impl == "reference":
         return run_reference(args)
     return {"packed": run_packed, "buffered": run_buffered, "fused": run_fused,
-            "stack": run_stack, "mamba": run_mamba}[args.workload](args)
+            "stack": run_stack, "mamba": run_mamba, "gemv": run_gemv}[args.workload](args)
 
 
 if __name__ == "__main__":

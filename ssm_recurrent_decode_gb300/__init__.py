@@ -27,6 +27,7 @@ __all__ = [
     "gdn_decode_step", "gdn_decode_step_indexed", "gdn_decode_buffered", "gdn_decode_fused",
     "gdn_strerror", "split_mixed_qkv", "fused_recurrent_gated_delta_rule_packed_decode", "PreparedCall",
     "MambaArgs", "mamba_selective_scan_decode", "gdn_selftest_bounded_wait",
+    "GemvArgs", "gdn_gemv_bf16", "gemv_workspace",
     "GDN_F32", "GDN_BF16", "GDN_DEVERR_BAD_INDEX", "GDN_DEVERR_BAD_WRITE_POS", "GDN_DEVERR_TIMEOUT",
     "EXPORTS",
 ]
@@ -42,7 +43,8 @@ ABI_VERSION = 4
 # every function the header declares
 EXPORTS = ("gdn_decode_step", "gdn_decode_step_indexed", "gdn_decode_buffered", "gdn_decode_fused",
            "gdn_strerror", "gdn_abi_struct_size", "gdn_abi_version", "mamba_selective_scan_decode",
-           "gdn_selftest_bounded_wait")
+           "gdn_selftest_bounded_wait", "gdn_gemv_bf16", "gdn_gemv_default_splits",
+           "gdn_gemv_workspace_bytes")
 
 _i32, _i64, _f32, _vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
 
@@ -80,6 +82,12 @@ class MambaArgs(ctypes.Structure):
                 ("z", _vp), ("h", _vp), ("h_out", _vp), ("y", _vp)]
 
 
+class GemvArgs(ctypes.Structure):
+    _fields_ = [("T", _i32), ("N", _i32), ("Kd", _i32), ("out_dtype", _i32), ("x", _vp),
+                ("x_stride", _i64), ("W", _vp), ("y", _vp), ("y_stride", _i64), ("splits", _i32),
+                ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t)]
+
+
 class GdnError(RuntimeError):
     """A non-zero status from the library (the message is gdn_strerror's)."""
 
@@ -113,6 +121,12 @@ def lib():
             L.mamba_selective_scan_decode.argtypes = [ctypes.POINTER(MambaArgs), _vp]
             L.mamba_selective_scan_decode.restype = ctypes.c_int
             L.gdn_selftest_bounded_wait.argtypes = [_vp, _i64, _i32, _vp]
+            L.gdn_gemv_bf16.argtypes = [ctypes.POINTER(GemvArgs), _vp]
+            L.gdn_gemv_bf16.restype = ctypes.c_int
+            L.gdn_gemv_default_splits.argtypes = [_i32, _i32, _i32]
+            L.gdn_gemv_default_splits.restype = _i32
+            L.gdn_gemv_workspace_bytes.argtypes = [_i32, _i32, _i32]
+            L.gdn_gemv_workspace_bytes.restype = ctypes.c_size_t
             L.gdn_selftest_bounded_wait.restype = ctypes.c_int
             for name in ("gdn_decode_step", "gdn_decode_step_indexed", "gdn_decode_buffered",
                          "gdn_decode_fused", "gdn_abi_version"):
@@ -432,3 +446,39 @@ def gdn_selftest_bounded_wait(err_flags, limit_cycles, arrive, stream=None):
     _check("gdn_selftest_bounded_wait",
            lib().gdn_selftest_bounded_wait(_ptr(err_flags, "err_flags", torch.int32), int(limit_cycles),
                                            int(bool(arrive)), _stream(stream)))
+
+
+def gemv_workspace(T, N, Kd, splits=0, device=None):
+    """A workspace tensor for gdn_gemv_bf16 with this split count (0: the library's choice), or
+    None when the call needs none."""
+    torch = _torch()
+    L = lib()
+    s = splits or L.gdn_gemv_default_splits(int(T), int(N), int(Kd))
+    nbytes = L.gdn_gemv_workspace_bytes(int(T), int(N), int(s))
+    if nbytes == 0:
+        return None
+    return torch.empty(nbytes // 4, dtype=torch.float32, device=device or "cuda")
+
+
+def gdn_gemv_bf16(x, W, y, *, splits=0, workspace=None, stream=None, prepare=False):
+    """Decode projection y [T, N] = x [T, Kd] W[N, Kd]^T (declared in include/gdn_gemv.h). x and W
+    bf16 with dense rows (x may be a row view), y fp32 or bf16. With more than one K split (splits
+    = 0 lets the library choose) a workspace is needed: see gemv_workspace."""
+    torch = _torch()
+    T, Kd = x.shape
+    N = W.shape[0]
+    if W.shape[1] != Kd or tuple(y.shape) != (T, N):
+        raise ValueError(f"expected W [{N}, {Kd}] and y [{T}, {N}]")
+    if x.stride(1) != 1 or y.stride(1) != 1:
+        raise ValueError("x and y need unit inner stride")
+    g = GemvArgs()
+    g.T, g.N, g.Kd = T, N, Kd
+    g.out_dtype = _dtype_code(y)
+    g.x, g.x_stride = _ptr(x, "x", torch.bfloat16), x.stride(0)
+    g.W = _ptr(_dense(W, "W"), "W", torch.bfloat16)
+    g.y, g.y_stride = _ptr(y, "y"), y.stride(0)
+    g.splits = int(splits)
+    if workspace is not None:
+        g.workspace = _ptr(_dense(workspace, "workspace"), "workspace", torch.float32)
+        g.workspace_bytes = workspace.numel() * 4
+    return _run_or_prepare("gdn_gemv_bf16", (ctypes.byref(g),), (g, workspace), stream, prepare, y)

@@ -106,6 +106,25 @@ def test_selftest_argument_checks():
     assert L.gdn_selftest_bounded_wait(1 << 40, 0, 0, None) == -6
 
 
+def test_gemv_checks():
+    L = gdn.lib()
+    g = gdn.GemvArgs()
+    assert L.gdn_gemv_bf16(None, None) == -1
+    g.T, g.N, g.Kd, g.out_dtype = 2, 64, 100, 0          # Kd not a multiple of 8
+    assert L.gdn_gemv_bf16(ctypes.byref(g), None) == -2
+    g.Kd = 128
+    assert L.gdn_gemv_bf16(ctypes.byref(g), None) == -1  # NULL pointers
+    g.x, g.W, g.y, g.x_stride, g.y_stride = 1 << 40, 1 << 41, 1 << 42, 128, 64
+    g.splits = 2                                       # needs a workspace
+    assert L.gdn_gemv_bf16(ctypes.byref(g), None) == -1
+    g.workspace, g.workspace_bytes = 1 << 43, 16
+    assert L.gdn_gemv_bf16(ctypes.byref(g), None) == -2  # too small
+    g.x = (1 << 40) + 8
+    assert L.gdn_gemv_bf16(ctypes.byref(g), None) == -4
+    assert L.gdn_gemv_workspace_bytes(2, 64, 2) == 2 * 2 * 64 * 4
+    assert L.gdn_gemv_workspace_bytes(2, 64, 1) == 0
+
+
 def test_empty_batch_launches_nothing():
     s = _valid_args()
     s.B = 0
