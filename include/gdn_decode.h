@@ -60,7 +60,9 @@ typedef enum gdn_status {
     GDN_ERR_DTYPE = -3,    /* unsupported dtype or dtype combination */
     GDN_ERR_ALIGN = -4,    /* a pointer or stride breaks the alignment rule */
     GDN_ERR_LAUNCH = -5,   /* the CUDA launch failed (cudaGetLastError) */
-    GDN_ERR_ARG = -6       /* another invalid argument (e.g. L < 1, unknown enum value) */
+    GDN_ERR_ARG = -6,      /* another invalid argument (e.g. L < 1, unknown enum value) */
+    GDN_ERR_SCRATCH = -7   /* the call needs more scratch than a no-allocation entry point's fixed
+                              buffer holds */
 } gdn_status;
 
 /* Bits OR-ed into *err_flags by the kernels. */

@@ -55,6 +55,30 @@ size_t gdn_gemv_workspace_bytes(int32_t T, int32_t N, int32_t splits);
  */
 int gdn_gemv_bf16(const gdn_gemv_args *args, gdn_stream_t stream);
 
+/* Size of the fixed buffer behind gdn_gemv_bf16_noalloc, in fp32 values (4 MiB). */
+#define GDN_GEMV_NOALLOC_MAX_FLOATS (1 << 20)
+
+/*
+ * gdn_gemv_bf16_noalloc -- the same projection for callers that cannot allocate device memory:
+ * code handed only raw device pointers by a host framework that owns every allocation, serving
+ * loops that must never call cudaMalloc (it can synchronise the device and stall other work),
+ * and runtimes with a fixed, pre-planned memory budget. The source pages have no counterpart; it
+ * is a library convenience.
+ *
+ * Arguments as for gdn_gemv_bf16, except that workspace and workspace_bytes are ignored: when the
+ * call splits K, its fp32 partial sums go to a buffer of GDN_GEMV_NOALLOC_MAX_FLOATS values that
+ * the library keeps on every GPU that loads it, until the process exits. A call whose
+ * splits * T * N exceeds that size is rejected with GDN_ERR_SCRATCH before anything is launched
+ * (pass splits = 1, which needs no buffer, or use gdn_gemv_bf16 with your own workspace).
+ * Nothing here allocates: the first call on a device that splits K looks up that device's buffer
+ * address (cudaGetSymbolAddress) with the device current, so make that first call before any
+ * stream capture. Every call on a device shares the one buffer, which keeps the last call's
+ * partial sums (each call writes all the sums it reads, so no clearing is needed); calls that can
+ * run at the same time on the GPU, e.g. on two streams, race on it and must be ordered.
+ * Returns the codes of gdn_gemv_bf16, and GDN_ERR_SCRATCH.
+ */
+int gdn_gemv_bf16_noalloc(const gdn_gemv_args *args, gdn_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

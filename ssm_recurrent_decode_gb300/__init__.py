@@ -44,7 +44,7 @@ ABI_VERSION = 4
 EXPORTS = ("gdn_decode_step", "gdn_decode_step_indexed", "gdn_decode_buffered", "gdn_decode_fused",
            "gdn_strerror", "gdn_abi_struct_size", "gdn_abi_version", "mamba_selective_scan_decode",
            "gdn_selftest_bounded_wait", "gdn_gemv_bf16", "gdn_gemv_default_splits",
-           "gdn_gemv_workspace_bytes")
+           "gdn_gemv_workspace_bytes", "gdn_gemv_bf16_noalloc")
 
 _i32, _i64, _f32, _vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
 

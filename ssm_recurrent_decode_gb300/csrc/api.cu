@@ -189,6 +189,7 @@ const char *gdn_strerror(int status)
     case GDN_ERR_ALIGN: return "a pointer or stride breaks the alignment rule";
     case GDN_ERR_LAUNCH: return "the CUDA launch failed";
     case GDN_ERR_ARG: return "invalid argument";
+    case GDN_ERR_SCRATCH: return "the call needs more scratch than the fixed no-allocation buffer holds";
     default: return "unknown status";
     }
 }

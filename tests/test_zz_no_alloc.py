@@ -1,0 +1,79 @@
+"""gdn_gemv_bf16_noalloc: the decode projection for callers that cannot allocate device memory
+(code that only receives raw pointers from a framework owning every allocation, serving loops that
+must never call cudaMalloc, fixed memory budgets). Its split-K partial sums live in a buffer the
+library holds itself. Called through the C ABI twice in a row, on two different shapes, it must
+give what gdn_gemv_bf16 with a caller workspace gives, within the fp32 tolerance of the other
+tests; a request larger than its buffer is refused before anything runs.
+
+This file is collected last on purpose: it runs after every other GPU test, and also passes on its
+own in a fresh process."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import gdn_synth as syn
+import ssm_recurrent_decode_gb300 as gdn
+from conftest import rel_err
+
+pytestmark = pytest.mark.gpu
+
+GDN_ERR_SCRATCH = -7
+MAX_FLOATS = 1 << 20
+
+
+def _args(x, W, y, splits=0):
+    g = gdn.GemvArgs()
+    g.T, g.N, g.Kd = x.shape[0], W.shape[0], x.shape[1]
+    g.out_dtype = gdn.GDN_F32 if y.dtype == torch.float32 else gdn.GDN_BF16
+    g.x, g.x_stride = x.data_ptr(), x.stride(0)
+    g.W = W.data_ptr()
+    g.y, g.y_stride = y.data_ptr(), y.stride(0)
+    g.splits = splits
+    return g
+
+
+def _noalloc(x, W, y, splits=0):
+    L = gdn.lib()
+    fn = L.gdn_gemv_bf16_noalloc
+    fn.argtypes = [ctypes.POINTER(gdn.GemvArgs), ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    g = _args(x, W, y, splits)
+    return fn(ctypes.byref(g), torch.cuda.current_stream().cuda_stream)
+
+
+def _inputs(T, N, Kd, seed):
+    x = torch.empty((T, Kd), dtype=torch.bfloat16, device="cuda")
+    W = torch.empty((N, Kd), dtype=torch.bfloat16, device="cuda")
+    syn.fill_normal_(x, seed, syn.Tag.X, 0, 1.0)
+    syn.fill_normal_(W, seed, syn.Tag.CONV_W, 0, 0.02)
+    return x, W
+
+
+def test_no_alloc_gemv_matches_the_workspace_entry_point_on_two_calls_in_a_row():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    shapes = [(4, 17408, 5120, 31), (3, 5120, 17408, 32)]   # [N, Kd] of the projections listed for decode
+    for T, N, Kd, seed in shapes:
+        x, W = _inputs(T, N, Kd, seed)
+        assert gdn.lib().gdn_gemv_default_splits(T, N, Kd) > 1   # the buffer is really used
+        want = torch.empty((T, N), device="cuda")
+        gdn.gdn_gemv_bf16(x, W, want, workspace=gdn.gemv_workspace(T, N, Kd))
+        got = torch.full((T, N), float("nan"), device="cuda")
+        assert _noalloc(x, W, got) == 0
+        torch.cuda.synchronize()
+        assert np.all(np.isfinite(got.cpu().numpy()))
+        assert rel_err(got.cpu().numpy(), want.cpu().numpy()) <= 1e-5
+
+
+def test_no_alloc_gemv_refuses_more_than_its_buffer():
+    T, N, Kd, splits = 8, 65536, 1024, 4          # 8 * 65536 * 4 fp32 partial sums > 1 Mi
+    assert splits * T * N > MAX_FLOATS
+    x, W = _inputs(T, N, Kd, 33)
+    y = torch.full((T, N), 7.0, device="cuda")
+    assert _noalloc(x, W, y, splits=splits) == GDN_ERR_SCRATCH
+    torch.cuda.synchronize()
+    assert torch.all(y == 7.0)
+    assert "scratch" in gdn.gdn_strerror(GDN_ERR_SCRATCH)
+    # with one K range the call needs no buffer and runs
+    assert _noalloc(x[:1], W[:1024], y[:1, :1024], splits=1) == 0
