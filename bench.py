@@ -831,9 +831,9 @@ def run_gemv(args):
         syn.fill_normal_(W, 91, syn.Tag.CONV_W, 0, 0.02, layer=p)
         Ws.append(W)
     y = torch.empty((T, N), dtype=torch.bfloat16, device=h.dev)
-    ws = gdn.gemv_workspace(T, N, Kd, 0, device=h.dev)
-    splits = gdn.lib().gdn_gemv_default_splits(T, N, Kd)
-    calls = [gdn.gdn_gemv_bf16(x, W, y, workspace=ws, prepare=True) for W in Ws]
+    splits = args.gemv_splits or gdn.lib().gdn_gemv_default_splits(T, N, Kd)
+    ws = gdn.gemv_workspace(T, N, Kd, splits, device=h.dev)
+    calls = [gdn.gdn_gemv_bf16(x, W, y, splits=splits, workspace=ws, prepare=True) for W in Ws]
 
     def step(i):
         calls[i % n_pools]()
@@ -843,16 +843,20 @@ def run_gemv(args):
     (ms,) = max_over_ranks([ms], h.world)
     if h.rank != 0:
         return h.finish(None)
-    gbs = h.world * w_bytes * ((T + 7) // 8) / (ms * 1e-3) / 1e9
+    gbs = h.world * w_bytes / (ms * 1e-3) / 1e9
+    passes = (T + 15) // 16                   # token rows per pass over W: 16 (one when T = 1)
     line = base_line(
         h, gbs, ms, steps, args.warmup,
         f"decode projection GEMV: T={T} token rows, W [{N}, {Kd}] bf16 ({w_bytes / 1e6:.0f} MB), "
         f"fp32 accumulation, {splits} K split(s)",
         {"T": T, "N": N, "Kd": Kd, "splits": splits, "weight_pools": n_pools,
-         "timing": f"CUDA-graph replays of {per_graph} calls"}, steps * (2 if splits > 1 else 1))
+         "timing": f"CUDA-graph replays of {per_graph} calls; roofline over the whole call "
+                   f"(GEMV launches plus the split-K sum)"},
+        steps * (passes + (1 if splits > 1 else 0)))
     line["metric"] = "decode projection weight-stream GB/s"
-    io = T * Kd * 2 + T * N * 2 + (2 * splits * T * N * 4 if splits > 1 else 0)
-    line["roofline"] = roofline(w_bytes * ((T + 7) // 8) + io, ms, "gemv", f"gemv_T{T}_N{N}_K{Kd}")
+    # algorithmic bytes: W once, x, y (the split-K workspace round trip is the kernel's overhead)
+    io = T * Kd * 2 + T * N * 2
+    line["roofline"] = roofline(w_bytes + io, ms, "gemv", f"gemv_T{T}_N{N}_K{Kd}")
     line["clocks"] = clk
     return h.finish(line)
 
@@ -873,6 +877,7 @@ def main(argv=None):
     p.add_argument("--D", type=int, default=1536)
     p.add_argument("--gemv-n", type=int, default=17408)
     p.add_argument("--gemv-k", type=int, default=5120)
+    p.add_argument("--gemv-splits", type=int, default=0, help="K ranges (0: the library's choice)")
     p.add_argument("--N", type=int, default=16)
     p.add_argument("--layers", type=int, default=48)
     p.add_argument("--pairs", type=int, default=8)

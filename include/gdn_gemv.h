@@ -39,8 +39,10 @@ typedef struct gdn_gemv_args {
     size_t workspace_bytes;
 } gdn_gemv_args;
 
-/* The split count gdn_gemv_bf16 uses when args->splits == 0 (enough CTAs to cover every SM about
- * four times; at most 16, and at least 256 inputs per range). */
+/* The split count gdn_gemv_bf16 uses when args->splits == 0: a power of two up to 64 with at least
+ * 512 inputs per range, chosen so that the grid fills one wave of resident CTAs (or at least two)
+ * and each CTA's slice of x fits its shared-memory staging budget. Queries the current device's
+ * SM count and kernel occupancy once (no allocation, no launch). */
 int32_t gdn_gemv_default_splits(int32_t T, int32_t N, int32_t Kd);
 
 /* Workspace bytes a call with this split count needs (0 when splits <= 1). */

@@ -47,14 +47,30 @@ def test_bf16_output():
     assert _check(2, 17408, 5120, seed=3, out_dtype=torch.bfloat16) <= 2e-2
 
 
+@pytest.mark.parametrize("T", [1, 3])
 @pytest.mark.parametrize("splits", [1, 2, 5, 16])
-def test_explicit_splits_and_ragged_inputs(splits):
-    """Kd = 1000 is not a multiple of the 256-input step; 5 ranges leave one empty."""
-    assert _check(3, 300, 1000, seed=10 + splits, splits=splits) <= 1e-5
+def test_explicit_splits_and_ragged_inputs(splits, T):
+    """N = 300 and Kd = 1000 are not multiples of the row and input tiles; 16 ranges leave some
+    empty (their partial sums are zeros); T = 1 runs the CUDA-core form, T = 3 the tensor-core one."""
+    assert _check(T, 300, 1000, seed=10 + splits + T, splits=splits) <= 1e-5
 
 
-def test_more_rows_than_one_pass():
-    """T = 12 takes two passes of 8 and 4 token rows."""
+@pytest.mark.parametrize("T", [2, 3, 5, 16, 17])
+def test_token_counts_of_the_tensor_core_form(T):
+    """From 2 token rows on, mma tiles of 8 token rows: partly filled (2, 3, 5), two full groups
+    (16), and a second pass of one token row (17)."""
+    assert _check(T, 17408 if T < 16 else 1000, 5120 if T < 16 else 2048, seed=30 + T) <= 1e-5
+
+
+@pytest.mark.parametrize("T,splits", [(8, 1), (1, 1), (6, 2)])
+def test_x_read_through_l1_when_too_large_to_stage(T, splits):
+    """x slices of 8 x 17408 and 6 x 8704 bf16 values are too large to stage in shared memory and
+    are read through L1; one row of 17408 values is staged."""
+    assert _check(T, 640, 17408, seed=40 + T, splits=splits) <= 1e-5
+
+
+def test_more_rows_than_one_mma_group():
+    """T = 12: one pass with a full and a partly filled group of 8 token rows."""
     assert _check(12, 1000, 2048, seed=21) <= 1e-5
 
 
