@@ -73,7 +73,9 @@ KERNEL_FILES = {
     "fused": ["ssm_recurrent_decode_gb300/csrc/fused_pipe.cu", "ssm_recurrent_decode_gb300/csrc/gdn_pipe.cuh",
               "ssm_recurrent_decode_gb300/csrc/gdn_tile.cuh", "ssm_recurrent_decode_gb300/csrc/gdn_common.cuh"],
     "mamba": ["ssm_recurrent_decode_gb300/csrc/mamba_kernel.cu", "ssm_recurrent_decode_gb300/csrc/gdn_common.cuh"],
-    "gemv": ["ssm_recurrent_decode_gb300/csrc/gemv_kernel.cu", "ssm_recurrent_decode_gb300/csrc/gdn_common.cuh"],
+    "gemv": ["ssm_recurrent_decode_gb300/csrc/gemv_kernel.cu", "ssm_recurrent_decode_gb300/csrc/gemv_tc.cu",
+             "ssm_recurrent_decode_gb300/csrc/gemv_internal.h", "ssm_recurrent_decode_gb300/csrc/gdn_cluster.cuh",
+             "ssm_recurrent_decode_gb300/csrc/gdn_pipe.cuh", "ssm_recurrent_decode_gb300/csrc/gdn_common.cuh"],
 }
 
 
@@ -851,10 +853,11 @@ def run_gemv(args):
         f"fp32 accumulation, {splits} K split(s)",
         {"T": T, "N": N, "Kd": Kd, "splits": splits, "weight_pools": n_pools,
          "timing": f"CUDA-graph replays of {per_graph} calls; roofline over the whole call "
-                   f"(GEMV launches plus the split-K sum)"},
-        steps * (passes + (1 if splits > 1 else 0)))
+                   f"(the K ranges are added inside a thread-block cluster up to 8 ranges, by a "
+                   f"second launch beyond)"},
+        steps * (passes + (1 if gdn.lib().gdn_gemv_workspace_bytes(T, N, splits) > 0 else 0)))
     line["metric"] = "decode projection weight-stream GB/s"
-    # algorithmic bytes: W once, x, y (the split-K workspace round trip is the kernel's overhead)
+    # algorithmic bytes: W once, x, y (any split-K exchange is the kernel's overhead)
     io = T * Kd * 2 + T * N * 2
     line["roofline"] = roofline(w_bytes + io, ms, "gemv", f"gemv_T{T}_N{N}_K{Kd}")
     line["clocks"] = clk

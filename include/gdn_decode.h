@@ -226,10 +226,11 @@ int gdn_selftest_bounded_wait(int32_t *err_flags, int64_t limit_cycles, int32_t 
 /* Static text for a gdn_status code. */
 const char *gdn_strerror(int status);
 
-/* ABI checks for bindings: sizeof of the args structs (which: 0 step, 1 ring, 2 fused). */
+/* ABI checks for bindings: sizeof of the args structs (which: 0 step, 1 ring, 2 fused, 3 the
+ * decode projection's gdn_gemv_args of gdn_gemv.h). */
 size_t gdn_abi_struct_size(int which);
 
-/* Library ABI version (incremented on any change of the structs above; currently 4). */
+/* Library ABI version (incremented on any change of the args structs; currently 5). */
 int gdn_abi_version(void);
 
 #ifdef __cplusplus

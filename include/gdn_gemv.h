@@ -7,9 +7,11 @@
  * split-K, the projections that dominate decode time): for T token rows (decode batch, T >= 1),
  *     y[t, n] = sum_k x[t, k] * W[n, k]        (bf16 x and W, fp32 accumulation)
  * with W stored one output row per line ([N, Kd], the nn.Linear weight layout). Split-K divides
- * the Kd inputs into `splits` ranges whose fp32 partial sums go to a caller workspace and are then
- * added in a fixed order (deterministic), so that narrow projections still spread over every SM.
- * HBM traffic: the weights once per 8 token rows, 2 * N * Kd bytes for T <= 8.
+ * the Kd inputs into `splits` ranges so that narrow projections still spread over every SM; the
+ * ranges' fp32 partial sums are added in range order (deterministic): with up to 8 ranges inside
+ * the launch (the ranges of a row tile form a thread-block cluster and add through distributed
+ * shared memory), with more in a caller workspace and a second launch.
+ * HBM traffic: the weights once per pass of up to 16 token rows, 2 * N * Kd bytes for T <= 16.
  */
 #ifndef GDN_GEMV_H
 #define GDN_GEMV_H
@@ -35,17 +37,20 @@ typedef struct gdn_gemv_args {
     int64_t y_stride;
     int32_t splits;         /* K ranges: 0 lets the library choose (gdn_gemv_default_splits) */
     float *workspace;       /* fp32, at least gdn_gemv_workspace_bytes(T, N, splits) bytes when the
-                               split count is above 1; unused (may be NULL) otherwise */
+                               split count is above 8; unused (may be NULL) otherwise */
     size_t workspace_bytes;
+    int32_t *err_flags;     /* optional device word; a kernel that gives up a bounded wait ORs
+                               GDN_DEVERR_TIMEOUT into it and leaves its outputs unwritten */
 } gdn_gemv_args;
 
-/* The split count gdn_gemv_bf16 uses when args->splits == 0: a power of two up to 64 with at least
- * 512 inputs per range, chosen so that the grid fills one wave of resident CTAs (or at least two)
- * and each CTA's slice of x fits its shared-memory staging budget. Queries the current device's
- * SM count and kernel occupancy once (no allocation, no launch). */
+/* The split count gdn_gemv_bf16 uses when args->splits == 0: a power of two up to 8 (so no
+ * workspace is needed) with at least 512 inputs per range, chosen so that the grid fills one wave
+ * of resident CTAs (or at least two) and each CTA's slice of x fits its shared-memory staging
+ * budget. Queries the current device's SM count and kernel occupancy once (no allocation, no
+ * launch). */
 int32_t gdn_gemv_default_splits(int32_t T, int32_t N, int32_t Kd);
 
-/* Workspace bytes a call with this split count needs (0 when splits <= 1). */
+/* Workspace bytes a call with this split count needs (0 when splits <= 8). */
 size_t gdn_gemv_workspace_bytes(int32_t T, int32_t N, int32_t splits);
 
 /*
@@ -53,7 +58,9 @@ size_t gdn_gemv_workspace_bytes(int32_t T, int32_t N, int32_t splits);
  * Kernel 3 (BF16 GEMV with split-K; M = 1 decode; key shapes [5120, 17408] and [17408, 5120]).
  * Returns GDN_OK, GDN_ERR_NULL (a missing pointer, or no workspace when one is needed),
  * GDN_ERR_SHAPE (negative sizes, Kd not a multiple of 8, workspace too small, splits > 64),
- * GDN_ERR_DTYPE, GDN_ERR_ALIGN or GDN_ERR_LAUNCH.
+ * GDN_ERR_DTYPE, GDN_ERR_ALIGN or GDN_ERR_LAUNCH. From 2 token rows on the library's tensor-core
+ * kernel waits on mbarriers with a bound; a wait that gives up ORs GDN_DEVERR_TIMEOUT into
+ * args->err_flags (when given) and leaves that CTA's outputs unwritten.
  */
 int gdn_gemv_bf16(const gdn_gemv_args *args, gdn_stream_t stream);
 
@@ -68,13 +75,13 @@ int gdn_gemv_bf16(const gdn_gemv_args *args, gdn_stream_t stream);
  * is a library convenience.
  *
  * Arguments as for gdn_gemv_bf16, except that workspace and workspace_bytes are ignored: when the
- * call splits K, its fp32 partial sums go to a buffer of GDN_GEMV_NOALLOC_MAX_FLOATS values that
- * the library keeps on every GPU that loads it, until the process exits. A call whose
- * splits * T * N exceeds that size is rejected with GDN_ERR_SCRATCH before anything is launched
- * (pass splits = 1, which needs no buffer, or use gdn_gemv_bf16 with your own workspace).
- * Nothing here allocates: the first call on a device that splits K looks up that device's buffer
- * address (cudaGetSymbolAddress) with the device current, so make that first call before any
- * stream capture. Every call on a device shares the one buffer, which keeps the last call's
+ * call needs a workspace (more than 8 K ranges), its fp32 partial sums go to a buffer of
+ * GDN_GEMV_NOALLOC_MAX_FLOATS values that the library keeps on every GPU that loads it, until the
+ * process exits. A call whose splits * T * N exceeds that size is rejected with GDN_ERR_SCRATCH
+ * before anything is launched (pass 8 or fewer ranges, which need no buffer, or use gdn_gemv_bf16
+ * with your own workspace). Nothing here allocates: the first call on a device that uses the
+ * buffer looks up that device's buffer address (cudaGetSymbolAddress) with the device current, so
+ * make that first call before any stream capture. Every call on a device shares the one buffer, which keeps the last call's
  * partial sums (each call writes all the sums it reads, so no clearing is needed); calls that can
  * run at the same time on the GPU, e.g. on two streams, race on it and must be ordered.
  * Returns the codes of gdn_gemv_bf16, and GDN_ERR_SCRATCH.

@@ -38,7 +38,7 @@ GDN_FUSED_GATE_KDA, GDN_FUSED_GATE_GDN = 0, 1
 GDN_ACT_SILU, GDN_ACT_SIGMOID = 0, 1
 GDN_DEVERR_BAD_INDEX, GDN_DEVERR_BAD_WRITE_POS, GDN_DEVERR_TIMEOUT = 0x1, 0x2, 0x4
 GDN_KERNEL = {"auto": 0, "tile": 1, "pipe": 2}
-ABI_VERSION = 4
+ABI_VERSION = 5
 
 # every function the header declares
 EXPORTS = ("gdn_decode_step", "gdn_decode_step_indexed", "gdn_decode_buffered", "gdn_decode_fused",
@@ -85,7 +85,7 @@ class MambaArgs(ctypes.Structure):
 class GemvArgs(ctypes.Structure):
     _fields_ = [("T", _i32), ("N", _i32), ("Kd", _i32), ("out_dtype", _i32), ("x", _vp),
                 ("x_stride", _i64), ("W", _vp), ("y", _vp), ("y_stride", _i64), ("splits", _i32),
-                ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t)]
+                ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t), ("err_flags", _vp)]
 
 
 class GdnError(RuntimeError):
@@ -135,8 +135,9 @@ def lib():
             L.gdn_strerror.restype = ctypes.c_char_p
             L.gdn_abi_struct_size.argtypes = [ctypes.c_int]
             L.gdn_abi_struct_size.restype = ctypes.c_size_t
-            sizes = [L.gdn_abi_struct_size(i) for i in range(3)]
-            want = [ctypes.sizeof(GdnStepArgs), ctypes.sizeof(GdnRingArgs), ctypes.sizeof(GdnFusedArgs)]
+            sizes = [L.gdn_abi_struct_size(i) for i in range(4)]
+            want = [ctypes.sizeof(GdnStepArgs), ctypes.sizeof(GdnRingArgs), ctypes.sizeof(GdnFusedArgs),
+                    ctypes.sizeof(GemvArgs)]
             if sizes != want or L.gdn_abi_version() != ABI_VERSION:
                 raise RuntimeError(f"libgdn_decode.so ABI mismatch: struct sizes {sizes} vs {want}")
             _lib = L
@@ -460,10 +461,11 @@ def gemv_workspace(T, N, Kd, splits=0, device=None):
     return torch.empty(nbytes // 4, dtype=torch.float32, device=device or "cuda")
 
 
-def gdn_gemv_bf16(x, W, y, *, splits=0, workspace=None, stream=None, prepare=False):
+def gdn_gemv_bf16(x, W, y, *, splits=0, workspace=None, err_flags=None, stream=None, prepare=False):
     """Decode projection y [T, N] = x [T, Kd] W[N, Kd]^T (declared in include/gdn_gemv.h). x and W
     bf16 with dense rows (x may be a row view), y fp32 or bf16. With more than one K split (splits
-    = 0 lets the library choose) a workspace is needed: see gemv_workspace."""
+    = 0 lets the library choose) a workspace is needed: see gemv_workspace. err_flags: optional
+    int32 CUDA tensor of one element that a kernel giving up a bounded wait ORs a bit into."""
     torch = _torch()
     T, Kd = x.shape
     N = W.shape[0]
@@ -481,4 +483,6 @@ def gdn_gemv_bf16(x, W, y, *, splits=0, workspace=None, stream=None, prepare=Fal
     if workspace is not None:
         g.workspace = _ptr(_dense(workspace, "workspace"), "workspace", torch.float32)
         g.workspace_bytes = workspace.numel() * 4
-    return _run_or_prepare("gdn_gemv_bf16", (ctypes.byref(g),), (g, workspace), stream, prepare, y)
+    if err_flags is not None:
+        g.err_flags = _ptr(err_flags, "err_flags", torch.int32)
+    return _run_or_prepare("gdn_gemv_bf16", (ctypes.byref(g),), (g, workspace, err_flags), stream, prepare, y)

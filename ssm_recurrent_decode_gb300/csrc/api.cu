@@ -5,11 +5,12 @@
 #include <cmath>
 #include <cstring>
 
+#include "gdn_gemv.h"
 #include "gdn_launch.h"
 
 namespace {
 
-constexpr int kAbiVersion = 4;
+constexpr int kAbiVersion = 5;
 
 bool k_supported(int K) { return K == 16 || K == 32 || K == 64 || K == 128; }
 bool dtype_ok(int d) { return d == GDN_F32 || d == GDN_BF16; }
@@ -200,6 +201,7 @@ size_t gdn_abi_struct_size(int which)
     case 0: return sizeof(gdn_step_args);
     case 1: return sizeof(gdn_ring_args);
     case 2: return sizeof(gdn_fused_args);
+    case 3: return sizeof(gdn_gemv_args);
     default: return 0;
     }
 }

@@ -1,0 +1,54 @@
+// gemv_internal.h -- declarations shared by the decode projection's translation units (internal to
+// libgdn_decode.so).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+
+#include "gdn_gemv.h"
+
+namespace gdn {
+
+// How a launch's K ranges are combined: one range writes y itself; up to kGemvMaxCluster ranges
+// of a row tile form one thread-block cluster and add their sums through distributed shared
+// memory, in range order; more ranges write partial sums to the caller's workspace, added in range
+// order by a second kernel.
+constexpr int kGemvReduceNone = 0;
+constexpr int kGemvReduceWorkspace = 1;
+constexpr int kGemvReduceCluster = 2;
+constexpr int kGemvMaxCluster = 8;   // the portable cluster size
+
+inline int gemv_reduce_mode(int splits)
+{
+    return splits <= 1 ? kGemvReduceNone : (splits <= kGemvMaxCluster ? kGemvReduceCluster : kGemvReduceWorkspace);
+}
+
+// y[t, n] = v, rounded to y's dtype
+__device__ __forceinline__ void gemv_store(const gdn_gemv_args &P, int t, int n, float v)
+{
+    if (P.out_dtype == GDN_BF16)
+        static_cast<__nv_bfloat16 *>(P.y)[(size_t)t * P.y_stride + n] = __float2bfloat16_rn(v);
+    else
+        static_cast<float *>(P.y)[(size_t)t * P.y_stride + n] = v;
+}
+
+// tcgen05 form: output rows per CTA (the MMA's M), inputs per stage, token rows per pass (N)
+constexpr int kTcRows = 128;
+constexpr int kTcK = 64;
+constexpr int kTcTok = 16;
+constexpr int kTcMaxStages = 8;
+
+// dynamic shared memory of a tcgen05-form CTA with `stages` stages
+size_t gemv_tc_smem_bytes(int stages);
+
+// CTAs of the tcgen05 form resident on one SM of the current device
+int gemv_tc_resident_ctas(int stages);
+
+// launches the tcgen05 form over every pass of 16 token rows (as a cluster launch when the ranges
+// are combined in a cluster; a workspace sum is left to the caller); k_per_split is a multiple of
+// kTcK
+int gemv_tc_launch(const gdn_gemv_args &p, int splits, int k_per_split, int stages, cudaStream_t stream);
+
+}  // namespace gdn

@@ -2,15 +2,13 @@
 //
 // A weight-streaming, HBM-bound product of a handful of token rows with a bf16 weight matrix, in
 // two forms:
-//  - one token row: CUDA cores. Each warp owns 4 output rows and walks its K range 512 inputs at a
-//    time, every lane loading 16 bytes (8 bf16) of each row for two 256-input steps before using
-//    them; one x value feeds 4 rows.
-//  - two or more token rows: tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate), weight
-//    rows as the M operand and groups of 8 token rows as N, loaded straight from global memory into
-//    the operand registers; the tensor core sums 128-input groups and the groups are added in fp32
-//    registers. At 8 token rows a CUDA-core form needs about 4 FMAs per weight byte, close to the
-//    SM's FMA rate at HBM speed; the tensor core takes that work off the FMA pipe.
-// In both, the token rows' slice of x is staged in shared memory (cp.async) when it fits.
+//  - one token row: CUDA cores (this file). Each warp owns 4 output rows and walks its K range 512
+//    inputs at a time, every lane loading 16 bytes (8 bf16) of each row for two 256-input steps
+//    before using them; one x value feeds 4 rows. The row's slice of x is staged in shared memory
+//    (cp.async) when it fits.
+//  - two or more token rows: tcgen05 tensor cores with TMA-staged tiles (gemv_tc.cu). At 8 token
+//    rows a CUDA-core form needs about 4 FMAs per weight byte, close to the SM's FMA rate at HBM
+//    speed; the tensor core takes that work off the FMA pipe.
 // Split-K: blockIdx.y selects a K range whose partial sums go to the workspace, and a second small
 // kernel adds the ranges in order (deterministic).
 //
@@ -18,8 +16,11 @@
 #include <cstdint>
 #include <mutex>
 
+#include "gdn_cluster.cuh"
 #include "gdn_common.cuh"
+#include "gdn_pipe.cuh"
 #include "gdn_gemv.h"
+#include "gemv_internal.h"
 
 namespace gdn {
 
@@ -75,9 +76,10 @@ __device__ __forceinline__ float reduce_scatter32(float (&x)[32], int lane)
 // W [17408, 5120].
 template <int TOK>
 __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const __grid_constant__ gdn_gemv_args P, int t0,
-                                                            int nt, int k_per_split, int xs_elems)
+                                                            int nt, int k_per_split, int xs_elems, int mode)
 {
     extern __shared__ __align__(16) unsigned char gemv_sm[];
+    __shared__ float red[kGemvWarps * kRows * TOK];   // this K range's sums, cluster mode
     bf16 *xs = reinterpret_cast<bf16 *>(gemv_sm);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int split = blockIdx.y;
@@ -97,190 +99,83 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const __grid_constan
         __syncthreads();
     }
     const int n0 = (blockIdx.x * kGemvWarps + warp) * kRows;
-    if (n0 >= P.N) return;
-    float acc[kRows][TOK];
-#pragma unroll
-    for (int r = 0; r < kRows; ++r)
-#pragma unroll
-        for (int t = 0; t < TOK; ++t) acc[r][t] = 0.f;
-    auto x_at = [&](int t, int k) -> uint4 {
-        return staged ? reinterpret_cast<const uint4 *>(xs)[((size_t)t * krange + (k - k_begin)) / 8]
-                      : __ldg(reinterpret_cast<const uint4 *>(X + (size_t)(t0 + t) * P.x_stride + k));
-    };
-    auto fma_step = [&](const uint4 (&wr)[kRows], int k) {
-        float wf[kRows][8];
-#pragma unroll
-        for (int r = 0; r < kRows; ++r) unpack8(wr[r], wf[r]);
-#pragma unroll
-        for (int t = 0; t < TOK; ++t) {
-            if (t < nt) {
-                float xf[8];
-                unpack8(x_at(t, k), xf);
-#pragma unroll
-                for (int r = 0; r < kRows; ++r)
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) acc[r][t] = fmaf(wf[r][i], xf[i], acc[r][t]);
-            }
-        }
-    };
-    auto load_rows = [&](int k, uint4 (&wr)[kRows]) {
+    float sum = 0.f;
+    if (n0 < P.N) {   // whole warps
+        float acc[kRows][TOK];
 #pragma unroll
         for (int r = 0; r < kRows; ++r)
-            wr[r] = (n0 + r < P.N && k < k_end) ? __ldcs(reinterpret_cast<const uint4 *>(W + (size_t)(n0 + r) * P.Kd + k))
-                                                : make_uint4(0u, 0u, 0u, 0u);
-    };
-    for (int k = k_begin + lane * 8; k < k_end; k += 512) {
-        uint4 wa[kRows], wb[kRows];
-        load_rows(k, wa);
-        load_rows(k + 256, wb);
-        fma_step(wa, k);
-        if (k + 256 < k_end) fma_step(wb, k + 256);
+#pragma unroll
+            for (int t = 0; t < TOK; ++t) acc[r][t] = 0.f;
+        auto x_at = [&](int t, int k) -> uint4 {
+            return staged ? reinterpret_cast<const uint4 *>(xs)[((size_t)t * krange + (k - k_begin)) / 8]
+                          : __ldg(reinterpret_cast<const uint4 *>(X + (size_t)(t0 + t) * P.x_stride + k));
+        };
+        auto fma_step = [&](const uint4 (&wr)[kRows], int k) {
+            float wf[kRows][8];
+#pragma unroll
+            for (int r = 0; r < kRows; ++r) unpack8(wr[r], wf[r]);
+#pragma unroll
+            for (int t = 0; t < TOK; ++t) {
+                if (t < nt) {
+                    float xf[8];
+                    unpack8(x_at(t, k), xf);
+#pragma unroll
+                    for (int r = 0; r < kRows; ++r)
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) acc[r][t] = fmaf(wf[r][i], xf[i], acc[r][t]);
+                }
+            }
+        };
+        auto load_rows = [&](int k, uint4 (&wr)[kRows]) {
+#pragma unroll
+            for (int r = 0; r < kRows; ++r)
+                wr[r] = (n0 + r < P.N && k < k_end) ? __ldcs(reinterpret_cast<const uint4 *>(W + (size_t)(n0 + r) * P.Kd + k))
+                                                    : make_uint4(0u, 0u, 0u, 0u);
+        };
+        for (int k = k_begin + lane * 8; k < k_end; k += 512) {
+            uint4 wa[kRows], wb[kRows];
+            load_rows(k, wa);
+            load_rows(k + 256, wb);
+            fma_step(wa, k);
+            if (k + 256 < k_end) fma_step(wb, k + 256);
+        }
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = 0.f;
+#pragma unroll
+        for (int r = 0; r < kRows; ++r)
+#pragma unroll
+            for (int t = 0; t < TOK; ++t) v[r * TOK + t] = acc[r][t];
+        sum = reduce_scatter32(v, lane);
     }
-    float v[32];
-#pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = 0.f;
-#pragma unroll
-    for (int r = 0; r < kRows; ++r)
-#pragma unroll
-        for (int t = 0; t < TOK; ++t) v[r * TOK + t] = acc[r][t];
-    const float sum = reduce_scatter32(v, lane);
-    if (lane >= kRows * TOK) return;
+    // lane r * TOK + t holds (row n0 + r, token t0 + t)
+    if (mode == kGemvReduceCluster) {
+        // The K ranges of this row block are the CTAs of one cluster (rank = range). CTA r adds the
+        // ranges' sums of its share of the block's outputs in range order, reading the other
+        // CTAs' shared memory, and writes y.
+        constexpr int kEntries = kGemvWarps * kRows * TOK;
+        if (lane < kRows * TOK) red[warp * kRows * TOK + lane] = sum;
+        __syncwarp();
+        cluster_sync_all();
+        const int rank = (int)cluster_ctarank(), nr = (int)gridDim.y;
+        const int chunk = (kEntries + nr - 1) / nr;
+        const int e = rank * chunk + threadIdx.x;
+        if (threadIdx.x < chunk && e < kEntries) {
+            float total = 0.f;
+            for (int q = 0; q < nr; ++q) total += cluster_ld_f32(cluster_map(smem_u32(&red[e]), (uint32_t)q));
+            const int t = e % TOK, n = blockIdx.x * kGemvWarps * kRows + e / TOK;
+            if (t < nt && n < P.N) gemv_store(P, t0 + t, n, total);
+        }
+        cluster_sync_all();   // no CTA leaves while another still reads its shared memory
+        return;
+    }
+    if (lane >= kRows * TOK || n0 >= P.N) return;
     const int r = lane / TOK, t = lane - r * TOK, n = n0 + r;
     if (t >= nt || n >= P.N) return;
-    if (gridDim.y > 1) {
+    if (mode == kGemvReduceWorkspace)
         P.workspace[((size_t)split * P.T + t0 + t) * P.N + n] = sum;
-    } else if (P.out_dtype == GDN_BF16) {
-        static_cast<bf16 *>(P.y)[(size_t)(t0 + t) * P.y_stride + n] = __float2bfloat16_rn(sum);
-    } else {
-        static_cast<float *>(P.y)[(size_t)(t0 + t) * P.y_stride + n] = sum;
-    }
-}
-
-// Tensor-core form for passes of 2 or more token rows: one warp owns kMmaRows = 16 output rows and
-// runs mma.sync m16n8k16 (bf16 in, fp32 accumulate) with the weight rows as the M operand and up
-// to 8 token rows per group as the N operand. The k order inside a 32-input block is permuted the
-// same way for both operands (a sum over k does not depend on its order), so that every lane's
-// operands are one 16-byte load: lane (g, q) loads inputs 8q .. 8q + 7 of rows g and g + 8 and of
-// token row g; its first mma takes the low 8 bytes of each load, its second the high 8 bytes. The
-// weights go from global memory to registers with no shared-memory round trip; kMmaUnroll blocks
-// of loads are in flight per lane.
-constexpr int kMmaWarps = 8;
-constexpr int kMmaThreads = 32 * kMmaWarps;
-constexpr int kMmaRows = 16;
-constexpr int kMmaUnroll = 4;
-constexpr int kMmaKStep = 32 * kMmaUnroll;
-constexpr int kMmaMaxGroups = 2;  // groups of 8 token rows per pass
-// Token rows from which the tensor-core form runs. At one token row the CUDA-core form was as fast
-// or faster on GB300 (28.2 vs 32.2 us for W [17408, 5120], 30.0 vs 30.3 us for W [5120, 17408]).
-constexpr int kMmaMinTokens = 2;
-
-__device__ __forceinline__ void mma_16816_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                               uint32_t a3, uint32_t b0, uint32_t b1)
-{
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-        "{%8, %9}, {%0, %1, %2, %3};\n"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// One pass over up to 8G token rows (t0 .. t0 + nt - 1) and one K range. xs_stride > 0: the x slice
-// is staged in shared memory, xs_stride uint4 per token row (padded so that the two token rows a
-// quarter-warp reads fall in different banks).
-template <int G>
-__global__ void __launch_bounds__(kMmaThreads) gemv_mma_kernel(const __grid_constant__ gdn_gemv_args P, int t0,
-                                                               int nt, int k_per_split, int xs_stride)
-{
-    extern __shared__ __align__(16) unsigned char gemv_sm[];
-    uint4 *xs = reinterpret_cast<uint4 *>(gemv_sm);
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int g = lane >> 2, q = lane & 3;
-    const int split = blockIdx.y;
-    const int k_begin = split * k_per_split;
-    const int k_end = min(P.Kd, k_begin + k_per_split);
-    const int krange = max(0, k_end - k_begin);
-    const bf16 *X = static_cast<const bf16 *>(P.x);
-    const bool staged = xs_stride > 0;
-    if (staged) {
-        const int per_row = krange / 8;
-        for (int e = threadIdx.x; e < nt * per_row; e += kMmaThreads) {
-            const int t = e / per_row, c = e - t * per_row;
-            cp_async16(xs + t * xs_stride + c, X + (size_t)(t0 + t) * P.x_stride + k_begin + 8 * c);
-        }
-    }
-    const int n0 = (blockIdx.x * kMmaWarps + warp) * kMmaRows;
-    const int ra = n0 + g, rb = n0 + g + 8;
-    const bool va = ra < P.N, vb = rb < P.N;
-    const uint4 *Wa = reinterpret_cast<const uint4 *>(static_cast<const bf16 *>(P.W) + (size_t)(va ? ra : 0) * P.Kd);
-    const uint4 *Wb = reinterpret_cast<const uint4 *>(static_cast<const bf16 *>(P.W) + (size_t)(vb ? rb : 0) * P.Kd);
-    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-    uint4 wa[kMmaUnroll], wb[kMmaUnroll];
-    auto load_w = [&](int kb) {
-#pragma unroll
-        for (int u = 0; u < kMmaUnroll; ++u) {
-            const int k = kb + 32 * u + 8 * q;
-            const bool in = k < k_end;
-            wa[u] = (va && in) ? __ldcs(Wa + k / 8) : zero;
-            wb[u] = (vb && in) ? __ldcs(Wb + k / 8) : zero;
-        }
-    };
-    load_w(k_begin);   // the first group's weights are in flight while x lands in shared memory
-    if (staged) {
-        cp_async_wait_all();
-        __syncthreads();
-    }
-    if (n0 >= P.N) return;   // whole warps only, after the CTA-wide barrier
-
-    float acc[G][4];
-#pragma unroll
-    for (int j = 0; j < G; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
-
-    for (int kb = k_begin; kb < k_end; kb += kMmaKStep) {
-        if (kb != k_begin) load_w(kb);
-        // the tensor core sums one 128-input group; the groups are added in fp32 registers with
-        // round-to-nearest, so a long K range accumulates as a plain fp32 sum does
-        float part[G][4];
-#pragma unroll
-        for (int j = 0; j < G; ++j)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) part[j][e] = 0.f;
-#pragma unroll
-        for (int u = 0; u < kMmaUnroll; ++u) {
-            const int k = kb + 32 * u + 8 * q;
-#pragma unroll
-            for (int j = 0; j < G; ++j) {
-                const int t = 8 * j + g;
-                uint4 xv = zero;
-                if (t < nt && k < k_end)
-                    xv = staged ? xs[t * xs_stride + (k - k_begin) / 8]
-                                : __ldg(reinterpret_cast<const uint4 *>(X + (size_t)(t0 + t) * P.x_stride + k));
-                mma_16816_bf16(part[j], wa[u].x, wb[u].x, wa[u].y, wb[u].y, xv.x, xv.y);
-                mma_16816_bf16(part[j], wa[u].z, wb[u].z, wa[u].w, wb[u].w, xv.z, xv.w);
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < G; ++j)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[j][e] += part[j][e];
-    }
-    // accumulator fragment: acc[j][0..1] row g, tokens 8j + 2q + {0, 1}; acc[j][2..3] row g + 8
-#pragma unroll
-    for (int j = 0; j < G; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int n = e < 2 ? ra : rb;
-            const int t = 8 * j + 2 * q + (e & 1);
-            if (t >= nt || n >= P.N) continue;
-            if (gridDim.y > 1) {
-                P.workspace[((size_t)split * P.T + t0 + t) * P.N + n] = acc[j][e];
-            } else if (P.out_dtype == GDN_BF16) {
-                static_cast<bf16 *>(P.y)[(size_t)(t0 + t) * P.y_stride + n] = __float2bfloat16_rn(acc[j][e]);
-            } else {
-                static_cast<float *>(P.y)[(size_t)(t0 + t) * P.y_stride + n] = acc[j][e];
-            }
-        }
+    else
+        gemv_store(P, t0 + t, n, sum);
 }
 
 // y[t, n] = sum over the splits, in order
@@ -306,9 +201,18 @@ static int sm_count_gemv()
     return sms;
 }
 
+// The form that runs T token rows: CUDA cores for one, tcgen05 (gemv_tc.cu) from two. At one token
+// row the CUDA-core form was as fast or faster on GB300 (a tensor-core form measured 32.2 against
+// 28.2 us for W [17408, 5120]).
+constexpr int kTcMinTokens = 2;
+enum class Form { kCore, kTc };
+constexpr int kTcStages = 4;   // shared-memory stages of the tcgen05 form (18 KB each)
+
+static Form form_for(int T) { return T < kTcMinTokens ? Form::kCore : Form::kTc; }
+
 // The layout of one call: which form runs, its grid, its K ranges and its staged x slice.
 struct GemvPlan {
-    bool mma;            // tensor-core form (T >= kMmaMinTokens) or CUDA-core form (one token row)
+    Form form;
     int per_pass;        // token rows per pass over W
     int ctas_n;          // CTAs along N
     int k_per_split;     // inputs per K range (a whole number of the form's steps)
@@ -318,32 +222,27 @@ struct GemvPlan {
 static GemvPlan make_plan(int T, int N, int Kd, int splits)
 {
     GemvPlan pl;
-    pl.mma = T >= kMmaMinTokens;
-    pl.per_pass = pl.mma ? 8 * kMmaMaxGroups : 1;
-    const int rows = pl.mma ? kMmaWarps * kMmaRows : kGemvWarps * kRows;
+    pl.form = form_for(T);
+    int rows, gran;
+    if (pl.form == Form::kCore) pl.per_pass = 1, rows = kGemvWarps * kRows, gran = 256;
+    else pl.per_pass = kTcTok, rows = kTcRows, gran = kTcK;
     pl.ctas_n = (N + rows - 1) / rows;
-    const int gran = pl.mma ? kMmaKStep : 256;
     const int chunks = (Kd + gran - 1) / gran;
     pl.k_per_split = ((chunks + splits - 1) / splits) * gran;
     pl.krange = pl.k_per_split < Kd ? pl.k_per_split : Kd;
     return pl;
 }
 
-// Shared-memory bytes of a pass's staged x slice (0: it is too large and x is read through L1)
-// and the kernel's staging argument (tensor-core form: row stride in uint4, padded to 64 bytes past
-// a 128-byte boundary; CUDA-core form: elements).
+// Dynamic shared memory of a pass. CUDA-core form: its staged x slice (0 when the slice is too
+// large and x is read through L1), with the kernel's staging argument (elements). The tcgen05 form
+// stages x with its weight tiles.
 static size_t stage_bytes(const GemvPlan &pl, int nt, int *arg)
 {
-    size_t bytes;
-    int a;
-    if (pl.mma) {
-        a = ((pl.krange / 8 + 7) / 8) * 8 + 4;
-        bytes = (size_t)nt * a * 16;
-    } else {
-        a = nt * pl.krange;
-        bytes = (size_t)a * 2;
-    }
-    if (bytes > kStageMaxBytes) bytes = 0, a = 0;
+    if (arg) *arg = 0;
+    if (pl.form == Form::kTc) return gemv_tc_smem_bytes(kTcStages);
+    const int a = nt * pl.krange;
+    const size_t bytes = (size_t)a * 2;
+    if (bytes > kStageMaxBytes) return 0;
     if (arg) *arg = a;
     return bytes;
 }
@@ -351,19 +250,32 @@ static size_t stage_bytes(const GemvPlan &pl, int nt, int *arg)
 int gemv_launch(const gdn_gemv_args &p, int splits, cudaStream_t stream)
 {
     const GemvPlan pl = make_plan(p.T, p.N, p.Kd, splits);
-    const dim3 grid((unsigned)pl.ctas_n, (unsigned)splits);
-    for (int t0 = 0; t0 < p.T; t0 += pl.per_pass) {
-        const int nt = p.T - t0 < pl.per_pass ? p.T - t0 : pl.per_pass;
-        int xs = 0;
-        const size_t smem = stage_bytes(pl, nt, &xs);
-        if (!pl.mma)
-            gemv_kernel<1><<<grid, kGemvThreads, smem, stream>>>(p, t0, 1, pl.k_per_split, xs);
-        else if (nt <= 8)
-            gemv_mma_kernel<1><<<grid, kMmaThreads, smem, stream>>>(p, t0, nt, pl.k_per_split, xs);
-        else
-            gemv_mma_kernel<2><<<grid, kMmaThreads, smem, stream>>>(p, t0, nt, pl.k_per_split, xs);
+    const int mode = gemv_reduce_mode(splits);
+    if (pl.form == Form::kTc) {
+        const int rc = gemv_tc_launch(p, splits, pl.k_per_split, kTcStages, stream);
+        if (rc != GDN_OK) return rc;
+    } else {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        cfg.gridDim = dim3((unsigned)pl.ctas_n, (unsigned)splits);
+        cfg.blockDim = dim3(kGemvThreads);
+        cfg.stream = stream;
+        if (mode == kGemvReduceCluster) {
+            attr[0].id = cudaLaunchAttributeClusterDimension;   // the K ranges of a row block
+            attr[0].val.clusterDim.x = 1;
+            attr[0].val.clusterDim.y = (unsigned)splits;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+        }
+        for (int t0 = 0; t0 < p.T; ++t0) {
+            int xs = 0;
+            cfg.dynamicSmemBytes = stage_bytes(pl, 1, &xs);
+            if (cudaLaunchKernelEx(&cfg, gemv_kernel<1>, p, t0, 1, pl.k_per_split, xs, mode) != cudaSuccess)
+                return GDN_ERR_LAUNCH;
+        }
     }
-    if (splits > 1) {
+    if (mode == kGemvReduceWorkspace) {
         const long long total = (long long)p.T * p.N;
         long long blocks = (total + 255) / 256;
         if (blocks > 4 * 152) blocks = 4 * 152;
@@ -373,51 +285,48 @@ int gemv_launch(const gdn_gemv_args &p, int splits, cudaStream_t stream)
 }
 
 // CTAs of the form that runs T token rows that fit on one SM with `smem` bytes of dynamic shared
-// memory each (registers, threads and shared memory; the occupancy query is made once per device
-// and form; without a device, the counts of the sm_103a build: 4 CUDA-core, 4 and 3 tensor-core
-// CTAs for one and two token groups).
-static int resident_ctas(bool mma, int groups, size_t smem)
+// memory each. CUDA-core form: the occupancy query (registers, threads, shared memory), made once
+// per device; without a device, the count of the sm_103a build (4). tcgen05 form: its
+// shared-memory bound (gemv_tc.cu).
+static int resident_ctas(Form form, size_t smem)
 {
+    if (form == Form::kTc) return gemv_tc_resident_ctas(kTcStages);
     constexpr int kMaxDevices = 64;
+    constexpr int kFallback = 4;
     static std::mutex lock;
-    static int occ[kMaxDevices][3];        // [device][CUDA-core, mma G=1, mma G=2], 0 = not asked
+    static int occ[kMaxDevices];        // 0 = not asked yet
     static int smem_sm[kMaxDevices];
     int dev = 0, n = 0;
-    const int which = mma ? groups : 0;
-    static const int fallback[3] = {4, 4, 3};
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
         cudaGetLastError();
-        n = fallback[which];
+        n = kFallback;
         if (smem > 0 && (int)(228 * 1024 / (smem + 1024)) < n) n = (int)(228 * 1024 / (smem + 1024));
         return n < 1 ? 1 : n;
     }
-    {
-        std::lock_guard<std::mutex> g(lock);
-        if (!occ[dev][which]) {
-            cudaError_t rc;
-            if (which == 0) rc = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemv_kernel<1>, kGemvThreads, 0);
-            else if (which == 1) rc = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemv_mma_kernel<1>, kMmaThreads, 0);
-            else rc = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemv_mma_kernel<2>, kMmaThreads, 0);
-            if (rc != cudaSuccess || n < 1) { cudaGetLastError(); n = fallback[which]; }
-            occ[dev][which] = n;
-            int sm = 0;
-            if (cudaDeviceGetAttribute(&sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess || sm <= 0) {
-                cudaGetLastError();
-                sm = 228 * 1024;
-            }
-            smem_sm[dev] = sm;
+    std::lock_guard<std::mutex> g(lock);
+    if (!occ[dev]) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemv_kernel<1>, kGemvThreads, 0) != cudaSuccess || n < 1) {
+            cudaGetLastError();
+            n = kFallback;
         }
-        n = occ[dev][which];
-        if (smem > 0) {
-            const int by_smem = (int)(smem_sm[dev] / (smem + 1024));   // 1 KB reserved per CTA
-            if (by_smem < n) n = by_smem;
+        occ[dev] = n;
+        int sm = 0;
+        if (cudaDeviceGetAttribute(&sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess || sm <= 0) {
+            cudaGetLastError();
+            sm = 228 * 1024;
         }
+        smem_sm[dev] = sm;
+    }
+    n = occ[dev];
+    if (smem > 0) {
+        const int by_smem = (int)(smem_sm[dev] / (smem + 1024));   // 1 KB reserved per CTA
+        if (by_smem < n) n = by_smem;
     }
     return n < 1 ? 1 : n;
 }
 
 // The split count for splits == 0, from measurements on GB300 at the decode shapes. Candidates are
-// powers of two up to 64 with at least 512 inputs per range whose x slice fits the staging budget;
+// powers of two up to the cluster size (so that no workspace is needed) with at least 512 inputs per range whose x slice fits the staging budget;
 // the largest whose grid fits in one wave of resident CTAs wins (more CTAs per SM keep more weight
 // loads in flight); failing that, the smallest that fills at least two waves (a grid of about 1.2
 // waves leaves a tail of a few CTAs per SM and was the slowest choice).
@@ -425,7 +334,7 @@ int gemv_default_splits(int T, int N, int Kd)
 {
     const long long sms = sm_count_gemv();
     int one_wave = 0, two_waves = 0, last_staged = 0, last = 1;
-    for (int s = 1; s <= 64; s *= 2) {
+    for (int s = 1; s <= kGemvMaxCluster; s *= 2) {
         if (s > 1 && Kd / s < 512) break;
         last = s;
         const GemvPlan pl = make_plan(T, N, Kd, s);
@@ -433,7 +342,7 @@ int gemv_default_splits(int T, int N, int Kd)
         const size_t smem = stage_bytes(pl, nt, nullptr);
         if (smem == 0) continue;
         last_staged = s;
-        const long long slots = resident_ctas(pl.mma, (nt + 7) / 8, smem) * sms;
+        const long long slots = resident_ctas(pl.form, smem) * sms;
         const long long ctas = (long long)pl.ctas_n * s;
         if (ctas <= slots) one_wave = s;
         else if (ctas >= 2 * slots && !two_waves) two_waves = s;
@@ -459,7 +368,7 @@ int32_t gdn_gemv_default_splits(int32_t T, int32_t N, int32_t Kd)
 
 size_t gdn_gemv_workspace_bytes(int32_t T, int32_t N, int32_t splits)
 {
-    if (splits <= 1 || T < 0 || N < 0) return 0;
+    if (gdn::gemv_reduce_mode(splits) != gdn::kGemvReduceWorkspace || T < 0 || N < 0) return 0;
     return sizeof(float) * (size_t)splits * (size_t)T * (size_t)N;
 }
 
@@ -474,7 +383,7 @@ int gdn_gemv_bf16(const gdn_gemv_args *a, gdn_stream_t stream)
     if (!al16(a->x) || !al16(a->W) || (reinterpret_cast<uintptr_t>(a->y) % (a->out_dtype == GDN_BF16 ? 2 : 4)) != 0)
         return GDN_ERR_ALIGN;
     const int splits = a->splits > 0 ? a->splits : (a->Kd == 0 ? 1 : gdn::gemv_default_splits(a->T, a->N, a->Kd));
-    if (splits > 1) {
+    if (gdn::gemv_reduce_mode(splits) == gdn::kGemvReduceWorkspace) {
         if (!a->workspace) return GDN_ERR_NULL;
         if (a->workspace_bytes < gdn_gemv_workspace_bytes(a->T, a->N, splits)) return GDN_ERR_SHAPE;
         if ((reinterpret_cast<uintptr_t>(a->workspace) & 3u) != 0) return GDN_ERR_ALIGN;

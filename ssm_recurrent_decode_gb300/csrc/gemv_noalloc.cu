@@ -45,8 +45,8 @@ extern "C" int gdn_gemv_bf16_noalloc(const gdn_gemv_args *args, gdn_stream_t str
     if (a.splits == 0 && a.T > 0 && a.N > 0 && a.Kd > 0) a.splits = gdn_gemv_default_splits(a.T, a.N, a.Kd);
     a.workspace = nullptr;
     a.workspace_bytes = 0;
-    if (a.splits > 1 && a.T > 0 && a.N > 0) {
-        const size_t need = gdn_gemv_workspace_bytes(a.T, a.N, a.splits);
+    const size_t need = a.T > 0 && a.N > 0 ? gdn_gemv_workspace_bytes(a.T, a.N, a.splits) : 0;
+    if (need > 0) {   // more K ranges than one cluster holds
         if (need > sizeof(float) * (size_t)GDN_GEMV_NOALLOC_MAX_FLOATS) return GDN_ERR_SCRATCH;
         float *scratch = nullptr;
         const int rc = scratch_for_current_device(&scratch);

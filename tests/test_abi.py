@@ -42,6 +42,7 @@ def test_struct_layout_and_version():
     assert L.gdn_abi_struct_size(0) == ctypes.sizeof(gdn.GdnStepArgs)
     assert L.gdn_abi_struct_size(1) == ctypes.sizeof(gdn.GdnRingArgs)
     assert L.gdn_abi_struct_size(2) == ctypes.sizeof(gdn.GdnFusedArgs)
+    assert L.gdn_abi_struct_size(3) == ctypes.sizeof(gdn.GemvArgs)
     assert L.gdn_abi_struct_size(9) == 0
     assert L.gdn_abi_version() == gdn.ABI_VERSION
 
@@ -115,14 +116,17 @@ def test_gemv_checks():
     g.Kd = 128
     assert L.gdn_gemv_bf16(ctypes.byref(g), None) == -1  # NULL pointers
     g.x, g.W, g.y, g.x_stride, g.y_stride = 1 << 40, 1 << 41, 1 << 42, 128, 64
-    g.splits = 2                                       # needs a workspace
+    g.splits = 9                                       # more ranges than a cluster: a workspace
     assert L.gdn_gemv_bf16(ctypes.byref(g), None) == -1
     g.workspace, g.workspace_bytes = 1 << 43, 16
     assert L.gdn_gemv_bf16(ctypes.byref(g), None) == -2  # too small
     g.x = (1 << 40) + 8
     assert L.gdn_gemv_bf16(ctypes.byref(g), None) == -4
-    assert L.gdn_gemv_workspace_bytes(2, 64, 2) == 2 * 2 * 64 * 4
+    assert L.gdn_gemv_workspace_bytes(2, 64, 9) == 9 * 2 * 64 * 4
+    assert L.gdn_gemv_workspace_bytes(2, 64, 8) == 0     # up to 8 ranges add inside a cluster
     assert L.gdn_gemv_workspace_bytes(2, 64, 1) == 0
+    for T, N, Kd in ((1, 17408, 5120), (8, 5120, 17408)):
+        assert 1 <= L.gdn_gemv_default_splits(T, N, Kd) <= 8
 
 
 def test_empty_batch_launches_nothing():

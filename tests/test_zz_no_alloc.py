@@ -1,7 +1,7 @@
 """gdn_gemv_bf16_noalloc: the decode projection for callers that cannot allocate device memory
 (code that only receives raw pointers from a framework owning every allocation, serving loops that
-must never call cudaMalloc, fixed memory budgets). Its split-K partial sums live in a buffer the
-library holds itself. Called through the C ABI twice in a row, on two different shapes, it must
+must never call cudaMalloc, fixed memory budgets). With more K ranges than one thread-block
+cluster holds (8), its split-K partial sums live in a buffer the library holds itself. Called through the C ABI twice in a row, on two different shapes, it must
 give what gdn_gemv_bf16 with a caller workspace gives, within the fp32 tolerance of the other
 tests; a request larger than its buffer is refused before anything runs.
 
@@ -53,21 +53,24 @@ def _inputs(T, N, Kd, seed):
 
 def test_no_alloc_gemv_matches_the_workspace_entry_point_on_two_calls_in_a_row():
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
-    shapes = [(4, 17408, 5120, 31), (3, 5120, 17408, 32)]   # [N, Kd] of the projections listed for decode
-    for T, N, Kd, seed in shapes:
+    # [N, Kd] of the projections listed for decode: two calls with more than 8 K ranges (the
+    # buffer is used), then one with the library's choice (ranges added inside a cluster)
+    shapes = [(4, 17408, 5120, 31, 12), (3, 5120, 17408, 32, 16), (2, 5120, 17408, 34, 0)]
+    for T, N, Kd, seed, splits in shapes:
         x, W = _inputs(T, N, Kd, seed)
-        assert gdn.lib().gdn_gemv_default_splits(T, N, Kd) > 1   # the buffer is really used
+        uses_buffer = gdn.lib().gdn_gemv_workspace_bytes(T, N, splits) > 0
+        assert uses_buffer == (splits > 8)
         want = torch.empty((T, N), device="cuda")
-        gdn.gdn_gemv_bf16(x, W, want, workspace=gdn.gemv_workspace(T, N, Kd))
+        gdn.gdn_gemv_bf16(x, W, want, splits=splits, workspace=gdn.gemv_workspace(T, N, Kd, splits))
         got = torch.full((T, N), float("nan"), device="cuda")
-        assert _noalloc(x, W, got) == 0
+        assert _noalloc(x, W, got, splits) == 0
         torch.cuda.synchronize()
         assert np.all(np.isfinite(got.cpu().numpy()))
         assert rel_err(got.cpu().numpy(), want.cpu().numpy()) <= 1e-5
 
 
 def test_no_alloc_gemv_refuses_more_than_its_buffer():
-    T, N, Kd, splits = 8, 65536, 1024, 4          # 8 * 65536 * 4 fp32 partial sums > 1 Mi
+    T, N, Kd, splits = 8, 65536, 1024, 16         # 16 * 8 * 65536 fp32 partial sums > 1 Mi
     assert splits * T * N > MAX_FLOATS
     x, W = _inputs(T, N, Kd, 33)
     y = torch.full((T, N), 7.0, device="cuda")
