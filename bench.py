@@ -73,6 +73,8 @@ KERNEL_FILES = {
     "fused": ["ssm_recurrent_decode_gb300/csrc/fused_pipe.cu", "ssm_recurrent_decode_gb300/csrc/gdn_pipe.cuh",
               "ssm_recurrent_decode_gb300/csrc/gdn_tile.cuh", "ssm_recurrent_decode_gb300/csrc/gdn_common.cuh"],
     "mamba": ["ssm_recurrent_decode_gb300/csrc/mamba_kernel.cu", "ssm_recurrent_decode_gb300/csrc/gdn_common.cuh"],
+    "front": ["ssm_recurrent_decode_gb300/csrc/front.cu", "ssm_recurrent_decode_gb300/csrc/gemv_kernel.cu",
+              "ssm_recurrent_decode_gb300/csrc/gemv_tc.cu", "ssm_recurrent_decode_gb300/csrc/fused_pipe.cu"],
     "gemv": ["ssm_recurrent_decode_gb300/csrc/gemv_kernel.cu", "ssm_recurrent_decode_gb300/csrc/gemv_tc.cu",
              "ssm_recurrent_decode_gb300/csrc/gemv_internal.h", "ssm_recurrent_decode_gb300/csrc/gdn_cluster.cuh",
              "ssm_recurrent_decode_gb300/csrc/gdn_pipe.cuh", "ssm_recurrent_decode_gb300/csrc/gdn_common.cuh"],
@@ -864,13 +866,90 @@ def run_gemv(args):
     return h.finish(line)
 
 
+def run_front(args):
+    """One DeltaNet layer's decode forward (gdn_decode_front): input projection -> conv update,
+    delta step, gated RMSNorm -> output projection, at the Optimization Log's model width 5120 with
+    32 heads of 128 (GDN gate), T tokens; synthetic bf16 weights N(0, 1/fan_in)."""
+    import numpy as np
+    import torch
+    import gdn_synth as syn
+    import ssm_recurrent_decode_gb300 as gdn
+    h = Harness(args)
+    gdn.lib()
+    T, hidden, heads, D = args.T, args.hidden, 32, 128
+    dim = heads * D
+    P = gdn.front_proj_width(heads, D, "gdn")
+    seed = 777 + h.rank
+    num_slots = T + 8
+    ins = syn.fused_inputs(T, heads, D, num_slots, seed)
+    dev = h.dev
+    conv_w = torch.from_numpy(ins["conv_w"]).to(dev)
+    conv_state = torch.from_numpy(ins["conv_state"].view(np.int16)).view(torch.bfloat16).to(dev)
+    A_log = torch.from_numpy(ins["A_log"]).to(dev)
+    dt_bias = torch.from_numpy(np.ascontiguousarray(ins["dt_bias"][:heads])).to(dev)
+    norm_w = torch.from_numpy(ins["norm_w"]).to(dev)
+    idx = torch.arange(1, T + 1, dtype=torch.int32, device=dev)
+    x = torch.empty((T, hidden), dtype=torch.bfloat16, device=dev)
+    syn.fill_normal_(x, seed, syn.Tag.X, 0, 1.0)
+    z = torch.empty((T, P), dtype=torch.bfloat16, device=dev)
+    o = torch.empty((T, dim), dtype=torch.bfloat16, device=dev)
+    y = torch.empty((T, hidden), dtype=torch.bfloat16, device=dev)
+    w_bytes = (P * hidden + hidden * dim) * 2
+    state_bytes = num_slots * heads * D * D * 4
+    n_pools = pool_count(w_bytes + state_bytes, dev)
+    layers = []
+    for p in range(n_pools):               # independent layers (weights and state), rotated
+        W_in = torch.empty((P, hidden), dtype=torch.bfloat16, device=dev)
+        W_out = torch.empty((hidden, dim), dtype=torch.bfloat16, device=dev)
+        syn.fill_normal_(W_in, seed, syn.Tag.CONV_W, 1, hidden ** -0.5, layer=p)
+        syn.fill_normal_(W_out, seed, syn.Tag.CONV_W, 2, dim ** -0.5, layer=p)
+        st = torch.empty((num_slots, heads, D, D), dtype=torch.float32, device=dev)
+        syn.fill_normal_(st, seed, syn.Tag.STATE, 0, 1.0, layer=p)
+        layers.append((W_in, W_out, st))
+    calls = [gdn.gdn_decode_front(x, W_in, W_out, z, o, y, conv_w, conv_state, A_log, dt_bias, st,
+                                  idx, norm_w, pad_slot_id=0, gate_kind="gdn", prepare=True)
+             for W_in, W_out, st in layers]
+    in_splits = gdn.lib().gdn_gemv_default_splits(T, P, hidden)
+    out_splits = gdn.lib().gdn_gemv_default_splits(T, hidden, dim)
+
+    def step(i):
+        calls[i % n_pools]()
+
+    per_graph = max(64, n_pools)
+    ms, steps, clk = h.time_graph(step, args.steps, args.warmup, per_graph)
+    (ms,) = max_over_ranks([ms], h.world)
+    if h.rank != 0:
+        return h.finish(None)
+    tile_bytes = 2 * T * heads * D * D * 4            # each token's state tile read and written
+    io = (T * hidden * 2 + 2 * T * P * 2               # x; z written and read
+          + 2 * T * 3 * dim * 3 * 2 + 3 * dim * 4 * 4  # conv state read + write, conv weights
+          + 2 * T * dim * 2 + T * hidden * 2           # o written and read, y
+          + heads * 8 + D * 4 + T * 4)
+    total = w_bytes + tile_bytes + io
+    gbs = h.world * total / (ms * 1e-3) / 1e9
+    line = base_line(
+        h, gbs, ms, steps, args.warmup,
+        f"DeltaNet layer decode front: T={T}, hidden {hidden}, {heads} heads x {D} (GDN gate), "
+        f"in_proj [{P}, {hidden}] + conv + step + gated RMSNorm + out_proj [{hidden}, {dim}], bf16 "
+        f"weights ({w_bytes / 1e6:.0f} MB)",
+        {"T": T, "hidden": hidden, "heads": heads, "head_dim": D, "proj_width": P,
+         "in_splits": in_splits, "out_splits": out_splits, "weight_bytes": w_bytes,
+         "layers_rotated": n_pools, "timing": f"CUDA-graph replays of {per_graph} calls (3 launches each)"},
+        steps * 3)
+    line["metric"] = "decode layer front GB/s (weights, state, activations)"
+    line["roofline"] = roofline(total, ms, "front", f"front_T{T}")
+    line["roofline"]["scope"] = "whole call: input projection, fused decode, output projection"
+    line["clocks"] = clk
+    return h.finish(line)
+
+
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=10000)
     p.add_argument("--warmup", type=int, default=50)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=["packed", "buffered", "fused", "stack", "mamba", "gemv"],
+    p.add_argument("--workload", choices=["packed", "buffered", "fused", "stack", "mamba", "gemv", "front"],
                    default="packed")
     p.add_argument("--B", type=int, default=256)
     p.add_argument("--L", type=int, default=16)
@@ -878,6 +957,7 @@ def main(argv=None):
     p.add_argument("--layout", choices=["DS", "SD"], default="DS")
     p.add_argument("--state-dtype", choices=["f32", "bf16"], default="f32")
     p.add_argument("--D", type=int, default=1536)
+    p.add_argument("--hidden", type=int, default=5120, help="model width of the front workload")
     p.add_argument("--gemv-n", type=int, default=17408)
     p.add_argument("--gemv-k", type=int, default=5120)
     p.add_argument("--gemv-splits", type=int, default=0, help="K ranges (0: the library's choice)")
@@ -891,7 +971,8 @@ def main(argv=None):
     if args.impl == "reference":
         return run_reference(args)
     return {"packed": run_packed, "buffered": run_buffered, "fused": run_fused,
-            "stack": run_stack, "mamba": run_mamba, "gemv": run_gemv}[args.workload](args)
+            "stack": run_stack, "mamba": run_mamba, "gemv": run_gemv,
+            "front": run_front}[args.workload](args)
 
 
 if __name__ == "__main__":

@@ -166,6 +166,10 @@ typedef struct gdn_fused_args {
     int32_t kernel;           /* GDN_KERNEL_AUTO: the pipelined kernel when head_dim == 128, the conv
                                  state is in the DS or SD layout and rows are 16-byte aligned, else
                                  the per-tile kernel; GDN_KERNEL_TILE / GDN_KERNEL_PIPE force one */
+    int64_t raw_g_stride;     /* row (token) strides in elements of raw_g, raw_beta and out_gate, at
+                                 least the dense row width; 0 selects the dense width. The pipelined */
+    int64_t raw_beta_stride;  /* kernel needs out_gate's (and a KDA raw_g's) to be a multiple of 8, */
+    int64_t out_gate_stride;  /* like x_stride. Lets the op read views of one projection output. */
 } gdn_fused_args;
 
 /*
@@ -227,10 +231,10 @@ int gdn_selftest_bounded_wait(int32_t *err_flags, int64_t limit_cycles, int32_t 
 const char *gdn_strerror(int status);
 
 /* ABI checks for bindings: sizeof of the args structs (which: 0 step, 1 ring, 2 fused, 3 the
- * decode projection's gdn_gemv_args of gdn_gemv.h). */
+ * decode projection's gdn_gemv_args of gdn_gemv.h, 4 gdn_front_args of gdn_front.h). */
 size_t gdn_abi_struct_size(int which);
 
-/* Library ABI version (incremented on any change of the args structs; currently 5). */
+/* Library ABI version (incremented on any change of the args structs; currently 6). */
 int gdn_abi_version(void);
 
 #ifdef __cplusplus

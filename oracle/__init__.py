@@ -6,7 +6,7 @@ path. The arithmetic lives in ``gdn_oracle.c`` (plain C, fp64, loops in the orde
 the method); this module only builds that file with gcc, moves dense fp64 numpy arrays in and out
 and splits packed inputs into their named parts.
 
-Readings of points the sources leave open (also listed in the design doc):
+Readings of points the sources leave open:
   * packed ``mixed_qkv`` row = [q (H*K) | k (H*K) | v (HV*V)], each head-major;
   * q/k head of value head hv is hv // (HV // H);
   * L2 norm is x / sqrt(sum x^2 + 1e-6); the K^-1/2 scale multiplies the normalised q;
@@ -318,3 +318,33 @@ def gemv(x, W):
     y = np.empty((T, N))
     lib().oracle_gemv(T, N, Kd, _p(x), _p(W), _p(y))
     return y
+
+
+def front_columns(heads, D, gate_kind="gdn"):
+    """Column ranges of the front's projection output z: q|k|v (3*dim), out_gate (dim), raw_g
+    (dim for the KDA gate, heads for the GDN gate), raw_beta (heads)."""
+    dim = heads * D
+    G = dim if gate_kind == "kda" else heads
+    return {"qkv": (0, 3 * dim), "out_gate": (3 * dim, 4 * dim), "raw_g": (4 * dim, 4 * dim + G),
+            "raw_beta": (4 * dim + G, 4 * dim + G + heads)}
+
+
+def decode_front(x, W_in, W_out, conv_w, conv_state, A_log, dt_bias, state, norm_w, *, heads, D,
+                 idx, pad_slot=0, gate_kind="gdn", gate_form=0, lower_bound=-5.0, act="silu",
+                 norm_eps=1e-5):
+    """One DeltaNet layer's decode forward ("Optimization Log", Integration: proj + conv1d +
+    recurrent + norm_gated + output): z = x W_in^T, then the fused decode on the columns of z,
+    then y = o W_out^T. z and o are rounded to bf16, the dtype the front stores them in; conv_state
+    and state (float64) are updated in place. Returns (y, bad)."""
+    x = _f64(x)
+    T = x.shape[0]
+    z = round_bf16(gemv(x, W_in))
+    col = front_columns(heads, D, gate_kind)
+    part = lambda name: z[:, col[name][0]:col[name][1]]
+    raw_g = part("raw_g").reshape(T, heads, D) if gate_kind == "kda" else part("raw_g")
+    o, bad = fused_kda(part("qkv"), conv_w, conv_state, raw_g, part("raw_beta"), A_log, dt_bias,
+                       state, part("out_gate").reshape(T, heads, D), norm_w, idx=idx,
+                       pad_slot=pad_slot, lower_bound=lower_bound, gate_form=gate_form,
+                       gate_kind=gate_kind, norm_eps=norm_eps, act=act)
+    o = round_bf16(o.reshape(T, heads * D))
+    return gemv(o, W_out), bad

@@ -38,13 +38,14 @@ GDN_FUSED_GATE_KDA, GDN_FUSED_GATE_GDN = 0, 1
 GDN_ACT_SILU, GDN_ACT_SIGMOID = 0, 1
 GDN_DEVERR_BAD_INDEX, GDN_DEVERR_BAD_WRITE_POS, GDN_DEVERR_TIMEOUT = 0x1, 0x2, 0x4
 GDN_KERNEL = {"auto": 0, "tile": 1, "pipe": 2}
-ABI_VERSION = 5
+ABI_VERSION = 6
 
 # every function the header declares
 EXPORTS = ("gdn_decode_step", "gdn_decode_step_indexed", "gdn_decode_buffered", "gdn_decode_fused",
            "gdn_strerror", "gdn_abi_struct_size", "gdn_abi_version", "mamba_selective_scan_decode",
            "gdn_selftest_bounded_wait", "gdn_gemv_bf16", "gdn_gemv_default_splits",
-           "gdn_gemv_workspace_bytes", "gdn_gemv_bf16_noalloc")
+           "gdn_gemv_workspace_bytes", "gdn_gemv_bf16_noalloc", "gdn_decode_front",
+           "gdn_front_proj_width")
 
 _i32, _i64, _f32, _vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
 
@@ -73,7 +74,14 @@ class GdnFusedArgs(ctypes.Structure):
                 ("lower_bound", _f32), ("scale", _f32), ("use_qk_l2norm", _i32),
                 ("state", _vp), ("state_indices", _vp), ("pad_slot_id", _i32),
                 ("out_gate", _vp), ("norm_w", _vp), ("norm_eps", _f32), ("gate_act", _i32),
-                ("out", _vp), ("err_flags", _vp), ("kernel", _i32)]
+                ("out", _vp), ("err_flags", _vp), ("kernel", _i32), ("raw_g_stride", _i64),
+                ("raw_beta_stride", _i64), ("out_gate_stride", _i64)]
+
+
+class GdnFrontArgs(ctypes.Structure):
+    _fields_ = [("T", _i32), ("hidden", _i32), ("x", _vp), ("x_stride", _i64), ("W_in", _vp),
+                ("W_out", _vp), ("z", _vp), ("o", _vp), ("y", _vp), ("y_dtype", _i32),
+                ("y_stride", _i64), ("in_splits", _i32), ("out_splits", _i32), ("core", GdnFusedArgs)]
 
 
 class MambaArgs(ctypes.Structure):
@@ -121,6 +129,10 @@ def lib():
             L.mamba_selective_scan_decode.argtypes = [ctypes.POINTER(MambaArgs), _vp]
             L.mamba_selective_scan_decode.restype = ctypes.c_int
             L.gdn_selftest_bounded_wait.argtypes = [_vp, _i64, _i32, _vp]
+            L.gdn_decode_front.argtypes = [ctypes.POINTER(GdnFrontArgs), _vp]
+            L.gdn_decode_front.restype = ctypes.c_int
+            L.gdn_front_proj_width.argtypes = [_i32, _i32, _i32]
+            L.gdn_front_proj_width.restype = _i64
             L.gdn_gemv_bf16.argtypes = [ctypes.POINTER(GemvArgs), _vp]
             L.gdn_gemv_bf16.restype = ctypes.c_int
             L.gdn_gemv_default_splits.argtypes = [_i32, _i32, _i32]
@@ -135,9 +147,9 @@ def lib():
             L.gdn_strerror.restype = ctypes.c_char_p
             L.gdn_abi_struct_size.argtypes = [ctypes.c_int]
             L.gdn_abi_struct_size.restype = ctypes.c_size_t
-            sizes = [L.gdn_abi_struct_size(i) for i in range(4)]
+            sizes = [L.gdn_abi_struct_size(i) for i in range(5)]
             want = [ctypes.sizeof(GdnStepArgs), ctypes.sizeof(GdnRingArgs), ctypes.sizeof(GdnFusedArgs),
-                    ctypes.sizeof(GemvArgs)]
+                    ctypes.sizeof(GemvArgs), ctypes.sizeof(GdnFrontArgs)]
             if sizes != want or L.gdn_abi_version() != ABI_VERSION:
                 raise RuntimeError(f"libgdn_decode.so ABI mismatch: struct sizes {sizes} vs {want}")
             _lib = L
@@ -340,6 +352,83 @@ def gdn_decode_buffered(q, k, v, state, out, d_cache, k_cache, g_cache, write_po
                             ctypes.byref(r)), (s, r), stream, prepare, out)
 
 
+def _fused_core(conv_w, conv_state, A_log, dt_bias, state, state_indices, norm_w, *, conv_b,
+                pad_slot_id, gate_kind, kda_gate_form, lower_bound, scale, use_qk_l2norm, norm_eps,
+                gate_act, err_flags, kernel):
+    """The arguments of gdn_decode_fused that do not depend on the per-token inputs."""
+    torch = _torch()
+    _dense(state, "state")
+    num_slots, heads, D, _ = state.shape
+    f = GdnFusedArgs()
+    f.heads, f.head_dim, f.num_slots = heads, D, num_slots
+    f.conv_w = _ptr(_dense(conv_w, "conv_w"), "conv_w", torch.float32)
+    f.conv_b = _ptr(conv_b, "conv_b", torch.float32)
+    if tuple(conv_state.shape) != (num_slots, 3 * heads * D, 3):
+        raise ValueError("conv_state must have logical shape [num_slots, 3*dim, 3]")
+    f.conv_state = _ptr(conv_state, "conv_state", torch.bfloat16)
+    f.cs_stride_slot, f.cs_stride_chan, f.cs_stride_tap = conv_state.stride()
+    f.gate_kind = {"kda": GDN_FUSED_GATE_KDA, "gdn": GDN_FUSED_GATE_GDN}[gate_kind]
+    f.kda_gate_form = int(kda_gate_form)
+    f.A_log = _ptr(_dense(A_log, "A_log"), "A_log", torch.float32)
+    f.dt_bias = _ptr(_dense(dt_bias, "dt_bias"), "dt_bias", torch.float32)
+    f.lower_bound = float(lower_bound)
+    f.scale = 0.0 if scale is None else float(scale)
+    f.use_qk_l2norm = int(bool(use_qk_l2norm))
+    f.state = _ptr(state, "state", torch.float32)
+    f.state_indices = _ptr(_dense(state_indices, "state_indices"), "state_indices", torch.int32)
+    f.pad_slot_id = int(pad_slot_id)
+    f.norm_w = _ptr(_dense(norm_w, "norm_w"), "norm_w", torch.float32)
+    f.norm_eps = float(norm_eps)
+    f.gate_act = {"silu": GDN_ACT_SILU, "sigmoid": GDN_ACT_SIGMOID}[gate_act]
+    f.err_flags = _ptr(err_flags, "err_flags", torch.int32)
+    f.kernel = GDN_KERNEL[kernel]
+    return f
+
+
+def front_proj_width(heads, head_dim, gate_kind="gdn"):
+    """P, the width of the front's input projection output z (see gdn_decode_front)."""
+    code = {"kda": GDN_FUSED_GATE_KDA, "gdn": GDN_FUSED_GATE_GDN}[gate_kind]
+    return int(lib().gdn_front_proj_width(int(heads), int(head_dim), code))
+
+
+def gdn_decode_front(x, W_in, W_out, z, o, y, conv_w, conv_state, A_log, dt_bias, state,
+                     state_indices, norm_w, *, conv_b=None, pad_slot_id=0, gate_kind="gdn",
+                     kda_gate_form=0, lower_bound=-5.0, scale=None, use_qk_l2norm=True,
+                     norm_eps=1e-5, gate_act="silu", in_splits=0, out_splits=0, err_flags=None,
+                     kernel="auto", stream=None, prepare=False):
+    """One DeltaNet layer's decode forward (declared in include/gdn_front.h): z = x W_in^T (bf16
+    z [T, P], columns q|k|v, out_gate, raw_g, raw_beta), o = conv -> step -> gated RMSNorm on views
+    of z, y = o W_out^T. x bf16 [T, hidden] (row view allowed); W_in bf16 [P, hidden]; W_out bf16
+    [hidden, dim]; z, o dense bf16 scratch [T, P], [T, dim]; y fp32 or bf16 [T, hidden]; the rest
+    as for gdn_decode_fused."""
+    torch = _torch()
+    T, hidden = x.shape
+    c = _fused_core(conv_w, conv_state, A_log, dt_bias, state, state_indices, norm_w,
+                    conv_b=conv_b, pad_slot_id=pad_slot_id, gate_kind=gate_kind,
+                    kda_gate_form=kda_gate_form, lower_bound=lower_bound, scale=scale,
+                    use_qk_l2norm=use_qk_l2norm, norm_eps=norm_eps, gate_act=gate_act,
+                    err_flags=err_flags, kernel=kernel)
+    P = front_proj_width(c.heads, c.head_dim, gate_kind)
+    dim = c.heads * c.head_dim
+    if tuple(W_in.shape) != (P, hidden) or tuple(W_out.shape) != (hidden, dim):
+        raise ValueError(f"expected W_in [{P}, {hidden}] and W_out [{hidden}, {dim}]")
+    if tuple(z.shape) != (T, P) or tuple(o.shape) != (T, dim) or tuple(y.shape) != (T, hidden):
+        raise ValueError(f"expected z [{T}, {P}], o [{T}, {dim}], y [{T}, {hidden}]")
+    if x.stride(1) != 1 or y.stride(1) != 1:
+        raise ValueError("x and y need unit inner stride")
+    a = GdnFrontArgs()
+    a.T, a.hidden = T, hidden
+    a.x, a.x_stride = _ptr(x, "x", torch.bfloat16), x.stride(0)
+    a.W_in = _ptr(_dense(W_in, "W_in"), "W_in", torch.bfloat16)
+    a.W_out = _ptr(_dense(W_out, "W_out"), "W_out", torch.bfloat16)
+    a.z = _ptr(_dense(z, "z"), "z", torch.bfloat16)
+    a.o = _ptr(_dense(o, "o"), "o", torch.bfloat16)
+    a.y, a.y_dtype, a.y_stride = _ptr(y, "y"), _dtype_code(y), y.stride(0)
+    a.in_splits, a.out_splits = int(in_splits), int(out_splits)
+    a.core = c
+    return _run_or_prepare("gdn_decode_front", (ctypes.byref(a),), (a,), stream, prepare, y)
+
+
 def gdn_decode_fused(x, conv_w, conv_state, raw_g, raw_beta, A_log, dt_bias, state, state_indices,
                      out_gate, norm_w, out, *, conv_b=None, pad_slot_id=0, gate_kind="kda",
                      kda_gate_form=0, lower_bound=-5.0, scale=None, use_qk_l2norm=True,
@@ -353,41 +442,27 @@ def gdn_decode_fused(x, conv_w, conv_state, raw_g, raw_beta, A_log, dt_bias, sta
     transposed view of [num_slots, 3, 3*dim]); raw_g bf16 [T, heads, D] (kda) or [T, heads] (gdn);
     raw_beta bf16 [T, heads]; A_log fp32 [heads]; dt_bias fp32 [heads*D] (kda) or [heads] (gdn);
     state fp32 [num_slots, heads, D, D]; state_indices int32 [T]; out_gate bf16 [T, heads, D];
-    norm_w fp32 [D]; out bf16 [T, heads, D]."""
+    norm_w fp32 [D]; out bf16 [T, heads, D]. raw_g, raw_beta and out_gate may be row views (any
+    token stride, dense within a row), e.g. slices of one projection output."""
     torch = _torch()
-    _dense(state, "state")
-    num_slots, heads, D, _ = state.shape
     T = x.shape[0]
-    f = GdnFusedArgs()
-    f.T, f.heads, f.head_dim, f.num_slots = T, heads, D, num_slots
+    f = _fused_core(conv_w, conv_state, A_log, dt_bias, state, state_indices, norm_w,
+                    conv_b=conv_b, pad_slot_id=pad_slot_id, gate_kind=gate_kind,
+                    kda_gate_form=kda_gate_form, lower_bound=lower_bound, scale=scale,
+                    use_qk_l2norm=use_qk_l2norm, norm_eps=norm_eps, gate_act=gate_act,
+                    err_flags=err_flags, kernel=kernel)
+    heads, D = f.heads, f.head_dim
+    f.T = T
     if x.stride(1) != 1:
         raise ValueError("x must have unit inner stride")
     f.x, f.x_stride = _ptr(x, "x", torch.bfloat16), x.stride(0)
-    f.conv_w = _ptr(_dense(conv_w, "conv_w"), "conv_w", torch.float32)
-    f.conv_b = _ptr(conv_b, "conv_b", torch.float32)
-    if tuple(conv_state.shape) != (num_slots, 3 * heads * D, 3):
-        raise ValueError("conv_state must have logical shape [num_slots, 3*dim, 3]")
-    f.conv_state = _ptr(conv_state, "conv_state", torch.bfloat16)
-    f.cs_stride_slot, f.cs_stride_chan, f.cs_stride_tap = conv_state.stride()
-    f.gate_kind = {"kda": GDN_FUSED_GATE_KDA, "gdn": GDN_FUSED_GATE_GDN}[gate_kind]
-    f.kda_gate_form = int(kda_gate_form)
-    f.raw_g = _ptr(_dense(raw_g, "raw_g"), "raw_g", torch.bfloat16)
-    f.raw_beta = _ptr(_dense(raw_beta, "raw_beta"), "raw_beta", torch.bfloat16)
-    f.A_log = _ptr(_dense(A_log, "A_log"), "A_log", torch.float32)
-    f.dt_bias = _ptr(_dense(dt_bias, "dt_bias"), "dt_bias", torch.float32)
-    f.lower_bound = float(lower_bound)
-    f.scale = 0.0 if scale is None else float(scale)
-    f.use_qk_l2norm = int(bool(use_qk_l2norm))
-    f.state = _ptr(state, "state", torch.float32)
-    f.state_indices = _ptr(_dense(state_indices, "state_indices"), "state_indices", torch.int32)
-    f.pad_slot_id = int(pad_slot_id)
-    f.out_gate = _ptr(_dense(out_gate, "out_gate"), "out_gate", torch.bfloat16)
-    f.norm_w = _ptr(_dense(norm_w, "norm_w"), "norm_w", torch.float32)
-    f.norm_eps = float(norm_eps)
-    f.gate_act = {"silu": GDN_ACT_SILU, "sigmoid": GDN_ACT_SIGMOID}[gate_act]
+    f.raw_g_stride = _rows(raw_g, "raw_g", heads * D if gate_kind == "kda" else heads)
+    f.raw_g = _ptr(raw_g, "raw_g", torch.bfloat16)
+    f.raw_beta_stride = _rows(raw_beta, "raw_beta", heads)
+    f.raw_beta = _ptr(raw_beta, "raw_beta", torch.bfloat16)
+    f.out_gate_stride = _rows(out_gate, "out_gate", heads * D)
+    f.out_gate = _ptr(out_gate, "out_gate", torch.bfloat16)
     f.out = _ptr(_dense(out, "out"), "out", torch.bfloat16)
-    f.err_flags = _ptr(err_flags, "err_flags", torch.int32)
-    f.kernel = GDN_KERNEL[kernel]
     return _run_or_prepare("gdn_decode_fused", (ctypes.byref(f),), (f,), stream, prepare, out)
 
 

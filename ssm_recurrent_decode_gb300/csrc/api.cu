@@ -5,12 +5,13 @@
 #include <cmath>
 #include <cstring>
 
+#include "gdn_front.h"
 #include "gdn_gemv.h"
 #include "gdn_launch.h"
 
 namespace {
 
-constexpr int kAbiVersion = 5;
+constexpr int kAbiVersion = 6;
 
 bool k_supported(int K) { return K == 16 || K == 32 || K == 64 || K == 128; }
 bool dtype_ok(int d) { return d == GDN_F32 || d == GDN_BF16; }
@@ -58,6 +59,86 @@ gdn::StepLaunch make_step(const gdn_step_args *a, const int32_t *idx, int32_t pa
 }
 
 }  // namespace
+
+namespace gdn {
+
+// Host checks of gdn_decode_fused and the choice of kernel, without any CUDA launch.
+int prepare_fused(const gdn_fused_args *a, FusedPlan *plan)
+{
+    plan->empty = false;
+    plan->use_pipe = false;
+    plan->sd = false;
+    if (!a) return GDN_ERR_NULL;
+    if (a->T < 0 || a->heads < 1 || a->num_slots < 1) return GDN_ERR_SHAPE;
+    if (!k_supported(a->head_dim)) return GDN_ERR_SHAPE;
+    if ((int64_t)a->T * a->heads > INT32_MAX) return GDN_ERR_SHAPE;
+    if (a->gate_kind != GDN_FUSED_GATE_KDA && a->gate_kind != GDN_FUSED_GATE_GDN) return GDN_ERR_ARG;
+    if (a->kda_gate_form != 0 && a->kda_gate_form != 1) return GDN_ERR_ARG;
+    if (a->gate_act != GDN_ACT_SILU && a->gate_act != GDN_ACT_SIGMOID) return GDN_ERR_ARG;
+    if (a->T == 0) {
+        plan->empty = true;
+        return GDN_OK;
+    }
+    if (!a->x || !a->conv_w || !a->conv_state || !a->raw_g || !a->raw_beta || !a->A_log ||
+        !a->dt_bias || !a->state || !a->state_indices || !a->out_gate || !a->norm_w || !a->out)
+        return GDN_ERR_NULL;
+    const int64_t dim = (int64_t)a->heads * a->head_dim;
+    if (a->x_stride < 3 * dim) return GDN_ERR_SHAPE;
+    // row strides of the per-token inputs (0: dense)
+    const int64_t g_width = a->gate_kind == GDN_FUSED_GATE_KDA ? dim : a->heads;
+    const int64_t g_stride = a->raw_g_stride ? a->raw_g_stride : g_width;
+    const int64_t b_stride = a->raw_beta_stride ? a->raw_beta_stride : a->heads;
+    const int64_t og_stride = a->out_gate_stride ? a->out_gate_stride : dim;
+    if (g_stride < g_width || b_stride < a->heads || og_stride < dim) return GDN_ERR_SHAPE;
+    if (!aligned(a->x, 2) || !aligned(a->conv_state, 2) || !aligned(a->raw_g, 2) ||
+        !aligned(a->raw_beta, 2) || !aligned(a->out_gate, 2) || !aligned(a->out, 2))
+        return GDN_ERR_ALIGN;
+    if (!aligned(a->conv_w, 16) || !aligned(a->state, 16) || !aligned(a->A_log, 4) ||
+        !aligned(a->dt_bias, 4) || !aligned(a->norm_w, 4) || (a->conv_b && !aligned(a->conv_b, 4)))
+        return GDN_ERR_ALIGN;
+    if (a->kernel < GDN_KERNEL_AUTO || a->kernel > GDN_KERNEL_PIPE) return GDN_ERR_ARG;
+    gdn::FusedLaunch &p = plan->p;
+    std::memset(&p, 0, sizeof(p));
+    p.a = *a;
+    p.a.raw_g_stride = g_stride;
+    p.a.raw_beta_stride = b_stride;
+    p.a.out_gate_stride = og_stride;
+    p.scale = a->scale != 0.f ? a->scale : 1.0f / std::sqrt((float)a->head_dim);
+    // the pipelined kernel: head_dim 128, conv state in the DS ([slot][chan][tap]) or SD
+    // ([slot][tap][chan]) layout, every bulk-copied row 16-byte aligned
+    const bool ds = a->cs_stride_chan == 3 && a->cs_stride_tap == 1;
+    const bool sd = a->cs_stride_chan == 1 && a->cs_stride_tap == 3 * dim;
+    bool pipe_ok = a->head_dim == 128 && (ds || sd);
+    const bool pipe_aligned = aligned(a->x, 16) && a->x_stride % 8 == 0 && aligned(a->conv_state, 16) &&
+                              a->cs_stride_slot % 8 == 0 && aligned(a->raw_g, 16) && aligned(a->out_gate, 16) &&
+                              og_stride % 8 == 0 && (a->gate_kind != GDN_FUSED_GATE_KDA || g_stride % 8 == 0) &&
+                              aligned(a->dt_bias, 16) && aligned(a->state, 16);
+    if (pipe_ok) {
+        int dev = 0, max_smem = 0;
+        pipe_ok = cudaGetDevice(&dev) == cudaSuccess &&
+                  cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess &&
+                  gdn::fused_pipe_fits(max_smem);
+    }
+    bool use_pipe = pipe_ok && pipe_aligned;
+    if (a->kernel == GDN_KERNEL_PIPE) {
+        if (!pipe_ok) return GDN_ERR_SHAPE;
+        if (!pipe_aligned) return GDN_ERR_ALIGN;
+    } else if (a->kernel == GDN_KERNEL_TILE) {
+        use_pipe = false;
+    }
+    plan->use_pipe = use_pipe;
+    plan->sd = sd;
+    return GDN_OK;
+}
+
+int launch_fused_plan(const FusedPlan &plan, cudaStream_t stream)
+{
+    if (plan.empty) return GDN_OK;
+    if (plan.use_pipe) return launch_fused_pipe(plan.p, plan.sd, stream);
+    return launch_fused(plan.p, stream);
+}
+
+}  // namespace gdn
 
 extern "C" {
 
@@ -131,53 +212,10 @@ int gdn_decode_buffered(const gdn_step_args *args, const int32_t *cache_indices,
 
 int gdn_decode_fused(const gdn_fused_args *a, gdn_stream_t stream)
 {
-    if (!a) return GDN_ERR_NULL;
-    if (a->T < 0 || a->heads < 1 || a->num_slots < 1) return GDN_ERR_SHAPE;
-    if (!k_supported(a->head_dim)) return GDN_ERR_SHAPE;
-    if ((int64_t)a->T * a->heads > INT32_MAX) return GDN_ERR_SHAPE;
-    if (a->gate_kind != GDN_FUSED_GATE_KDA && a->gate_kind != GDN_FUSED_GATE_GDN) return GDN_ERR_ARG;
-    if (a->kda_gate_form != 0 && a->kda_gate_form != 1) return GDN_ERR_ARG;
-    if (a->gate_act != GDN_ACT_SILU && a->gate_act != GDN_ACT_SIGMOID) return GDN_ERR_ARG;
-    if (a->T == 0) return GDN_OK;
-    if (!a->x || !a->conv_w || !a->conv_state || !a->raw_g || !a->raw_beta || !a->A_log ||
-        !a->dt_bias || !a->state || !a->state_indices || !a->out_gate || !a->norm_w || !a->out)
-        return GDN_ERR_NULL;
-    const int64_t dim = (int64_t)a->heads * a->head_dim;
-    if (a->x_stride < 3 * dim) return GDN_ERR_SHAPE;
-    if (!aligned(a->x, 2) || !aligned(a->conv_state, 2) || !aligned(a->raw_g, 2) ||
-        !aligned(a->raw_beta, 2) || !aligned(a->out_gate, 2) || !aligned(a->out, 2))
-        return GDN_ERR_ALIGN;
-    if (!aligned(a->conv_w, 16) || !aligned(a->state, 16) || !aligned(a->A_log, 4) ||
-        !aligned(a->dt_bias, 4) || !aligned(a->norm_w, 4) || (a->conv_b && !aligned(a->conv_b, 4)))
-        return GDN_ERR_ALIGN;
-    if (a->kernel < GDN_KERNEL_AUTO || a->kernel > GDN_KERNEL_PIPE) return GDN_ERR_ARG;
-    gdn::FusedLaunch p;
-    std::memset(&p, 0, sizeof(p));
-    p.a = *a;
-    p.scale = a->scale != 0.f ? a->scale : 1.0f / std::sqrt((float)a->head_dim);
-    // the pipelined kernel: head_dim 128, conv state in the DS ([slot][chan][tap]) or SD
-    // ([slot][tap][chan]) layout, every bulk-copied row 16-byte aligned
-    const bool ds = a->cs_stride_chan == 3 && a->cs_stride_tap == 1;
-    const bool sd = a->cs_stride_chan == 1 && a->cs_stride_tap == 3 * dim;
-    bool pipe_ok = a->head_dim == 128 && (ds || sd);
-    const bool pipe_aligned = aligned(a->x, 16) && a->x_stride % 8 == 0 && aligned(a->conv_state, 16) &&
-                              a->cs_stride_slot % 8 == 0 && aligned(a->raw_g, 16) && aligned(a->out_gate, 16) &&
-                              aligned(a->dt_bias, 16) && aligned(a->state, 16);
-    if (pipe_ok) {
-        int dev = 0, max_smem = 0;
-        pipe_ok = cudaGetDevice(&dev) == cudaSuccess &&
-                  cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess &&
-                  gdn::fused_pipe_fits(max_smem);
-    }
-    bool use_pipe = pipe_ok && pipe_aligned;
-    if (a->kernel == GDN_KERNEL_PIPE) {
-        if (!pipe_ok) return GDN_ERR_SHAPE;
-        if (!pipe_aligned) return GDN_ERR_ALIGN;
-    } else if (a->kernel == GDN_KERNEL_TILE) {
-        use_pipe = false;
-    }
-    if (use_pipe) return gdn::launch_fused_pipe(p, sd, reinterpret_cast<cudaStream_t>(stream));
-    return gdn::launch_fused(p, reinterpret_cast<cudaStream_t>(stream));
+    gdn::FusedPlan plan;
+    const int rc = gdn::prepare_fused(a, &plan);
+    if (rc != GDN_OK) return rc;
+    return gdn::launch_fused_plan(plan, reinterpret_cast<cudaStream_t>(stream));
 }
 
 const char *gdn_strerror(int status)
@@ -202,6 +240,7 @@ size_t gdn_abi_struct_size(int which)
     case 1: return sizeof(gdn_ring_args);
     case 2: return sizeof(gdn_fused_args);
     case 3: return sizeof(gdn_gemv_args);
+    case 4: return sizeof(gdn_front_args);
     default: return 0;
     }
 }

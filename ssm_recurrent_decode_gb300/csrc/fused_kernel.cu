@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(kThreads, 2) fused_kernel(const __grid_constan
     float4 gk;
     const float A = expf(a.A_log[h]);
     if (a.gate_kind == GDN_FUSED_GATE_KDA) {
-        const size_t gi = ((size_t)t_ * heads + h) * D + t.col;
+        const size_t gi = (size_t)t_ * a.raw_g_stride + (size_t)h * D + t.col;
         const float *db = a.dt_bias + (size_t)h * D + t.col;
         float gv[4];
 #pragma unroll
@@ -86,11 +86,11 @@ __global__ void __launch_bounds__(kThreads, 2) fused_kernel(const __grid_constan
         }
         gk = make_float4(gv[0], gv[1], gv[2], gv[3]);
     } else {
-        const float gv = -A * softplus_f(bf(a.raw_g, (size_t)t_ * heads + h) + a.dt_bias[h]);
+        const float gv = -A * softplus_f(bf(a.raw_g, (size_t)t_ * a.raw_g_stride + h) + a.dt_bias[h]);
         gk = make_float4(gv, gv, gv, gv);
     }
     const float4 dec = make_float4(expf(gk.x), expf(gk.y), expf(gk.z), expf(gk.w));
-    const float beta = sigmoid_f(bf(a.raw_beta, (size_t)t_ * heads + h));
+    const float beta = sigmoid_f(bf(a.raw_beta, (size_t)t_ * a.raw_beta_stride + h));
     __syncthreads();
 
     const float4 q4 = *reinterpret_cast<const float4 *>(qkv + t.col);
@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(kThreads, 2) fused_kernel(const __grid_constan
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) tot += red[w];
     const float rs = 1.0f / sqrtf(tot / D + a.norm_eps);
-    const size_t gbase = ((size_t)t_ * heads + h) * D;
+    const size_t gbase = (size_t)t_ * a.out_gate_stride + (size_t)h * D;
     for (int r = threadIdx.x; r < D; r += kThreads) {
         const float gt = bf(a.out_gate, gbase + r);
         const float act = a.gate_act == GDN_ACT_SILU ? gt * sigmoid_f(gt) : sigmoid_f(gt);

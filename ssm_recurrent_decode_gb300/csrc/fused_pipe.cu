@@ -101,10 +101,10 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_pipe_kernel(const __grid_c
                 const int t = my_tile / heads, h = my_tile - t * heads;
                 my_slot = a.state_indices[t];
                 my_status = my_slot == a.pad_slot_id ? 1 : (my_slot < 0 || my_slot >= a.num_slots) ? 2 : 0;
-                my_beta = sigmoid_f(__bfloat162float(static_cast<const bf16 *>(a.raw_beta)[(size_t)t * heads + h]));
+                my_beta = sigmoid_f(__bfloat162float(static_cast<const bf16 *>(a.raw_beta)[(size_t)t * a.raw_beta_stride + h]));
                 my_A = expf(a.A_log[h]);
                 if (a.gate_kind == GDN_FUSED_GATE_GDN)
-                    my_g = -my_A * softplus_f(__bfloat162float(static_cast<const bf16 *>(a.raw_g)[(size_t)t * heads + h]) + a.dt_bias[h]);
+                    my_g = -my_A * softplus_f(__bfloat162float(static_cast<const bf16 *>(a.raw_g)[(size_t)t * a.raw_g_stride + h]) + a.dt_bias[h]);
             }
             for (int i = 0; i < 32; ++i) {
                 const int tile = base + i * gridDim.x;
@@ -156,9 +156,9 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_pipe_kernel(const __grid_c
                             bulk_g2s(stage + FL::cs + part * 768u, csr + ch0 * 3, 768u, &full[st]);
                         }
                     }
-                    bulk_g2s(stage + FL::og, static_cast<const bf16 *>(a.out_gate) + ((size_t)t * heads + h) * D, 256u, &full[st]);
+                    bulk_g2s(stage + FL::og, static_cast<const bf16 *>(a.out_gate) + (size_t)t * a.out_gate_stride + (size_t)h * D, 256u, &full[st]);
                     if (kda) {
-                        bulk_g2s(stage + FL::rg, static_cast<const bf16 *>(a.raw_g) + ((size_t)t * heads + h) * D, 256u, &full[st]);
+                        bulk_g2s(stage + FL::rg, static_cast<const bf16 *>(a.raw_g) + (size_t)t * a.raw_g_stride + (size_t)h * D, 256u, &full[st]);
                         bulk_g2s(stage + FL::db, a.dt_bias + (size_t)h * D, 512u, &full[st]);
                     }
                 }

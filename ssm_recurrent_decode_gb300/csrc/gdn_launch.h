@@ -30,6 +30,18 @@ struct FusedLaunch {
     float scale;
 };
 
+// A checked gdn_decode_fused call: its launch arguments and kernel choice.
+struct FusedPlan {
+    FusedLaunch p;
+    bool empty;      // T == 0: nothing to launch
+    bool use_pipe;   // the persistent pipelined kernel
+    bool sd;         // its conv state is in the SD layout
+};
+
+// The host checks of gdn_decode_fused (the same status codes) and its kernel choice; no CUDA launch.
+int prepare_fused(const gdn_fused_args *a, FusedPlan *plan);
+int launch_fused_plan(const FusedPlan &plan, cudaStream_t stream);
+
 // Host launchers, one per kernel family; each dispatches on K and the dtypes. They return
 // GDN_OK or GDN_ERR_LAUNCH / GDN_ERR_SHAPE and never synchronise.
 int launch_step(const StepLaunch &p, cudaStream_t stream);

@@ -34,6 +34,11 @@ __device__ __forceinline__ void gemv_store(const gdn_gemv_args &P, int t, int n,
         static_cast<float *>(P.y)[(size_t)t * P.y_stride + n] = v;
 }
 
+// The host checks of gdn_gemv_bf16 and its split count (*splits = 0: nothing to launch), without
+// any CUDA launch; gemv_launch then launches a checked call.
+int gemv_check(const gdn_gemv_args *a, int *splits);
+int gemv_launch(const gdn_gemv_args &p, int splits, cudaStream_t stream);
+
 // tcgen05 form: output rows per CTA (the MMA's M), inputs per stage, token rows per pass (N)
 constexpr int kTcRows = 128;
 constexpr int kTcK = 64;

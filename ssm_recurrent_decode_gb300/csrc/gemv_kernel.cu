@@ -358,6 +358,33 @@ namespace {
 bool al16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 }
 
+namespace gdn {
+
+// The host checks of gdn_gemv_bf16 (its status codes) and the split count it uses; *splits = 0
+// when there is nothing to launch. No CUDA launch.
+int gemv_check(const gdn_gemv_args *a, int *splits)
+{
+    *splits = 0;
+    if (!a) return GDN_ERR_NULL;
+    if (a->T < 0 || a->N < 0 || a->Kd < 0 || a->Kd % 8 != 0 || a->splits < 0 || a->splits > 64) return GDN_ERR_SHAPE;
+    if (a->out_dtype != GDN_F32 && a->out_dtype != GDN_BF16) return GDN_ERR_DTYPE;
+    if (a->T == 0 || a->N == 0) return GDN_OK;
+    if (!a->x || !a->W || !a->y) return GDN_ERR_NULL;
+    if (a->x_stride < a->Kd || a->x_stride % 8 != 0 || a->y_stride < a->N) return GDN_ERR_SHAPE;
+    if (!al16(a->x) || !al16(a->W) || (reinterpret_cast<uintptr_t>(a->y) % (a->out_dtype == GDN_BF16 ? 2 : 4)) != 0)
+        return GDN_ERR_ALIGN;
+    const int s = a->splits > 0 ? a->splits : (a->Kd == 0 ? 1 : gemv_default_splits(a->T, a->N, a->Kd));
+    if (gemv_reduce_mode(s) == kGemvReduceWorkspace) {
+        if (!a->workspace) return GDN_ERR_NULL;
+        if (a->workspace_bytes < gdn_gemv_workspace_bytes(a->T, a->N, s)) return GDN_ERR_SHAPE;
+        if ((reinterpret_cast<uintptr_t>(a->workspace) & 3u) != 0) return GDN_ERR_ALIGN;
+    }
+    *splits = s;
+    return GDN_OK;
+}
+
+}  // namespace gdn
+
 extern "C" {
 
 int32_t gdn_gemv_default_splits(int32_t T, int32_t N, int32_t Kd)
@@ -374,20 +401,9 @@ size_t gdn_gemv_workspace_bytes(int32_t T, int32_t N, int32_t splits)
 
 int gdn_gemv_bf16(const gdn_gemv_args *a, gdn_stream_t stream)
 {
-    if (!a) return GDN_ERR_NULL;
-    if (a->T < 0 || a->N < 0 || a->Kd < 0 || a->Kd % 8 != 0 || a->splits < 0 || a->splits > 64) return GDN_ERR_SHAPE;
-    if (a->out_dtype != GDN_F32 && a->out_dtype != GDN_BF16) return GDN_ERR_DTYPE;
-    if (a->T == 0 || a->N == 0) return GDN_OK;
-    if (!a->x || !a->W || !a->y) return GDN_ERR_NULL;
-    if (a->x_stride < a->Kd || a->x_stride % 8 != 0 || a->y_stride < a->N) return GDN_ERR_SHAPE;
-    if (!al16(a->x) || !al16(a->W) || (reinterpret_cast<uintptr_t>(a->y) % (a->out_dtype == GDN_BF16 ? 2 : 4)) != 0)
-        return GDN_ERR_ALIGN;
-    const int splits = a->splits > 0 ? a->splits : (a->Kd == 0 ? 1 : gdn::gemv_default_splits(a->T, a->N, a->Kd));
-    if (gdn::gemv_reduce_mode(splits) == gdn::kGemvReduceWorkspace) {
-        if (!a->workspace) return GDN_ERR_NULL;
-        if (a->workspace_bytes < gdn_gemv_workspace_bytes(a->T, a->N, splits)) return GDN_ERR_SHAPE;
-        if ((reinterpret_cast<uintptr_t>(a->workspace) & 3u) != 0) return GDN_ERR_ALIGN;
-    }
+    int splits = 0;
+    const int rc = gdn::gemv_check(a, &splits);
+    if (rc != GDN_OK || splits == 0) return rc;
     return gdn::gemv_launch(*a, splits, reinterpret_cast<cudaStream_t>(stream));
 }
 

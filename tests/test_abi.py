@@ -175,3 +175,30 @@ def test_binding_refuses_cpu_tensors():
         gdn.gdn_decode_step(q, k, v, torch.zeros((2, 4, 16, 16)), torch.zeros((2, 4, 16)), H=2,
                             a=torch.zeros(2, 4), b=torch.zeros(2, 4), A_log=torch.zeros(4),
                             dt_bias=torch.zeros(4))
+
+
+def test_front_checks():
+    """gdn_decode_front rejects bad arguments before launching anything."""
+    L = gdn.lib()
+    assert L.gdn_abi_struct_size(4) == ctypes.sizeof(gdn.GdnFrontArgs)
+    assert L.gdn_front_proj_width(32, 128, gdn.GDN_FUSED_GATE_GDN) == 4 * 4096 + 64
+    assert L.gdn_front_proj_width(16, 128, gdn.GDN_FUSED_GATE_KDA) == 5 * 2048 + 16
+    assert L.gdn_front_proj_width(16, 128, 7) == 0
+    assert L.gdn_decode_front(None, None) == -1
+    a = gdn.GdnFrontArgs()
+    a.T, a.hidden = 2, 5120
+    a.core.heads, a.core.head_dim, a.core.num_slots = 32, 128, 4
+    a.core.gate_kind = gdn.GDN_FUSED_GATE_GDN
+    assert L.gdn_decode_front(ctypes.byref(a), None) == -1            # no z / o
+    a.z, a.o = 1 << 40, (1 << 40) + 8
+    assert L.gdn_decode_front(ctypes.byref(a), None) == -4            # o not 16-byte aligned
+    a.o = 1 << 41
+    assert L.gdn_decode_front(ctypes.byref(a), None) == -1            # no x, W, y (projection)
+    a.in_splits = 9
+    assert L.gdn_decode_front(ctypes.byref(a), None) == -6            # more ranges than a cluster
+    a.in_splits, a.hidden = 0, 5121
+    assert L.gdn_decode_front(ctypes.byref(a), None) == -2
+    a.hidden, a.core.gate_kind = 5120, 5
+    assert L.gdn_decode_front(ctypes.byref(a), None) == -6
+    a.core.gate_kind, a.T = gdn.GDN_FUSED_GATE_GDN, 0
+    assert L.gdn_decode_front(ctypes.byref(a), None) == 0             # nothing to do

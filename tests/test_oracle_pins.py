@@ -617,6 +617,48 @@ def test_gemv():
     check_gemv()
 
 
+# --------------------------------------------------------------------------------------------
+# decode layer front (projection -> fused decode -> projection)
+# --------------------------------------------------------------------------------------------
+def check_decode_front_selects_columns():
+    """With an identity input projection (x carries z itself) and an output projection that copies
+    the first dim columns, the front is the fused decode on z's column blocks, its output rounded
+    to bf16: exactly, for both gate kinds. Each block holds different random values, so a block
+    read from the wrong columns fails."""
+    T, heads, D = 3, 2, 16
+    dim = heads * D
+    f = lambda bits: syn.bf16_bits_to_f32(bits).astype(np.float64)
+    for kind in ("gdn", "kda"):
+        ins = syn.fused_inputs(T, heads, D, T + 2, seed=61)
+        raw_g = f(ins["raw_g"]) if kind == "kda" else f(ins["raw_g"])[:, :, 0]
+        dt_bias = ins["dt_bias"] if kind == "kda" else ins["dt_bias"][:heads]
+        z = np.concatenate([f(ins["x"]), f(ins["out_gate"]).reshape(T, dim), raw_g.reshape(T, -1),
+                            f(ins["raw_beta"]).reshape(T, heads)], axis=1)
+        P = z.shape[1]
+        col = oracle.front_columns(heads, D, kind)
+        assert col["raw_beta"][1] == P
+        W_out = np.zeros((P, dim))
+        W_out[np.arange(dim), np.arange(dim)] = 1.0
+        idx = np.array([2, 0, 1], dtype=np.int32)          # row 1 is the pad (slot 0) row
+        st = syn.normal_f32(61, syn.Tag.STATE, 0, (T + 2, heads, D, D), 1.0).astype(np.float64)
+        cs = f(ins["conv_state"]).reshape(T + 2, 3 * dim, 3)
+        s1, c1, s2, c2 = st.copy(), cs.copy(), st.copy(), cs.copy()
+        y, _ = oracle.decode_front(z, np.eye(P), W_out, ins["conv_w"], c1, ins["A_log"], dt_bias,
+                                   s1, ins["norm_w"], heads=heads, D=D, idx=idx, pad_slot=0,
+                                   gate_kind=kind)
+        o, _ = oracle.fused_kda(f(ins["x"]), ins["conv_w"], c2, raw_g, f(ins["raw_beta"]),
+                                ins["A_log"], dt_bias, s2, f(ins["out_gate"]), ins["norm_w"],
+                                idx=idx, pad_slot=0, gate_kind=kind)
+        np.testing.assert_array_equal(y[:, :dim], oracle.round_bf16(o.reshape(T, dim)))
+        np.testing.assert_array_equal(y[:, dim:], 0.0)
+        np.testing.assert_array_equal(s1, s2)
+        np.testing.assert_array_equal(c1, c2)
+
+
+def test_decode_front_selects_columns():
+    check_decode_front_selects_columns()
+
+
 ALL_CHECKS = [
     check_hand_worked_step, check_invariant_no_decay_no_write, check_invariant_exact_recall,
     check_invariant_full_decay, check_closed_matrix_form, check_gqa_duplication,
@@ -625,4 +667,5 @@ ALL_CHECKS = [
     check_conv_update_is_causal_convolution, check_gated_rmsnorm, check_bf16_rounding,
     check_fused_per_key_gate_reduces_to_scalar, check_bf16_state_storage,
     check_mamba_constant_input_geometric_series, check_mamba_output_and_gates, check_gemv,
+    check_decode_front_selects_columns,
 ]
