@@ -612,7 +612,7 @@ def run_fused(args):
     calls = [gdn.gdn_decode_fused(w["x"], w["conv_w"], w["conv_state"], w["raw_g"], w["raw_beta"],
                                   w["A_log"], w["dt_bias"], pool, w["idx"], w["out_gate"],
                                   w["norm_w"], w["out"], pad_slot_id=0, gate_kind="kda",
-                                  kda_gate_form=0, gate_act="silu", prepare=True)
+                                  kda_gate_form=0, gate_act="silu", kernel=args.kernel, prepare=True)
              for pool in pools]
 
     def step(i):
@@ -637,7 +637,7 @@ def run_fused(args):
         f"fused KDA decode: T={T} tokens, {heads} heads x {D}, conv width 4 ({args.layout} conv "
         f"state), per-key decay bounded at -5, gated RMSNorm with silu",
         {"T": T, "heads": heads, "head_dim": D, "state_bytes_per_step": state_bytes,
-         "state_pools": n_pools,
+         "state_pools": n_pools, "kernel": args.kernel,
          "l2": f"{n_pools} state pool(s) rotated, at least 4x the L2 size per pass",
          "timing": f"CUDA-graph replays of {per_graph} calls"}, steps)
     line["roofline"] = roofline(state_bytes + io, ms, "fused", f"fused_T{T}")
@@ -907,7 +907,8 @@ def run_front(args):
         syn.fill_normal_(st, seed, syn.Tag.STATE, 0, 1.0, layer=p)
         layers.append((W_in, W_out, st))
     calls = [gdn.gdn_decode_front(x, W_in, W_out, z, o, y, conv_w, conv_state, A_log, dt_bias, st,
-                                  idx, norm_w, pad_slot_id=0, gate_kind="gdn", prepare=True)
+                                  idx, norm_w, pad_slot_id=0, gate_kind="gdn", kernel=args.kernel,
+                                  prepare=True)
              for W_in, W_out, st in layers]
     in_splits = gdn.lib().gdn_gemv_default_splits(T, P, hidden)
     out_splits = gdn.lib().gdn_gemv_default_splits(T, hidden, dim)
@@ -955,6 +956,8 @@ def main(argv=None):
     p.add_argument("--L", type=int, default=16)
     p.add_argument("--T", type=int, default=128)
     p.add_argument("--layout", choices=["DS", "SD"], default="DS")
+    p.add_argument("--kernel", choices=["auto", "tile", "pipe"], default="auto",
+                   help="fused conv/step/norm kernel of the fused and front workloads")
     p.add_argument("--state-dtype", choices=["f32", "bf16"], default="f32")
     p.add_argument("--D", type=int, default=1536)
     p.add_argument("--hidden", type=int, default=5120, help="model width of the front workload")

@@ -113,16 +113,23 @@ int prepare_fused(const gdn_fused_args *a, FusedPlan *plan)
                               a->cs_stride_slot % 8 == 0 && aligned(a->raw_g, 16) && aligned(a->out_gate, 16) &&
                               og_stride % 8 == 0 && (a->gate_kind != GDN_FUSED_GATE_KDA || g_stride % 8 == 0) &&
                               aligned(a->dt_bias, 16) && aligned(a->state, 16);
+    int sms = 0;
     if (pipe_ok) {
         int dev = 0, max_smem = 0;
         pipe_ok = cudaGetDevice(&dev) == cudaSuccess &&
                   cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess &&
-                  gdn::fused_pipe_fits(max_smem);
+                  gdn::fused_pipe_fits(max_smem) &&
+                  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess;
     }
-    bool use_pipe = pipe_ok && pipe_aligned;
+    // With at most two tiles per SM the persistent kernel's pipeline never fills and the per-tile
+    // kernel was faster on GB300 (6.6 against 7.3 us for 96 tiles, 8.7 against 9.8 for 192); from
+    // four tiles per SM the pipelined kernel wins.
+    const bool few_tiles = (int64_t)a->T * a->heads <= 2 * (int64_t)sms;
+    bool use_pipe = pipe_ok && pipe_aligned && !few_tiles;
     if (a->kernel == GDN_KERNEL_PIPE) {
         if (!pipe_ok) return GDN_ERR_SHAPE;
         if (!pipe_aligned) return GDN_ERR_ALIGN;
+        use_pipe = true;
     } else if (a->kernel == GDN_KERNEL_TILE) {
         use_pipe = false;
     }

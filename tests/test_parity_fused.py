@@ -91,9 +91,10 @@ def _run_fused(T, heads, D, *, layout="DS", gate_kind="kda", form=0, act="silu",
 
 @pytest.mark.parametrize("kernel", ["tile", "pipe"])
 @pytest.mark.parametrize("layout", ["DS", "SD"])
-@pytest.mark.parametrize("T", [1, 8])
+@pytest.mark.parametrize("T", [1, 2, 4, 8])
 def test_kda_config_shapes(layout, T, kernel):
-    """The fused KDA decode shapes: 96 heads x 128, conv width 4, lower bound -5, silu gate."""
+    """The fused KDA decode shapes: 96 heads x 128, conv width 4, lower bound -5, silu gate. The
+    per-tile kernel splits each tile over a cluster of 8, 4, 2 and 1 CTAs at T = 1, 2, 4, 8."""
     w = _run_fused(T, 96, 128, layout=layout, seed=T, kernel=kernel)
     assert w["out"] <= 2e-2 and w["state"] <= 1e-5, w
 
@@ -114,13 +115,14 @@ def test_gate_readings_and_activations(form, act):
     assert w["out"] <= 2e-2 and w["state"] <= 1e-5, w
 
 
-@pytest.mark.parametrize("D", [16, 32, 128])
-def test_gdn_gate_and_small_heads(D):
-    w = _run_fused(5, 4, D, gate_kind="gdn", seed=D, steps=2, layout="SD")
+@pytest.mark.parametrize("D,kernel", [(16, "auto"), (32, "auto"), (128, "auto"), (128, "tile")])
+def test_gdn_gate_and_small_heads(D, kernel):
+    """At head_dim 128 the per-tile kernel splits these 20 tiles over clusters of 8 CTAs."""
+    w = _run_fused(5, 4, D, gate_kind="gdn", seed=D, steps=2, layout="SD", kernel=kernel)
     assert w["out"] <= 2e-2 and w["state"] <= 1e-5, w
 
 
-@pytest.mark.parametrize("D,kernel", [(64, "auto"), (128, "pipe")])
+@pytest.mark.parametrize("D,kernel", [(64, "auto"), (128, "pipe"), (128, "tile")])
 def test_null_slot_rows_are_skipped(D, kernel):
     w = _run_fused(6, 4, D, seed=9, pad_rows=(0, 4), steps=2, kernel=kernel)
     assert w["out"] <= 2e-2 and w["state"] <= 1e-5, w
