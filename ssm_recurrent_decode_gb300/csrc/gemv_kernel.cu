@@ -206,7 +206,7 @@ static int sm_count_gemv()
 // 28.2 us for W [17408, 5120]).
 constexpr int kTcMinTokens = 2;
 enum class Form { kCore, kTc };
-constexpr int kTcStages = 4;   // shared-memory stages of the tcgen05 form (18 KB each)
+constexpr int kTcStages = 2;   // shared-memory stages of the tcgen05 form (36 KB each)
 
 static Form form_for(int T) { return T < kTcMinTokens ? Form::kCore : Form::kTc; }
 
@@ -225,7 +225,7 @@ static GemvPlan make_plan(int T, int N, int Kd, int splits)
     pl.form = form_for(T);
     int rows, gran;
     if (pl.form == Form::kCore) pl.per_pass = 1, rows = kGemvWarps * kRows, gran = 256;
-    else pl.per_pass = kTcTok, rows = kTcRows, gran = kTcK;
+    else pl.per_pass = kTcTok, rows = kTcRows, gran = kTcStageK;
     pl.ctas_n = (N + rows - 1) / rows;
     const int chunks = (Kd + gran - 1) / gran;
     pl.k_per_split = ((chunks + splits - 1) / splits) * gran;

@@ -2,15 +2,16 @@
 // to 16 token rows.
 //
 // One CTA owns 128 output rows (the MMA's M) and one K range. The range streams through a ring of
-// shared-memory stages, each filled by two TMA tile copies (cp.async.bulk.tensor, 128-byte
-// swizzle): 128 weight rows x 64 inputs (16 KB) and 16 token rows x 64 inputs of x (2 KB; rows
-// past T and inputs past Kd are zero-filled by the copy). One thread issues tcgen05.mma
-// (kind::f16: bf16 operands, fp32 accumulation; M = 128, N = 16, K = 16, four per stage) into one
-// of two 128-lane x 16-column fp32 accumulators in tensor memory, one buffer per group of two
-// stages (128 inputs); tcgen05.commit returns a stage to the producer once the MMAs reading it are
-// done and hands a finished group to the epilogue. Four epilogue warps read each group's sum
-// (tcgen05.ld, one output row per thread, 16 token columns), add it to fp32 registers while the
-// next group accumulates in the other buffer, and finally write y or the split-K partial sums.
+// shared-memory stages (kTcStages x kTcChunks tiles, see gemv_internal.h), each tile filled by two
+// TMA copies (cp.async.bulk.tensor, 128-byte swizzle): 128 weight rows x 64 inputs (16 KB) and 16
+// token rows x 64 inputs of x (2 KB; rows past T and inputs past Kd are zero-filled by the copy).
+// The tiles of a stage are adjacent in K, so a stage reads 256 contiguous bytes of every weight
+// row. One thread issues tcgen05.mma (kind::f16: bf16 operands, fp32 accumulation; M = 128,
+// N = 16, K = 16, four per tile) into one of two 128-lane x 16-column fp32 accumulators in tensor
+// memory, one buffer per 128 inputs; tcgen05.commit returns a stage to the producer once the MMAs
+// reading it are done and hands a finished group to the epilogue. Four epilogue warps read each
+// group's sum (tcgen05.ld, one output row per thread, 16 token columns), add it to fp32 registers
+// while the next group accumulates in the other buffer, and finally write y or the partial sums.
 // Adding the groups with round-to-nearest fp32 adds keeps a long K range as accurate as a plain
 // fp32 sum; a single tensor-memory accumulation over 2560 inputs measured 2.1e-5 relative error.
 //
@@ -37,10 +38,10 @@ namespace gdn {
 
 constexpr int kTcEpiThreads = 128;                         // warps 2 .. 5
 constexpr int kTcThreads = 64 + kTcEpiThreads;              // producer warp, MMA warp, epilogue
-constexpr int kTcGroupStages = 2;                           // stages summed per accumulator buffer
+constexpr int kTcGroupStages = kTcChunks >= 2 ? 1 : 2;      // stages summed per accumulator buffer
 constexpr uint32_t kTcABytes = kTcRows * kTcK * 2;          // weight tile, 16 KB
 constexpr uint32_t kTcBBytes = kTcTok * kTcK * 2;           // token tile, 2 KB
-constexpr uint32_t kTcStageBytes = kTcABytes + kTcBBytes;   // a multiple of 1024
+constexpr uint32_t kTcStageBytes = kTcChunks * (kTcABytes + kTcBBytes);   // a multiple of 1024
 constexpr uint32_t kTcTmemCols = 32;                        // two 16-column accumulators
 constexpr long long kTcWaitLimit = 1LL << 31;               // SM clock cycles, about one second
 
@@ -136,7 +137,7 @@ __global__ void __launch_bounds__(kTcThreads) gemv_tc_kernel(const __grid_consta
     const int n0 = blockIdx.x * kTcRows;
     const int k_begin = split * k_per_split;
     const int k_end = min(P.Kd, k_begin + k_per_split);
-    const int nk = k_end > k_begin ? (k_end - k_begin + kTcK - 1) / kTcK : 0;
+    const int nk = k_end > k_begin ? (k_end - k_begin + kTcStageK - 1) / kTcStageK : 0;
     const int ngroups = (nk + kTcGroupStages - 1) / kTcGroupStages;
 
     if (threadIdx.x == 0) {
@@ -180,8 +181,12 @@ __global__ void __launch_bounds__(kTcThreads) gemv_tc_kernel(const __grid_consta
                 }
                 const uint32_t a = sbase + (uint32_t)s * kTcStageBytes;
                 mbar_arrive_expect_tx(&full[s], kTcStageBytes);
-                tma_tile_2d_hint(a, &wmap, k_begin + it * kTcK, n0, &full[s], pol);
-                tma_tile_2d(a + kTcABytes, &xmap, k_begin + it * kTcK, t0, &full[s]);
+#pragma unroll
+                for (int c = 0; c < kTcChunks; ++c) {   // adjacent 64-input tiles of the same rows
+                    const int k = k_begin + it * kTcStageK + c * kTcK;
+                    tma_tile_2d_hint(a + c * kTcABytes, &wmap, k, n0, &full[s], pol);
+                    tma_tile_2d(a + kTcChunks * kTcABytes + c * kTcBBytes, &xmap, k, t0, &full[s]);
+                }
             }
             if (*(volatile int *)&abort_flag) {
                 // let the copies of the stages still in flight land before the CTA exits
@@ -215,11 +220,16 @@ __global__ void __launch_bounds__(kTcThreads) gemv_tc_kernel(const __grid_consta
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a = sbase + (uint32_t)s * kTcStageBytes, b = a + kTcABytes;
+                    const uint32_t a0 = sbase + (uint32_t)s * kTcStageBytes, b0 = a0 + kTcChunks * kTcABytes;
                     const bool first = it == g * kTcGroupStages;
 #pragma unroll
-                    for (int j = 0; j < kTcK / 16; ++j)
-                        tc_mma(d, sw128_desc(a + 32u * j), sw128_desc(b + 32u * j), (first && j == 0) ? 0u : 1u);
+                    for (int c = 0; c < kTcChunks; ++c) {
+                        const uint32_t a = a0 + c * kTcABytes, b = b0 + c * kTcBBytes;
+#pragma unroll
+                        for (int j = 0; j < kTcK / 16; ++j)
+                            tc_mma(d, sw128_desc(a + 32u * j), sw128_desc(b + 32u * j),
+                                   (first && c == 0 && j == 0) ? 0u : 1u);
+                    }
                     tc_commit(&empty[s]);
                 }
                 if (ok) tc_commit(&acc_full[buf]);
@@ -368,7 +378,7 @@ size_t gemv_tc_smem_bytes(int stages) { return (size_t)stages * kTcStageBytes + 
 // Resident CTAs per SM, from the shared-memory bound (each CTA holds its stages plus 1 KB of
 // alignment slack, 1 KB is reserved per CTA; registers and threads allow more). The occupancy
 // query reported one CTA per SM for this kernel on GB300, while timings over split counts follow
-// the shared-memory bound (three CTAs at four stages).
+// the shared-memory bound (three CTAs at two stages of two tiles).
 int gemv_tc_resident_ctas(int stages)
 {
     static std::mutex lock;
@@ -395,7 +405,7 @@ int gemv_tc_resident_ctas(int stages)
 
 int gemv_tc_launch(const gdn_gemv_args &p, int splits, int k_per_split, int stages, cudaStream_t stream)
 {
-    if (stages < 2 || stages > kTcMaxStages || k_per_split % kTcK != 0) return GDN_ERR_ARG;
+    if (stages < 2 || stages > kTcMaxStages || k_per_split % kTcStageK != 0) return GDN_ERR_ARG;
     CUtensorMap wmap, xmap;
     if (!encode_bf16_tiles(&wmap, p.W, p.N, p.Kd, p.Kd, kTcRows) ||
         !encode_bf16_tiles(&xmap, p.x, p.T, p.Kd, p.x_stride, kTcTok))
