@@ -476,16 +476,67 @@ def fused_recurrent_gated_delta_rule_packed_decode(mixed_qkv, a, b, A_log, dt_bi
     [num_slots, HV, V, K] fp32 (updated in place), out [B, 1, HV, V], ssm_state_indices int32 [B].
     H is recovered from the row width."""
     _, HV, V, K = initial_state.shape
-    width = mixed_qkv.shape[1]
-    if (width - HV * V) <= 0 or (width - HV * V) % (2 * K):
-        raise ValueError("mixed_qkv width does not match 2*H*K + HV*V")
-    H = (width - HV * V) // (2 * K)
+    H = _heads_from_width(mixed_qkv, HV, V, K)
     q, k, v = split_mixed_qkv(mixed_qkv, H, HV, K, V)
     return gdn_decode_step_indexed(q, k, v, initial_state, out, ssm_state_indices,
                                    pad_slot_id=pad_slot_id, H=H, a=a, b=b, A_log=A_log,
                                    dt_bias=dt_bias, scale=scale,
                                    use_qk_l2norm=use_qk_l2norm_in_kernel, err_flags=err_flags,
                                    stream=stream)
+
+
+def _heads_from_width(mixed_qkv, HV, V, K):
+    width = mixed_qkv.shape[1]
+    if (width - HV * V) <= 0 or (width - HV * V) % (2 * K):
+        raise ValueError("mixed_qkv width does not match 2*H*K + HV*V")
+    return (width - HV * V) // (2 * K)
+
+
+def fused_recurrent_gdn_replayssm_decode(mixed_qkv, a, b, A_log, dt_bias, scale, initial_state,
+                                         d_cache, k_cache, g_cache, out, ssm_state_indices,
+                                         write_pos, use_qk_l2norm_in_kernel=True, nk=2,
+                                         pad_slot_id=-1, err_flags=None, stream=None):
+    """The buffered output-only decode with the keyword names of the sglang microbenchmark's
+    run_replay: initial_state [num_slots, HV, V, K] fp32 holds the checkpoints; d_cache
+    [num_slots, HV, L, V], k_cache [num_slots, H, L, K], g_cache [num_slots, HV, L]; write_pos
+    int32 [B] is read, not advanced. nk (the number of key chunks that page's kernel walks while
+    replaying its ring) is accepted and has no effect: this library's replay is low-rank and
+    never re-forms the state outside the flush step."""
+    del nk
+    _, HV, V, K = initial_state.shape
+    H = _heads_from_width(mixed_qkv, HV, V, K)
+    q, k, v = split_mixed_qkv(mixed_qkv, H, HV, K, V)
+    return gdn_decode_buffered(q, k, v, initial_state, out, d_cache, k_cache, g_cache, write_pos,
+                               cache_indices=ssm_state_indices, pad_slot_id=pad_slot_id, H=H, a=a,
+                               b=b, A_log=A_log, dt_bias=dt_bias, scale=scale,
+                               use_qk_l2norm=use_qk_l2norm_in_kernel, err_flags=err_flags,
+                               stream=stream)
+
+
+def conv_weight_from_stacked(weight):
+    """Converts conv weights stacked per q/k/v part as [3, width, dim] (the layout the KDA
+    microbenchmark passes to its fused op) to this library's [3*dim, width], channel-major. A
+    one-time parameter conversion, not part of the decode step."""
+    parts, width, dim = weight.shape
+    return weight.permute(0, 2, 1).reshape(parts * dim, width).contiguous()
+
+
+def fused_kda_decode(x, weight, bias, conv_state, raw_g, raw_beta, A_log, dt_bias, state_indices,
+                     state, out, lower_bound, output_gate, norm_weight, norm_eps, *,
+                     pad_slot_id=0, gate_act="silu", err_flags=None, stream=None):
+    """The fused KDA decode with the keyword names of the KDA microbenchmark's `fused` call: x
+    [T, 3*dim], weight [3*dim, 4] (conv_weight_from_stacked converts the stacked layout), bias or
+    None, conv_state logical [num_slots, 3*dim, 3] (DS tensor or SD transposed view), raw_g
+    [1, T, heads, D] or [T, heads, D], raw_beta [1, T, heads] or [T, heads], state [num_slots,
+    heads, D, D], out [1, T, heads, D] or [T, heads, D], output_gate [T, heads, D], norm_weight
+    [D] fp32. Slot 0 is the NULL (pad) slot, as on that page."""
+    T = x.shape[0]
+    heads, D = state.shape[1], state.shape[2]
+    return gdn_decode_fused(x, weight, conv_state, raw_g.view(T, heads, D), raw_beta.view(T, heads),
+                            A_log, dt_bias, state, state_indices, output_gate, norm_weight,
+                            out.view(T, heads, D), conv_b=bias, pad_slot_id=pad_slot_id,
+                            gate_kind="kda", lower_bound=lower_bound, norm_eps=norm_eps,
+                            gate_act=gate_act, err_flags=err_flags, stream=stream)
 
 
 def mamba_selective_scan_decode(x, dt, A, Bm, Cm, h, y, *, Dskip=None, z=None, h_out=None,
