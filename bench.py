@@ -24,6 +24,7 @@ import datetime as _dt
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -58,10 +59,16 @@ def hbm_peak():
 
 
 def kernel_sources_hash(files) -> str:
+    """Hash of the kernel sources with comments and blank lines removed, so that a comment edit
+    does not orphan a traffic record taken on the same code."""
     h = hashlib.sha256()
     for rel in files:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        lines = [ln.rstrip() for ln in text.splitlines() if ln.strip()]
+        h.update("\n".join(lines).encode())
     return h.hexdigest()[:16]
 
 

@@ -4,11 +4,13 @@
 // The state is fp32, or bf16 when it is stored in bf16 (8-byte accesses of four values, fp32
 // arithmetic, the updated tile rounded to nearest even as it is stored).
 //
-// Grid: one CTA per (row b, value head hv), blockIdx.x = b * HV + hv, so the G value heads that
-// share a q/k head sit next to each other and find its q/k in L2. Each CTA streams its 64 KB
-// (K = V = 128) fp32 tile in with 16-byte loads, takes S.(Dk) and S.(Dq) from registers, and
-// writes S' back with 16-byte streaming stores: one HBM read and one HBM write of the state,
-// which is the whole roofline of this memory-bound matrix-vector step.
+// Grid: 1, 2, 4 or 8 CTAs per (row b, value head hv) tile, tiles ordered b * HV + hv, so the G
+// value heads that share a q/k head sit next to each other and find its q/k in L2. At K = 128
+// with an fp32 state a tile is two CTAs of 64 rows each (8 rows per thread, four CTAs per SM),
+// the fastest split on GB300 at every batch size; small batches split further. Each CTA streams
+// its rows in with 16-byte loads, takes S.(Dk) and S.(Dq) from registers, and writes S' back with
+// 16-byte streaming stores: one HBM read and one HBM write of the state, which is the whole
+// roofline of this memory-bound matrix-vector step.
 //
 // Sources: "Optimization Log: Qwen3.5-27B Dense on B200", "Kernel 4: Fused DeltaNet Recurrent
 // (FLAGSHIP)" (the Math block); "Microbenchmark: buffered output-only GDN decode (ReplaySSM Part
@@ -20,9 +22,9 @@
 
 namespace gdn {
 
-// R rows per warp: R = 16 for the bulk of the work (a CTA owns a whole tile, looping over row
-// passes when V is larger than 128); R = 8, 4 or 2 split a tile's rows over `splits` CTAs for small
-// batches, which have too few tiles to fill the GPU. Row dots are complete within a row, so the
+// R rows per warp: R = 16 lets a CTA own a whole tile (looping over row passes when V is larger
+// than 128); R = 8, 4 or 2 split a tile's rows over `splits` CTAs (R = 8 at K = 128 with an fp32
+// state, and smaller R for batches with too few tiles to fill the GPU). Row dots are complete within a row, so the
 // split needs no exchange between CTAs; each CTA normalises q and k itself.
 template <int K, typename Tin, typename TS, int R>
 __global__ void __launch_bounds__(kThreads, R >= 16 ? 2 : 4) step_kernel(const __grid_constant__ StepLaunch P, int splits)
