@@ -1,0 +1,31 @@
+"""CPU checks of bench.py's bookkeeping: the kernel-source hash that keys the committed ncu traffic
+records ignores comments but not code, every traffic record names a workload kernel family, and
+the host CPU description is a non-empty string."""
+import json
+import os
+
+import bench
+
+
+def test_source_hash_ignores_comments_but_not_code(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    (tmp_path / "k.cu").write_text("// header\nint f(int x) { return x + 1; }  // inc\n/* block\n */\n")
+    h0 = bench.kernel_sources_hash(["k.cu"])
+    (tmp_path / "k.cu").write_text("// a different header\n\nint f(int x) { return x + 1; }\n")
+    assert bench.kernel_sources_hash(["k.cu"]) == h0
+    (tmp_path / "k.cu").write_text("int f(int x) { return x + 2; }\n")
+    assert bench.kernel_sources_hash(["k.cu"]) != h0
+
+
+def test_traffic_records_are_well_formed():
+    path = os.path.join(os.path.dirname(bench.__file__), "profiles", "traffic.json")
+    records = json.load(open(path))
+    assert "packed_B256" in records
+    for key, rec in records.items():
+        assert rec["dram_bytes_per_launch"] > 0, key
+        assert len(rec["sources_hash"]) == 16, key
+        assert rec.get("command", "").lstrip().startswith("ncu ") or "phases" in rec, key
+
+
+def test_cpu_model_is_described():
+    assert isinstance(bench.cpu_model(), str) and bench.cpu_model()

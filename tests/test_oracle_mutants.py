@@ -78,3 +78,25 @@ def test_pins_catch_mutant(name, old, new, tmp_path):
             except (ValueError, FloatingPointError):
                 failed.append(check.__name__)
     assert failed, f"no pin caught the mutant '{name}'"
+
+
+# The front's composition lives in oracle/__init__.py (Python). Its mutants, like the C ones, are
+# copies of the function's source with one deliberate error, run in the oracle module's namespace.
+FRONT_MUTANTS = [
+    ("front raw_g from the gate columns", oracle.front_columns,
+     '"raw_g": (4 * dim, 4 * dim + G)', '"raw_g": (3 * dim, 3 * dim + G)'),
+    ("front o not rounded", oracle.decode_front,
+     "o = round_bf16(o.reshape(T, heads * D))", "o = o.reshape(T, heads * D)"),
+]
+
+
+@pytest.mark.parametrize("name,fn,old,new", FRONT_MUTANTS, ids=[m[0] for m in FRONT_MUTANTS])
+def test_front_pin_catches_mutant(name, fn, old, new, monkeypatch):
+    import inspect
+    src = inspect.getsource(fn)
+    assert src.count(old) == 1, f"mutation site for '{name}' not found exactly once"
+    ns = dict(vars(oracle))
+    exec(compile(src.replace(old, new), f"<mutant {name}>", "exec"), ns)
+    monkeypatch.setattr(oracle, fn.__name__, ns[fn.__name__])
+    with pytest.raises(AssertionError):
+        pins.check_decode_front_selects_columns()
