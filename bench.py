@@ -590,7 +590,8 @@ def run_buffered(args):
     pos = [torch.full((B,), p, dtype=torch.int32, device=h.dev) for p in range(L)]
     calls = [gdn.gdn_decode_buffered(q, k, v, w["state"], w["out"], d_cache, k_cache, g_cache, pos[p],
                                      cache_indices=w["idx"], H=H, a=w["a"], b=w["b"],
-                                     A_log=w["A_log"], dt_bias=w["dt_bias"], prepare=True)
+                                     A_log=w["A_log"], dt_bias=w["dt_bias"], kernel=args.kernel,
+                                     prepare=True)
              for p in range(L)]
 
     def step(i):
@@ -1021,7 +1022,7 @@ def main(argv=None):
     p.add_argument("--T", type=int, default=128)
     p.add_argument("--layout", choices=["DS", "SD"], default="DS")
     p.add_argument("--kernel", choices=["auto", "tile", "pipe"], default="auto",
-                   help="fused conv/step/norm kernel of the fused and front workloads")
+                   help="kernel family of the buffered, fused and front workloads")
     p.add_argument("--state-dtype", choices=["f32", "bf16"], default="f32")
     p.add_argument("--D", type=int, default=1536)
     p.add_argument("--hidden", type=int, default=5120, help="model width of the front workload")

@@ -114,8 +114,8 @@ typedef struct gdn_ring_args {
     void *k_cache;            /* [num_slots, H, L, K] normalised-key records */
     float *g_cache;           /* [num_slots, HV, L] log-decay records */
     const int32_t *write_pos; /* [B] cursor of each row, 0 <= write_pos[b] < L; read only */
-    int32_t kernel;           /* GDN_KERNEL_AUTO (0): the pipelined kernel when it applies, else the
-                                 per-tile kernel; GDN_KERNEL_TILE (1) / GDN_KERNEL_PIPE (2) force one
+    int32_t kernel;           /* GDN_KERNEL_AUTO (0): the pipelined kernel when it applies and L > 1,
+                                 else the per-tile kernel; GDN_KERNEL_TILE (1) / GDN_KERNEL_PIPE (2) force one
                                  (PIPE needs K == V == 128, L == 1 or a multiple of 4, and 16-byte
                                  aligned rows and rings: GDN_ERR_SHAPE or GDN_ERR_ALIGN otherwise) */
 } gdn_ring_args;

@@ -325,8 +325,8 @@ def gdn_decode_buffered(q, k, v, state, out, d_cache, k_cache, g_cache, write_po
     """Buffered output-only decode. state holds the checkpoints; d_cache [num_slots, HV, L, V],
     k_cache [num_slots, H, L, K] (both fp32 or both bf16), g_cache [num_slots, HV, L] fp32;
     write_pos int32 [B] is read, never advanced (the caller moves it to (p+1) % L).
-    kernel: "auto" (the persistent pipelined kernel when K == V == 128 and rows are 16-byte
-    aligned, else the per-tile kernel), "tile" or "pipe" to force one."""
+    kernel: "auto" (the persistent pipelined kernel when K == V == 128, rows are 16-byte aligned
+    and L > 1, else the per-tile kernel), "tile" or "pipe" to force one."""
     torch = _torch()
     s = _step_args(q, k, v, state, out, H=H, a=a, b=b, A_log=A_log, dt_bias=dt_bias, g=g,
                    beta=beta, scale=scale, use_qk_l2norm=use_qk_l2norm, err_flags=err_flags)

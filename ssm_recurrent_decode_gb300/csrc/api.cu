@@ -204,7 +204,9 @@ int gdn_decode_buffered(const gdn_step_args *args, const int32_t *cache_indices,
         if (!tile_ok) return GDN_ERR_SHAPE;
         use_pipe = false;
     } else {
-        use_pipe = pipe_ok && pipe_aligned;
+        // At L = 1 every step flushes and the per-tile kernel was faster on GB300 (170.4 against
+        // 174.4 us at B = 256); from L = 8 the pipelined kernel is far ahead (96 against 147 us).
+        use_pipe = pipe_ok && pipe_aligned && !(ring->L == 1 && tile_ok);
         if (!use_pipe && !tile_ok) return GDN_ERR_SHAPE;
     }
     gdn::StepLaunch p = make_step(args, cache_indices, pad_slot_id);

@@ -89,8 +89,8 @@ def test_exact_ring_shapes_mixed_phases(K, G, kernel):
     assert max(w.values()) <= 1e-5, w
 
 
-@pytest.mark.parametrize("kernel", ["tile", "pipe"])
-@pytest.mark.parametrize("L", [8, 16])
+@pytest.mark.parametrize("kernel", ["auto", "tile", "pipe"])
+@pytest.mark.parametrize("L", [1, 8, 16])
 def test_bf16_ring_packed_shapes(L, kernel):
     """The packed decode shapes (H=16, HV=32, K=V=128) with bf16 inputs, outputs and records over
     one full cycle plus one step."""
