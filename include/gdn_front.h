@@ -58,6 +58,9 @@ int64_t gdn_front_proj_width(int32_t heads, int32_t head_dim, int32_t gate_kind)
  * gdn_gemv_bf16 and gdn_decode_fused for the stage whose arguments fail (GDN_ERR_ARG for splits
  * outside 0 .. 8); then nothing was launched. Device-side errors go to core.err_flags as in
  * gdn_decode_fused (and GDN_DEVERR_TIMEOUT from a projection).
+ * Three launches on `stream`, ordered as ordinary stream work towards the caller: the first is an
+ * ordinary launch; the second and third are programmatic dependent launches that may start while
+ * the launch before them finishes and wait for it before reading its output.
  */
 int gdn_decode_front(const gdn_front_args *args, gdn_stream_t stream);
 

@@ -138,11 +138,11 @@ int prepare_fused(const gdn_fused_args *a, FusedPlan *plan)
     return GDN_OK;
 }
 
-int launch_fused_plan(const FusedPlan &plan, cudaStream_t stream)
+int launch_fused_plan(const FusedPlan &plan, cudaStream_t stream, bool chained)
 {
     if (plan.empty) return GDN_OK;
-    if (plan.use_pipe) return launch_fused_pipe(plan.p, plan.sd, stream);
-    return launch_fused(plan.p, stream);
+    if (plan.use_pipe) return launch_fused_pipe(plan.p, plan.sd, stream, chained);
+    return launch_fused(plan.p, stream, chained);
 }
 
 }  // namespace gdn

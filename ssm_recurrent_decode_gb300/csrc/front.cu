@@ -91,10 +91,13 @@ int gdn_decode_front(const gdn_front_args *a, gdn_stream_t stream)
     if ((rc = gdn::gemv_check(&out, &out_splits)) != GDN_OK) return rc;
     if (in_splits > gdn::kGemvMaxCluster || out_splits > gdn::kGemvMaxCluster) return GDN_ERR_ARG;
 
+    // The fused step and the output projection are chained launches: each may start while the
+    // kernel before it finishes and waits for it before reading that kernel's output. The input
+    // projection is an ordinary launch, so everything before this call has completed first.
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if ((rc = gdn::gemv_launch(in, in_splits, s)) != GDN_OK) return rc;
-    if ((rc = gdn::launch_fused_plan(plan, s)) != GDN_OK) return rc;
-    return gdn::gemv_launch(out, out_splits, s);
+    if ((rc = gdn::launch_fused_plan(plan, s, true)) != GDN_OK) return rc;
+    return gdn::gemv_launch(out, out_splits, s, true);
 }
 
 }  // extern "C"

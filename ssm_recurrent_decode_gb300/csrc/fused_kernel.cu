@@ -40,16 +40,21 @@ __global__ void __launch_bounds__(kThreads, 2) fused_kernel(const __grid_constan
     __shared__ float o_s[D];
     __shared__ float red[kWarps];
 
+    grid_launch_dependents();
     const int slot = a.state_indices[t_];
-    if (slot == a.pad_slot_id || slot < 0 || slot >= a.num_slots) {   // uniform over the CTA
+    const bool skip = slot == a.pad_slot_id || slot < 0 || slot >= a.num_slots;   // uniform over the CTA
+    float *S = a.state + ((size_t)(skip ? 0 : slot) * heads + h) * (size_t)D * D;
+    TL t;
+    t.init();
+    if (!skip) t.load(S, D, 0);
+    // In a chained layer call the previous kernel (the input projection) writes x and the gate
+    // rows, never the state or the slot indices: the state tile is already in flight here.
+    grid_dependency_wait();
+    if (skip) {
         if (slot != a.pad_slot_id && threadIdx.x == 0) raise_flag(a.err_flags, GDN_DEVERR_BAD_INDEX);
         for (int r = threadIdx.x; r < D; r += kThreads) out[r] = __float2bfloat16_rn(0.f);
         return;
     }
-    float *S = a.state + ((size_t)slot * heads + h) * (size_t)D * D;
-    TL t;
-    t.init();
-    t.load(S, D, 0);
 
     // (1) conv update of the 3*D channels of this head
     bf16 *cs = static_cast<bf16 *>(a.conv_state);
@@ -140,20 +145,26 @@ __global__ void __launch_bounds__(kThreads, 2) fused_kernel(const __grid_constan
 }
 
 template <int D>
-static int launch_fused_t(const FusedLaunch &p, cudaStream_t stream)
+static int launch_fused_t(const FusedLaunch &p, cudaStream_t stream, bool chained)
 {
-    const unsigned ctas = (unsigned)p.a.T * (unsigned)p.a.heads;
-    fused_kernel<D><<<ctas, kThreads, 0, stream>>>(p);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3((unsigned)p.a.T * (unsigned)p.a.heads);
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    if (chained) set_programmatic(attr[cfg.numAttrs++]);
+    if (cudaLaunchKernelEx(&cfg, fused_kernel<D>, p) != cudaSuccess) return GDN_ERR_LAUNCH;
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
 }
 
-int launch_fused(const FusedLaunch &p, cudaStream_t stream)
+int launch_fused(const FusedLaunch &p, cudaStream_t stream, bool chained)
 {
     switch (p.a.head_dim) {
-    case 16: return launch_fused_t<16>(p, stream);
-    case 32: return launch_fused_t<32>(p, stream);
-    case 64: return launch_fused_t<64>(p, stream);
-    case 128: return launch_fused_t<128>(p, stream);
+    case 16: return launch_fused_t<16>(p, stream, chained);
+    case 32: return launch_fused_t<32>(p, stream, chained);
+    case 64: return launch_fused_t<64>(p, stream, chained);
+    case 128: return launch_fused_t<128>(p, stream, chained);
     default: return GDN_ERR_SHAPE;
     }
 }

@@ -86,6 +86,8 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_pipe_kernel(const __grid_c
         zero_flag = 0;
         fence_barrier_init();
     }
+    grid_launch_dependents();
+    grid_dependency_wait();   // in a chained layer call x and the gate rows are the previous kernel's output
     __syncthreads();
 
     if (warp == kFCW) {
@@ -372,7 +374,7 @@ static size_t fused_pipe_smem() { return 3 * (size_t)FusedLayout::stage + 2 * 3 
 
 bool fused_pipe_fits(int max_smem) { return fused_pipe_smem() + 8192 <= (size_t)max_smem; }
 
-int launch_fused_pipe(const FusedLaunch &p, bool sd, cudaStream_t stream)
+int launch_fused_pipe(const FusedLaunch &p, bool sd, cudaStream_t stream, bool chained)
 {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -383,8 +385,15 @@ int launch_fused_pipe(const FusedLaunch &p, bool sd, cudaStream_t stream)
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return GDN_ERR_LAUNCH;
     const int tiles = p.a.T * p.a.heads;
-    const int grid = tiles < sms ? tiles : sms;
-    kern<<<grid, kFThreads, smem, stream>>>(p);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3((unsigned)(tiles < sms ? tiles : sms));
+    cfg.blockDim = dim3(kFThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    if (chained) set_programmatic(attr[cfg.numAttrs++]);
+    if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return GDN_ERR_LAUNCH;
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
 }
 

@@ -39,14 +39,17 @@ struct FusedPlan {
 };
 
 // The host checks of gdn_decode_fused (the same status codes) and its kernel choice; no CUDA launch.
+// chained (launch_fused_plan and the launchers below): the launch may start while the previous
+// kernel on the stream finishes (programmatic dependent launch); the kernel waits for that kernel
+// before it reads its inputs, and reads before the wait only the state tile and the slot indices.
 int prepare_fused(const gdn_fused_args *a, FusedPlan *plan);
-int launch_fused_plan(const FusedPlan &plan, cudaStream_t stream);
+int launch_fused_plan(const FusedPlan &plan, cudaStream_t stream, bool chained = false);
 
 // Host launchers, one per kernel family; each dispatches on K and the dtypes. They return
 // GDN_OK or GDN_ERR_LAUNCH / GDN_ERR_SHAPE and never synchronise.
 int launch_step(const StepLaunch &p, cudaStream_t stream);
 int launch_buffered(const StepLaunch &p, int ring_dtype, cudaStream_t stream);
-int launch_fused(const FusedLaunch &p, cudaStream_t stream);
+int launch_fused(const FusedLaunch &p, cudaStream_t stream, bool chained = false);
 
 // Dynamic shared memory the buffered kernel needs for ring length L, value dim V and key dim K.
 size_t buffered_smem_bytes(int L, int V, int K);
@@ -58,7 +61,7 @@ bool buffered_pipe_fits(int L, int in_dtype, int ring_dtype, int max_smem);
 
 // The persistent, warp-specialised fused kernel (head_dim 128; conv state in the DS layout, or in
 // the SD layout when sd is true).
-int launch_fused_pipe(const FusedLaunch &p, bool sd, cudaStream_t stream);
+int launch_fused_pipe(const FusedLaunch &p, bool sd, cudaStream_t stream, bool chained = false);
 bool fused_pipe_fits(int max_smem);
 
 }  // namespace gdn

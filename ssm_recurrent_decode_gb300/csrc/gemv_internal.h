@@ -34,10 +34,17 @@ __device__ __forceinline__ void gemv_store(const gdn_gemv_args &P, int t, int n,
         static_cast<float *>(P.y)[(size_t)t * P.y_stride + n] = v;
 }
 
+// A chained launch (below) prefetches its weights into L2 while it waits for the kernel before it
+// when W takes at most half of L2; larger weights would evict one another before use.
+constexpr size_t kPrefetchMaxBytes = 64u << 20;
+inline bool gemv_prefetch_fits(const gdn_gemv_args &p) { return (size_t)p.N * (size_t)p.Kd * 2 <= kPrefetchMaxBytes; }
+
 // The host checks of gdn_gemv_bf16 and its split count (*splits = 0: nothing to launch), without
-// any CUDA launch; gemv_launch then launches a checked call.
+// any CUDA launch; gemv_launch then launches a checked call. chained: the launch may start while
+// the previous kernel on the stream finishes (programmatic dependent launch; the kernel waits for
+// that kernel before it reads x).
 int gemv_check(const gdn_gemv_args *a, int *splits);
-int gemv_launch(const gdn_gemv_args &p, int splits, cudaStream_t stream);
+int gemv_launch(const gdn_gemv_args &p, int splits, cudaStream_t stream, bool chained = false);
 
 // tcgen05 form: output rows per CTA (the MMA's M), inputs per stage, token rows per pass (N)
 constexpr int kTcRows = 128;
@@ -61,6 +68,7 @@ int gemv_tc_resident_ctas(int stages);
 // launches the tcgen05 form over every pass of 16 token rows (as a cluster launch when the ranges
 // are combined in a cluster; a workspace sum is left to the caller); k_per_split is a multiple of
 // kTcStageK
-int gemv_tc_launch(const gdn_gemv_args &p, int splits, int k_per_split, int stages, cudaStream_t stream);
+int gemv_tc_launch(const gdn_gemv_args &p, int splits, int k_per_split, int stages, cudaStream_t stream,
+                   bool chained = false);
 
 }  // namespace gdn

@@ -9,8 +9,9 @@
 //  - two or more token rows: tcgen05 tensor cores with TMA-staged tiles (gemv_tc.cu). At 8 token
 //    rows a CUDA-core form needs about 4 FMAs per weight byte, close to the SM's FMA rate at HBM
 //    speed; the tensor core takes that work off the FMA pipe.
-// Split-K: blockIdx.y selects a K range whose partial sums go to the workspace, and a second small
-// kernel adds the ranges in order (deterministic).
+// Split-K: blockIdx.y selects a K range. Up to 8 ranges of a row block are one thread-block cluster
+// and add their sums, in range order, through distributed shared memory; more ranges leave partial
+// sums in the workspace and a second small kernel adds them in order (deterministic either way).
 //
 // Source: "Optimization Log: Qwen3.5-27B Dense on B200", Kernel 3 (BF16 GEMV with split-K).
 #include <cstdint>
@@ -76,7 +77,8 @@ __device__ __forceinline__ float reduce_scatter32(float (&x)[32], int lane)
 // W [17408, 5120].
 template <int TOK>
 __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const __grid_constant__ gdn_gemv_args P, int t0,
-                                                            int nt, int k_per_split, int xs_elems, int mode)
+                                                            int nt, int k_per_split, int xs_elems, int mode,
+                                                            int prefetch_w)
 {
     extern __shared__ __align__(16) unsigned char gemv_sm[];
     __shared__ float red[kGemvWarps * kRows * TOK];   // this K range's sums, cluster mode
@@ -89,6 +91,18 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const __grid_constan
     const bf16 *W = static_cast<const bf16 *>(P.W);
     const bf16 *X = static_cast<const bf16 *>(P.x);
     const bool staged = xs_elems > 0;
+    const int n0 = (blockIdx.x * kGemvWarps + warp) * kRows;
+    grid_launch_dependents();
+    if (prefetch_w) {
+        // A chained launch may start while the previous kernel still runs: bring this warp's
+        // weight rows into L2 in the meantime, one 128-byte line per lane and prefetch.
+#pragma unroll
+        for (int r = 0; r < kRows; ++r)
+            if (n0 + r < P.N)
+                for (int k = k_begin + lane * 64; k < k_end; k += 32 * 64)
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(W + (size_t)(n0 + r) * P.Kd + k));
+    }
+    grid_dependency_wait();   // in a chained layer call x is the previous kernel's output
     if (staged) {
         const int per_row = krange / 8;
         for (int e = threadIdx.x; e < nt * per_row; e += kGemvThreads) {
@@ -98,7 +112,6 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const __grid_constan
         cp_async_wait_all();
         __syncthreads();
     }
-    const int n0 = (blockIdx.x * kGemvWarps + warp) * kRows;
     float sum = 0.f;
     if (n0 < P.N) {   // whole warps
         float acc[kRows][TOK];
@@ -247,31 +260,33 @@ static size_t stage_bytes(const GemvPlan &pl, int nt, int *arg)
     return bytes;
 }
 
-int gemv_launch(const gdn_gemv_args &p, int splits, cudaStream_t stream)
+int gemv_launch(const gdn_gemv_args &p, int splits, cudaStream_t stream, bool chained)
 {
     const GemvPlan pl = make_plan(p.T, p.N, p.Kd, splits);
     const int mode = gemv_reduce_mode(splits);
     if (pl.form == Form::kTc) {
-        const int rc = gemv_tc_launch(p, splits, pl.k_per_split, kTcStages, stream);
+        const int rc = gemv_tc_launch(p, splits, pl.k_per_split, kTcStages, stream, chained);
         if (rc != GDN_OK) return rc;
     } else {
         cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         cfg.gridDim = dim3((unsigned)pl.ctas_n, (unsigned)splits);
         cfg.blockDim = dim3(kGemvThreads);
         cfg.stream = stream;
+        cfg.attrs = attr;
         if (mode == kGemvReduceCluster) {
-            attr[0].id = cudaLaunchAttributeClusterDimension;   // the K ranges of a row block
-            attr[0].val.clusterDim.x = 1;
-            attr[0].val.clusterDim.y = (unsigned)splits;
-            attr[0].val.clusterDim.z = 1;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
+            attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;   // the K ranges of a row block
+            attr[cfg.numAttrs].val.clusterDim.x = 1;
+            attr[cfg.numAttrs].val.clusterDim.y = (unsigned)splits;
+            attr[cfg.numAttrs].val.clusterDim.z = 1;
+            ++cfg.numAttrs;
         }
+        if (chained) set_programmatic(attr[cfg.numAttrs++]);
+        const int prefetch_w = chained && gemv_prefetch_fits(p) ? 1 : 0;
         for (int t0 = 0; t0 < p.T; ++t0) {
             int xs = 0;
             cfg.dynamicSmemBytes = stage_bytes(pl, 1, &xs);
-            if (cudaLaunchKernelEx(&cfg, gemv_kernel<1>, p, t0, 1, pl.k_per_split, xs, mode) != cudaSuccess)
+            if (cudaLaunchKernelEx(&cfg, gemv_kernel<1>, p, t0, 1, pl.k_per_split, xs, mode, prefetch_w) != cudaSuccess)
                 return GDN_ERR_LAUNCH;
         }
     }

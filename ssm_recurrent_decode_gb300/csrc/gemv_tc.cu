@@ -70,6 +70,14 @@ __device__ __forceinline__ void tma_tile_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// asks L2 to fetch a tile (no shared-memory destination, no completion to wait for)
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int c0, int c1)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tma_tile_2d_hint(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar,
                                                  uint64_t policy)
 {
@@ -120,7 +128,8 @@ __device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16])
 __global__ void __launch_bounds__(kTcThreads) gemv_tc_kernel(const __grid_constant__ gdn_gemv_args P,
                                                              const __grid_constant__ CUtensorMap wmap,
                                                              const __grid_constant__ CUtensorMap xmap, int t0, int nt,
-                                                             int k_per_split, int stages, int mode)
+                                                             int k_per_split, int stages, int mode,
+                                                             int prefetch_w)
 {
     extern __shared__ unsigned char tc_sm[];
     __shared__ __align__(8) uint64_t full[kTcMaxStages];    // stage filled (TMA bytes landed)
@@ -161,6 +170,15 @@ __global__ void __launch_bounds__(kTcThreads) gemv_tc_kernel(const __grid_consta
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
+    grid_launch_dependents();
+    if (prefetch_w && threadIdx.x == 0) {
+        // A chained launch may start while the previous kernel still runs: bring this CTA's weight
+        // tiles (the same tiles the producer copies below) into L2 in the meantime.
+        for (int it = 0; it < nk; ++it)
+#pragma unroll
+            for (int c = 0; c < kTcChunks; ++c) tma_prefetch_2d(&wmap, k_begin + it * kTcStageK + c * kTcK, n0);
+    }
+    grid_dependency_wait();   // in a chained layer call x is the previous kernel's output
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -403,7 +421,8 @@ int gemv_tc_resident_ctas(int stages)
     return n < 1 ? 1 : n;
 }
 
-int gemv_tc_launch(const gdn_gemv_args &p, int splits, int k_per_split, int stages, cudaStream_t stream)
+int gemv_tc_launch(const gdn_gemv_args &p, int splits, int k_per_split, int stages, cudaStream_t stream,
+                   bool chained)
 {
     if (stages < 2 || stages > kTcMaxStages || k_per_split % kTcStageK != 0) return GDN_ERR_ARG;
     CUtensorMap wmap, xmap;
@@ -414,22 +433,25 @@ int gemv_tc_launch(const gdn_gemv_args &p, int splits, int k_per_split, int stag
     if (!prepare_device(smem)) return GDN_ERR_LAUNCH;
     const int mode = gemv_reduce_mode(splits);
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cfg.gridDim = dim3((unsigned)((p.N + kTcRows - 1) / kTcRows), (unsigned)splits);
     cfg.blockDim = dim3(kTcThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
+    cfg.attrs = attr;
     if (mode == kGemvReduceCluster) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;   // the K ranges of a row tile
-        attr[0].val.clusterDim.x = 1;
-        attr[0].val.clusterDim.y = (unsigned)splits;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;   // the K ranges of a row tile
+        attr[cfg.numAttrs].val.clusterDim.x = 1;
+        attr[cfg.numAttrs].val.clusterDim.y = (unsigned)splits;
+        attr[cfg.numAttrs].val.clusterDim.z = 1;
+        ++cfg.numAttrs;
     }
+    if (chained) set_programmatic(attr[cfg.numAttrs++]);
+    const int prefetch_w = chained && gemv_prefetch_fits(p) ? 1 : 0;
     for (int t0 = 0; t0 < p.T; t0 += kTcTok) {
         const int nt = p.T - t0 < kTcTok ? p.T - t0 : kTcTok;
-        if (cudaLaunchKernelEx(&cfg, gemv_tc_kernel, p, wmap, xmap, t0, nt, k_per_split, stages, mode) != cudaSuccess)
+        if (cudaLaunchKernelEx(&cfg, gemv_tc_kernel, p, wmap, xmap, t0, nt, k_per_split, stages, mode,
+                               prefetch_w) != cudaSuccess)
             return GDN_ERR_LAUNCH;
     }
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;

@@ -114,3 +114,61 @@ def test_explicit_splits_bf16_output_and_row_view(in_splits, out_splits):
     w = _run_front(5, 512, 4, 64, seed=9, steps=2, in_splits=in_splits, out_splits=out_splits,
                    y_dtype=torch.bfloat16, x_pitch=640)
     assert _ok(w, y_bar=2e-2), w          # bf16 y: its own rounding, 2^-8 relative
+
+
+@pytest.mark.parametrize("T", [1, 3, 12])
+def test_graph_replay_matches_eager_calls(T):
+    """The chained launches of one call (programmatic dependent launch) become graph edges under
+    capture; replaying the captured call gives the same bits as eager calls, step after step, for
+    the one-row projection (T = 1), the tensor-core projection (T = 3) and the pipelined fused
+    kernel (T = 12: 384 (token, head) tiles)."""
+    hidden, heads, D, steps = 512, 32, 128, 3
+    dim = heads * D
+    P = gdn.front_proj_width(heads, D, "gdn")
+    num_slots = T + 4
+    ins = syn.fused_inputs(T, heads, D, num_slots, 21)
+    W_in, W_out = _weights(P, hidden, dim, 21)
+    conv_w = torch.from_numpy(ins["conv_w"]).cuda()
+    A_log = torch.from_numpy(ins["A_log"]).cuda()
+    dtb = torch.from_numpy(np.ascontiguousarray(ins["dt_bias"][:heads])).cuda()
+    norm_w = torch.from_numpy(ins["norm_w"]).cuda()
+    idx = torch.arange(1, T + 1, dtype=torch.int32, device="cuda")
+    S0 = torch.empty((num_slots, heads, D, D), dtype=torch.float32, device="cuda")
+    syn.fill_normal_(S0, 21, syn.Tag.STATE, 0, 1.0)
+    cs0 = bits_to_torch_bf16(ins["conv_state"]).clone()
+    xs = []
+    for step in range(steps):
+        xb = torch.empty((T, hidden), dtype=torch.bfloat16, device="cuda")
+        syn.fill_normal_(xb, 21, syn.Tag.X, step, 1.0)
+        xs.append(xb)
+    runs = []
+    for graphed in (False, True):
+        state, cs = S0.clone(), cs0.clone()
+        x = torch.empty((T, hidden), dtype=torch.bfloat16, device="cuda")
+        z = torch.empty((T, P), dtype=torch.bfloat16, device="cuda")
+        o = torch.empty((T, dim), dtype=torch.bfloat16, device="cuda")
+        y = torch.empty((T, hidden), dtype=torch.float32, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+        def call():
+            gdn.gdn_decode_front(x, W_in, W_out, z, o, y, conv_w, cs, A_log, dtb, state, idx,
+                                 norm_w, pad_slot_id=0, gate_kind="gdn", err_flags=err)
+
+        graph = None
+        if graphed:
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=side):
+                call()
+            torch.cuda.current_stream().wait_stream(side)
+        ys = []
+        for step in range(steps):
+            x.copy_(xs[step])
+            graph.replay() if graph is not None else call()
+            ys.append(y.clone())
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        runs.append(ys + [state, cs])
+    for a_, b_ in zip(*runs):
+        assert torch.equal(a_, b_)
