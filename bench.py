@@ -78,13 +78,16 @@ KERNEL_FILES = {
     "buffered": ["ssm_recurrent_decode_gb300/csrc/buffered_pipe.cu", "ssm_recurrent_decode_gb300/csrc/gdn_pipe.cuh",
                  "ssm_recurrent_decode_gb300/csrc/gdn_tile.cuh", "ssm_recurrent_decode_gb300/csrc/gdn_common.cuh"],
     "fused": ["ssm_recurrent_decode_gb300/csrc/fused_pipe.cu", "ssm_recurrent_decode_gb300/csrc/gdn_pipe.cuh",
-              "ssm_recurrent_decode_gb300/csrc/gdn_tile.cuh", "ssm_recurrent_decode_gb300/csrc/gdn_common.cuh"],
+              "ssm_recurrent_decode_gb300/csrc/gdn_tile.cuh", "ssm_recurrent_decode_gb300/csrc/gdn_common.cuh",
+              "ssm_recurrent_decode_gb300/csrc/gdn_chain.cuh"],
     "mamba": ["ssm_recurrent_decode_gb300/csrc/mamba_kernel.cu", "ssm_recurrent_decode_gb300/csrc/gdn_common.cuh"],
     "front": ["ssm_recurrent_decode_gb300/csrc/front.cu", "ssm_recurrent_decode_gb300/csrc/gemv_kernel.cu",
-              "ssm_recurrent_decode_gb300/csrc/gemv_tc.cu", "ssm_recurrent_decode_gb300/csrc/fused_pipe.cu"],
+              "ssm_recurrent_decode_gb300/csrc/gemv_tc.cu", "ssm_recurrent_decode_gb300/csrc/fused_pipe.cu",
+              "ssm_recurrent_decode_gb300/csrc/fused_kernel.cu", "ssm_recurrent_decode_gb300/csrc/gdn_chain.cuh"],
     "gemv": ["ssm_recurrent_decode_gb300/csrc/gemv_kernel.cu", "ssm_recurrent_decode_gb300/csrc/gemv_tc.cu",
              "ssm_recurrent_decode_gb300/csrc/gemv_internal.h", "ssm_recurrent_decode_gb300/csrc/gdn_cluster.cuh",
-             "ssm_recurrent_decode_gb300/csrc/gdn_pipe.cuh", "ssm_recurrent_decode_gb300/csrc/gdn_common.cuh"],
+             "ssm_recurrent_decode_gb300/csrc/gdn_pipe.cuh", "ssm_recurrent_decode_gb300/csrc/gdn_common.cuh",
+             "ssm_recurrent_decode_gb300/csrc/gdn_chain.cuh"],
 }
 
 

@@ -15,6 +15,7 @@
 // raw_g/raw_beta/A_log/dt_bias; _gated_rmsnorm); "Optimization Log: Qwen3.5-27B Dense on B200",
 // "Kernel 2" (rmsnorm times silu(gate)) and "Kernel 5" (shift + insert + dot product + SiLU).
 // The KDA decay formula is not printed on those pages; kda_gate_form selects one of two readings.
+#include "gdn_chain.cuh"
 #include "gdn_launch.h"
 #include "gdn_tile.cuh"
 

@@ -15,6 +15,7 @@
 // Sources: "Microbenchmark for the fused Kimi-K3 KDA decode kernel on ROCm" (module docstring,
 // Inputs, triton_chain, _gated_rmsnorm, fused); "Optimization Log: Qwen3.5-27B Dense on B200",
 // Kernel 2, Kernel 4 and Kernel 5.
+#include "gdn_chain.cuh"
 #include "gdn_launch.h"
 #include "gdn_pipe.cuh"
 #include "gdn_tile.cuh"

@@ -17,6 +17,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "gdn_chain.cuh"
 #include "gdn_cluster.cuh"
 #include "gdn_common.cuh"
 #include "gdn_pipe.cuh"
