@@ -26,7 +26,10 @@ __device__ __forceinline__ float bf(const void *p, size_t i)
     return __bfloat162float(static_cast<const bf16 *>(p)[i]);
 }
 
-template <int D>
+// CHAIN: the instance for chained launches (gdn_decode_front), which waits for the kernel before it
+// after its state loads; ordinary launches run the instance without the wait, which measured
+// about 1% faster standalone on GB300 at one or eight tokens.
+template <int D, bool CHAIN>
 __global__ void __launch_bounds__(kThreads, 2) fused_kernel(const __grid_constant__ FusedLaunch P)
 {
     using TL = Tile<D>;
@@ -41,7 +44,7 @@ __global__ void __launch_bounds__(kThreads, 2) fused_kernel(const __grid_constan
     __shared__ float o_s[D];
     __shared__ float red[kWarps];
 
-    grid_launch_dependents();
+    if constexpr (CHAIN) grid_launch_dependents();
     const int slot = a.state_indices[t_];
     const bool skip = slot == a.pad_slot_id || slot < 0 || slot >= a.num_slots;   // uniform over the CTA
     float *S = a.state + ((size_t)(skip ? 0 : slot) * heads + h) * (size_t)D * D;
@@ -50,7 +53,7 @@ __global__ void __launch_bounds__(kThreads, 2) fused_kernel(const __grid_constan
     if (!skip) t.load(S, D, 0);
     // In a chained layer call the previous kernel (the input projection) writes x and the gate
     // rows, never the state or the slot indices: the state tile is already in flight here.
-    grid_dependency_wait();
+    if constexpr (CHAIN) grid_dependency_wait();
     if (skip) {
         if (slot != a.pad_slot_id && threadIdx.x == 0) raise_flag(a.err_flags, GDN_DEVERR_BAD_INDEX);
         for (int r = threadIdx.x; r < D; r += kThreads) out[r] = __float2bfloat16_rn(0.f);
@@ -155,7 +158,8 @@ static int launch_fused_t(const FusedLaunch &p, cudaStream_t stream, bool chaine
     cfg.stream = stream;
     cfg.attrs = attr;
     if (chained) set_programmatic(attr[cfg.numAttrs++]);
-    if (cudaLaunchKernelEx(&cfg, fused_kernel<D>, p) != cudaSuccess) return GDN_ERR_LAUNCH;
+    if (cudaLaunchKernelEx(&cfg, chained ? fused_kernel<D, true> : fused_kernel<D, false>, p) != cudaSuccess)
+        return GDN_ERR_LAUNCH;
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
 }
 
