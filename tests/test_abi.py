@@ -202,3 +202,24 @@ def test_front_checks():
     assert L.gdn_decode_front(ctypes.byref(a), None) == -6
     a.core.gate_kind, a.T = gdn.GDN_FUSED_GATE_GDN, 0
     assert L.gdn_decode_front(ctypes.byref(a), None) == 0             # nothing to do
+
+
+@pytest.mark.parametrize("T,N,Kd,want", [
+    (1, 17408, 5120, 1),    # 544 one-row CTAs fit the 608 slots (4 per SM) at one range
+    (1, 5120, 17408, 2),    # one range would stage 34 KB of x per CTA (over 24 KB): two
+    (8, 17408, 5120, 2),    # 136 tensor-core tiles; 272 CTAs fit the 456 slots (3 per SM), 544 do not
+    (8, 5120, 17408, 8),    # 40 tiles: 320 CTAs at eight ranges still fit one wave
+    (16, 5120, 17408, 8),
+    (2, 4096, 1024, 2),     # at least 512 inputs per range caps the split count
+])
+def test_gemv_default_split_rule_on_the_page_shapes(T, N, Kd, want):
+    """The split count for splits == 0: the largest power of two up to 8 whose grid fits one
+    wave of resident CTAs (with its x slice staged), at least 512 inputs per range. Without a
+    device the library takes GB300's counts (152 SMs; 4 one-row CTAs or 3 tensor-core CTAs per
+    SM), and these are the counts measured at the Optimization Log's decode shapes."""
+    import torch
+    if torch.cuda.is_available():
+        props = torch.cuda.get_device_properties(0)
+        if props.multi_processor_count != 152:
+            pytest.skip("the expected counts are GB300's")
+    assert gdn.lib().gdn_gemv_default_splits(T, N, Kd) == want
