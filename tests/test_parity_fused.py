@@ -93,8 +93,9 @@ def _run_fused(T, heads, D, *, layout="DS", gate_kind="kda", form=0, act="silu",
 @pytest.mark.parametrize("layout", ["DS", "SD"])
 @pytest.mark.parametrize("T", [1, 2, 4, 8])
 def test_kda_config_shapes(layout, T, kernel):
-    """The fused KDA decode shapes: 96 heads x 128, conv width 4, lower bound -5, silu gate. The
-    per-tile kernel splits each tile over a cluster of 8, 4, 2 and 1 CTAs at T = 1, 2, 4, 8."""
+    """The fused KDA decode shapes: 96 heads x 128, conv width 4, lower bound -5, silu gate, at
+    the token counts where the library picks the per-tile kernel (one CTA per (token, head)); both
+    kernels forced."""
     w = _run_fused(T, 96, 128, layout=layout, seed=T, kernel=kernel)
     assert w["out"] <= 2e-2 and w["state"] <= 1e-5, w
 
@@ -103,6 +104,13 @@ def test_kda_config_shapes(layout, T, kernel):
 def test_kda_32_tokens_sampled_rows(kernel):
     """3072 tiles: the pipelined kernel walks about twenty per CTA through its stages."""
     w = _run_fused(32, 96, 128, seed=32, sample_rows=[0, 7, 19, 31], kernel=kernel, steps=2)
+    assert w["out"] <= 2e-2 and w["state"] <= 1e-5, w
+
+
+def test_kda_full_size_sampled_rows():
+    """The benchmark's launch: 128 tokens x 96 heads (12288 tiles, the pipelined kernel's default
+    choice, about 80 tiles per persistent CTA), sampled token rows against the oracle."""
+    w = _run_fused(128, 96, 128, seed=128, sample_rows=[0, 41, 90, 127])
     assert w["out"] <= 2e-2 and w["state"] <= 1e-5, w
 
 
@@ -117,7 +125,7 @@ def test_gate_readings_and_activations(form, act):
 
 @pytest.mark.parametrize("D,kernel", [(16, "auto"), (32, "auto"), (128, "auto"), (128, "tile")])
 def test_gdn_gate_and_small_heads(D, kernel):
-    """At head_dim 128 the per-tile kernel splits these 20 tiles over clusters of 8 CTAs."""
+    """The GDN gate (one decay per head) at several head sizes; 20 (token, head) tiles."""
     w = _run_fused(5, 4, D, gate_kind="gdn", seed=D, steps=2, layout="SD", kernel=kernel)
     assert w["out"] <= 2e-2 and w["state"] <= 1e-5, w
 
