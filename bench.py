@@ -270,6 +270,15 @@ def cpu_baseline(H, HV, K, V, seed, budget_s=10.0):
             "all_cores": all_cores}
 
 
+def packed_workload_config(B, H, HV, K, V, state_dtype="f32"):
+    """The packed decode workload as both arms name it: the `workload` text and its sizes."""
+    sbytes = 4 if state_dtype == "f32" else 2
+    return (f"gdn packed decode over a slot pool: B={B} H={H} HV={HV} K=V={K}, bf16 mixed_qkv/a/b/out, "
+            f"{state_dtype} state [{B},{HV},{V},{K}], permuted int32 cache indices",
+            {"B": B, "H": H, "HV": HV, "K": K, "V": V, "input_dtype": "bf16", "state_dtype": state_dtype,
+             "state_bytes_per_step": 2 * B * HV * V * K * sbytes})
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -287,16 +296,16 @@ def run_reference(args):
         spent += sampler.run(tiles_per_step)[1]
     state_bytes = args.steps * tiles_per_step * 2 * V * K * 4
     value = state_bytes / spent / 1e9
+    name, sizes = packed_workload_config(B, H, HV, K, V)
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(spent / args.steps * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"gdn packed decode B={B} H={H} HV={HV} K=V={K}, fp64 CPU oracle on "
-                               f"{tiles_per_step} (slot, value head) tiles per step",
-                   "B": B, "H": H, "HV": HV, "K": K, "V": V},
+        "config": {"workload": name, **sizes},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{tiles_per_step} tiles per step, one thread"},
+                         "sample": f"{tiles_per_step} of the {B * HV} (slot, value head) tiles per step "
+                                   f"through the fp64 C oracle, one thread"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -548,12 +557,11 @@ def run_packed(args):
     state_bytes = 2 * B * HV * V * K * sbytes
     gbs = h.world * state_bytes / (ms * 1e-3) / 1e9
     peak, _ = hbm_peak()
+    name, sizes = packed_workload_config(B, H, HV, K, V, args.state_dtype)
+    assert sizes["state_bytes_per_step"] == state_bytes
     line = base_line(
-        h, gbs, ms, steps, args.warmup,
-        f"gdn packed decode over a slot pool: B={B} H={H} HV={HV} K=V={K}, bf16 mixed_qkv/a/b/out, "
-        f"{args.state_dtype} state [{B},{HV},{V},{K}], permuted int32 cache indices",
-        {"B": B, "H": H, "HV": HV, "K": K, "V": V, "input_dtype": "bf16", "state_dtype": args.state_dtype,
-         "state_bytes_per_step": state_bytes, "state_pools": n_pools,
+        h, gbs, ms, steps, args.warmup, name,
+        {**sizes, "state_pools": n_pools,
          "l2": (f"state of {state_bytes / 2 / 1e9:.2f} GB read per step, larger than the L2: no flush "
                 f"between steps" if n_pools == 1 else
                 f"{n_pools} state pools rotated, at least 4x the L2 size per pass"),

@@ -29,3 +29,13 @@ def test_traffic_records_are_well_formed():
 
 def test_cpu_model_is_described():
     assert isinstance(bench.cpu_model(), str) and bench.cpu_model()
+
+
+def test_both_arms_name_the_same_packed_workload():
+    """The GPU arm and the oracle arm describe the packed decode with one config: its text and
+    sizes, and the state bytes of one step (read and written once)."""
+    name, sizes = bench.packed_workload_config(256, 16, 32, 128, 128)
+    assert "B=256" in name and "HV=32" in name and "K=V=128" in name and "f32 state" in name
+    assert sizes["state_bytes_per_step"] == 2 * 256 * 32 * 128 * 128 * 4
+    _, half = bench.packed_workload_config(256, 16, 32, 128, 128, "bf16")
+    assert half["state_bytes_per_step"] * 2 == sizes["state_bytes_per_step"]
