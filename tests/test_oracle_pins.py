@@ -659,6 +659,93 @@ def test_decode_front_selects_columns():
     check_decode_front_selects_columns()
 
 
+# --------------------------------------------------------------------------------------------
+# scalar closed form and an independent restatement of the packed step
+# --------------------------------------------------------------------------------------------
+def check_scalar_closed_form():
+    """K = V = 1 with |k|, |q| so large that x / sqrt(x^2 + 1e-6) rounds to sign(x) in fp64: one
+    step is S' = e^g S (1 - beta) + beta v sign(k) and o = S' sign(q) (the scale 1^-1/2 is 1)."""
+    gs = [0.0, -0.7, -3.0, 0.0, -0.2, -1.5]
+    betas = [0.0, 0.3, 1.0, 1.0, 0.55, 0.9]
+    ks = [1e5, -2e5, 3e4, -1e6, 5e4, -7e4]
+    qs = [-4e4, 1e5, 2e5, 3e4, -6e5, 1e4]
+    vs = [0.25, -1.5, 2.0, 0.75, -0.3, 1.1]
+    S0 = [1.0, -0.5, 3.0, -2.0, 0.125, 0.7]
+    B = len(gs)
+    q = np.array(qs).reshape(B, 1, 1); k = np.array(ks).reshape(B, 1, 1)
+    v = np.array(vs).reshape(B, 1, 1)
+    S = np.array(S0).reshape(B, 1, 1, 1)
+    out, _ = oracle.delta_step(q, k, v, np.array(gs).reshape(B, 1), np.array(betas).reshape(B, 1), S,
+                               scale=1.0)
+    for i in range(B):
+        want = math.exp(gs[i]) * S0[i] * (1.0 - betas[i]) + betas[i] * vs[i] * math.copysign(1.0, ks[i])
+        assert abs(S[i, 0, 0, 0] - want) <= 1e-14 * max(1.0, abs(want)), (i, S[i, 0, 0, 0], want)
+        assert abs(out[i, 0, 0] - want * math.copysign(1.0, qs[i])) <= 1e-14 * max(1.0, abs(want)), i
+
+
+def _twin_packed_step(mixed, a, b, A_log, dt_bias, S, H, HV, K, V):
+    """One packed GDN decode step restated with Python floats and loops, row b on slot b, written
+    from the sources independently of the oracle: the gates g = -exp(A_log) softplus(a + dt_bias)
+    and beta = sigmoid(b), q/k L2-normalised with eps 1e-6 and q scaled by K^-1/2, q/k head
+    hv // (HV / H), then decay, u = S k, delta = beta (v - u), S += delta k^T, o = S q
+    ("Optimization Log: Qwen3.5-27B Dense on B200", Kernel 4 Math block). S is nested lists
+    [slot][hv][v][k], updated in place; returns o as nested lists [b][hv][v]."""
+    G = HV // H
+    out = []
+    for bb in range(len(mixed)):
+        row = [float(x) for x in mixed[bb]]
+        o_row = []
+        for hv in range(HV):
+            h = hv // G
+            q = row[h * K:(h + 1) * K]
+            k = row[H * K + h * K:H * K + (h + 1) * K]
+            v = row[2 * H * K + hv * V:2 * H * K + (hv + 1) * V]
+            g = -math.exp(float(A_log[hv])) * math.log1p(math.exp(float(a[bb][hv]) + float(dt_bias[hv])))
+            beta = 1.0 / (1.0 + math.exp(-float(b[bb][hv])))
+            nk = math.sqrt(sum(t * t for t in k) + 1e-6)
+            nq = math.sqrt(sum(t * t for t in q) + 1e-6)
+            kh = [t / nk for t in k]
+            qh = [t / nq * K ** -0.5 for t in q]
+            M = S[bb][hv]
+            e = math.exp(g)
+            for i in range(V):
+                for j in range(K):
+                    M[i][j] *= e
+            u = [sum(M[i][j] * kh[j] for j in range(K)) for i in range(V)]
+            d = [beta * (v[i] - u[i]) for i in range(V)]
+            for i in range(V):
+                for j in range(K):
+                    M[i][j] += d[i] * kh[j]
+            o_row.append([sum(M[i][j] * qh[j] for j in range(K)) for i in range(V)])
+        out.append(o_row)
+    return out
+
+
+def check_python_twin_tiny():
+    """The tiny decode (B=2, H=2, HV=4, K=V=16, fp32 inputs, 8 sequential steps): the C oracle
+    and its pure-Python restatement agree to 1e-12 on every output and on the final state."""
+    B, H, HV, K, V = TINY["B"], TINY["H"], TINY["HV"], TINY["K"], TINY["V"]
+    S64 = tiny_state(seed=31, num_slots=B, HV=HV, V=V, K=K)
+    S_twin = S64.tolist()
+    for step in range(8):
+        d = syn.packed_inputs(B, H, HV, K, V, "f32", 31, step)
+        mixed, a, b = (d[n].astype(np.float64) for n in ("mixed_qkv", "a", "b"))
+        A_log, dt_bias = d["A_log"].astype(np.float64), d["dt_bias"].astype(np.float64)
+        o, _ = oracle.gdn_step_packed(mixed, a, b, A_log, dt_bias, S64, H=H, HV=HV, K=K, V=V)
+        o_twin = _twin_packed_step(mixed.tolist(), a.tolist(), b.tolist(), A_log.tolist(),
+                                   dt_bias.tolist(), S_twin, H, HV, K, V)
+        assert rel_err(o, np.array(o_twin)) <= 1e-12, step
+    assert rel_err(S64, np.array(S_twin)) <= 1e-12
+
+
+def test_scalar_closed_form():
+    check_scalar_closed_form()
+
+
+def test_python_twin_tiny():
+    check_python_twin_tiny()
+
+
 ALL_CHECKS = [
     check_hand_worked_step, check_invariant_no_decay_no_write, check_invariant_exact_recall,
     check_invariant_full_decay, check_closed_matrix_form, check_gqa_duplication,
@@ -667,5 +754,5 @@ ALL_CHECKS = [
     check_conv_update_is_causal_convolution, check_gated_rmsnorm, check_bf16_rounding,
     check_fused_per_key_gate_reduces_to_scalar, check_bf16_state_storage,
     check_mamba_constant_input_geometric_series, check_mamba_output_and_gates, check_gemv,
-    check_decode_front_selects_columns,
+    check_decode_front_selects_columns, check_scalar_closed_form, check_python_twin_tiny,
 ]
