@@ -279,6 +279,62 @@ def packed_workload_config(B, H, HV, K, V, state_dtype="f32"):
              "state_bytes_per_step": 2 * B * HV * V * K * sbytes})
 
 
+def cpu_baseline_buffered(H, HV, K, V, L, seed, budget_s=10.0):
+    """The fp64 oracle's buffered decode on one host thread: whole L-step cycles of one request
+    row (all HV value heads, bf16 inputs and rings) until budget_s seconds of oracle time, counted
+    with the GPU line's mean state traffic, (1 + 1/L) V K 4 bytes per (row, value head) and step."""
+    import gdn_synth as syn
+    import oracle
+    f64 = lambda bits: syn.bf16_bits_to_f32(bits).astype(np.float64)
+    S = syn.normal_f32(seed, syn.Tag.STATE, 0, (1, HV, V, K), 1.0).astype(np.float64)
+    d_c, k_c, g_c = np.zeros((1, HV, L, V)), np.zeros((1, H, L, K)), np.zeros((1, HV, L))
+    steps = []
+    for p in range(L):
+        d = syn.packed_inputs(1, H, HV, K, V, "bf16", seed, p)
+        q, k, v = oracle.split_packed(f64(d["mixed_qkv"]), H, HV, K, V)
+        g, beta = oracle.gdn_gates(f64(d["a"]), f64(d["b"]), d["A_log"], d["dt_bias"])
+        steps.append((q, k, v, g, beta))
+    done, spent = 0, 0.0
+    while spent < budget_s or done % L:
+        p = done % L
+        q, k, v, g, beta = steps[p]
+        t0 = time.perf_counter()
+        oracle.gdn_buffered(q, k, v, g, beta, S, d_c, k_c, g_c, np.array([p], np.int32), L=L,
+                            ring_bf16=True, scale=K ** -0.5)
+        spent += time.perf_counter() - t0
+        done += 1
+    traffic = done * HV * (1 + 1 / L) * V * K * 4
+    return {"value": round(traffic / spent / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "cpu": cpu_model(),
+            "sample": f"{done // L} whole {L}-step cycles of one request row ({HV} value heads, H={H}, "
+                      f"K={K}, V={V}, bf16 inputs and rings), fp64 C oracle, one thread, {spent:.1f} s"}
+
+
+def cpu_baseline_fused(heads, D, seed, budget_s=10.0):
+    """The fp64 oracle's fused KDA decode on one host thread: single-token calls (every head) until
+    budget_s seconds of oracle time, counted with the GPU line's state bytes, 2 D^2 4 per
+    (token, head)."""
+    import gdn_synth as syn
+    import oracle
+    f64 = lambda bits: syn.bf16_bits_to_f32(bits).astype(np.float64)
+    ins = syn.fused_inputs(1, heads, D, 2, seed)
+    S = syn.normal_f32(seed, syn.Tag.STATE, 0, (2, heads, D, D), 1.0).astype(np.float64)
+    cs = f64(ins["conv_state"]).reshape(2, 3 * heads * D, 3)
+    args = (f64(ins["x"]), ins["conv_w"], cs, f64(ins["raw_g"]), f64(ins["raw_beta"]), ins["A_log"],
+            ins["dt_bias"], S, f64(ins["out_gate"]), ins["norm_w"])
+    idx = np.array([1], np.int32)
+    calls, spent = 0, 0.0
+    while spent < budget_s or calls == 0:
+        t0 = time.perf_counter()
+        oracle.fused_kda(*args, idx=idx, pad_slot=0)
+        spent += time.perf_counter() - t0
+        calls += 1
+    return {"value": round(calls * heads * 2 * D * D * 4 / spent / 1e9, 4), "unit": "GB/s", "cores": 1,
+            "kind": "oracle", "cpu": cpu_model(),
+            "sample": f"{calls} single-token calls ({heads} heads x {D}, conv update, per-key decay, "
+                      f"gated RMSNorm), fp64 C oracle, one thread, {spent:.1f} s"}
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -641,6 +697,7 @@ def run_buffered(args):
         "packed_equivalent_state_GBs": round(2 * S / (ms * 1e-3) / 1e9, 2)}, steps)
     line["roofline"] = roofline(state_traffic + ring_append + ring_read_mean + io, ms, "buffered",
                                 f"buffered_B{B}_L{L}")
+    line["cpu_baseline"] = cpu_baseline_buffered(H, HV, K, V, L, seed=8, budget_s=args.cpu_budget)
     line["phase_us"] = [round(p * 1e3, 2) for p in phase_ms]
     line["flush_over_nonflush"] = (round(phase_ms[-1] / statistics.mean(phase_ms[:-1]), 3)
                                    if L > 1 else None)
@@ -717,6 +774,7 @@ def run_fused(args):
          "l2": f"{n_pools} state pool(s) rotated, at least 4x the L2 size per pass",
          "timing": f"CUDA-graph replays of {per_graph} calls"}, steps)
     line["roofline"] = roofline(state_bytes + io, ms, "fused", f"fused_T{T}")
+    line["cpu_baseline"] = cpu_baseline_fused(heads, D, seed=9, budget_s=args.cpu_budget)
     line["clocks"] = clk
     return h.finish(line)
 

@@ -39,3 +39,13 @@ def test_both_arms_name_the_same_packed_workload():
     assert sizes["state_bytes_per_step"] == 2 * 256 * 32 * 128 * 128 * 4
     _, half = bench.packed_workload_config(256, 16, 32, 128, 128, "bf16")
     assert half["state_bytes_per_step"] * 2 == sizes["state_bytes_per_step"]
+
+
+def test_oracle_baselines_of_the_buffered_and_fused_lines():
+    """The buffered baseline runs whole L-step cycles (every phase equally often) and the fused one
+    at least one call; both report a positive figure from one thread."""
+    b = bench.cpu_baseline_buffered(2, 4, 16, 16, 4, seed=1, budget_s=0.05)
+    assert b["value"] > 0 and b["kind"] == "oracle" and b["cores"] == 1
+    assert "whole 4-step cycles" in b["sample"]
+    f = bench.cpu_baseline_fused(4, 16, seed=1, budget_s=0.05)
+    assert f["value"] > 0 and f["kind"] == "oracle" and "single-token" in f["sample"]
