@@ -1,9 +1,9 @@
 /*
  * abi_client.c -- a plain C (C11) client of libgdn_decode.so, built against the headers in
- * include/ only. It needs no GPU: it prints the library's ABI version, the argument struct sizes as this C
- * compiler lays them out next to the library's own, and the status codes that the host-side
- * checks return for calls that must be refused before any CUDA work (the device addresses below
- * are aligned and never dereferenced).
+ * include/ only. It needs no GPU: it prints the library's ABI version, the argument struct sizes
+ * as this C compiler lays them out next to the library's own, and the status codes that the
+ * host-side checks return for calls that must be refused before any CUDA work (the device
+ * addresses below are aligned and never dereferenced).
  */
 #include <stdint.h>
 #include <stdio.h>
