@@ -73,7 +73,7 @@ __device__ __forceinline__ float reduce_scatter32(float (&x)[32], int lane)
 // K range. The rows' slice of x is staged in shared memory when it fits (xs_elems > 0), otherwise
 // read through L1. Each lane issues the weight loads of two 256-input steps before using them
 // (8 x 16 bytes in flight per lane, 4 KB per warp); the 4 x TOK sums are reduced with a butterfly
-// reduce-scatter. On GB300 this form (64 registers, four CTAs per SM) measured faster at one token
+// reduce-scatter. On GB300 this form (56 registers, four CTAs per SM) measured faster at one token
 // row than a leaner single-row variant (44 registers, five CTAs per SM): 27.3 against 31.1 us for
 // W [17408, 5120].
 template <int TOK>
