@@ -279,6 +279,35 @@ def packed_workload_config(B, H, HV, K, V, state_dtype="f32"):
              "state_bytes_per_step": 2 * B * HV * V * K * sbytes})
 
 
+# ------------------------------------------------------------------------------------------------
+# byte counts that the pages print figures for (checked against them in tests/golden/)
+# ------------------------------------------------------------------------------------------------
+def mamba_page_bytes(B, D, N):
+    """Bytes per Mamba-1 decode step by the page's own model: each (row, channel) program moves five
+    N-vectors of fp32 (A row, B, C, old and new state) and about six fp32 scalars, B D (20 N + 24)
+    ("Triton decode kernel + MBU analysis", Microbench, bytes-moved model)."""
+    return B * D * (20 * N + 24)
+
+
+def gemv_weight_bytes(N, Kd):
+    """Bytes of one bf16 projection weight [N, Kd], read once per decode call."""
+    return N * Kd * 2
+
+
+def state_tile_bytes(V, K, state_dtype="f32"):
+    """Bytes of one (slot, head) state tile [V, K] as stored."""
+    return V * K * (4 if state_dtype == "f32" else 2)
+
+
+def fused_layer_bytes(T, heads, D):
+    """Device bytes of one fused-KDA layer's tensors at T tokens with T + 8 slots: the fp32 state
+    pool, the bf16 conv state, x, raw_g, raw_beta, output gate and output, and the fp32 parameters
+    (conv weights, A_log, dt_bias, norm weight), as the fused workload allocates them."""
+    dim, slots = heads * D, T + 8
+    return (slots * heads * D * D * 4 + slots * 3 * dim * 3 * 2 + T * 3 * dim * 2 + T * dim * 2
+            + T * heads * 2 + T * dim * 2 + T * dim * 2 + 3 * dim * 4 * 4 + heads * 4 + dim * 4 + D * 4)
+
+
 def cpu_baseline_buffered(H, HV, K, V, L, seed, budget_s=10.0):
     """The fp64 oracle's buffered decode on one host thread: whole L-step cycles of one request
     row (all HV value heads, bf16 inputs and rings) until budget_s seconds of oracle time, counted
@@ -934,7 +963,7 @@ def run_mamba(args):
     (ms,) = max_over_ranks([ms], h.world)
     if h.rank != 0:
         return h.finish(None)
-    page_bytes = B * D * (20 * N + 24)
+    page_bytes = mamba_page_bytes(B, D, N)
     gbs = h.world * page_bytes / (ms * 1e-3) / 1e9
     line = base_line(
         h, gbs, ms, steps, args.warmup,
@@ -961,7 +990,7 @@ def run_gemv(args):
     T, N, Kd = args.T, args.gemv_n, args.gemv_k
     x = torch.empty((T, Kd), dtype=torch.bfloat16, device=h.dev)
     syn.fill_normal_(x, 91, syn.Tag.X, 0, 1.0)
-    w_bytes = N * Kd * 2
+    w_bytes = gemv_weight_bytes(N, Kd)
     n_pools = pool_count(w_bytes, h.dev)
     Ws = []
     for p in range(n_pools):
