@@ -19,6 +19,10 @@
  *   - conv update, KDA gate, beta and gated RMSNorm: "Microbenchmark for the fused Kimi-K3 KDA decode
  *     kernel on ROCm", functions Inputs, triton_chain and _gated_rmsnorm; "Optimization Log", section
  *     "Kernel 5: Fused Causal Conv1d Update" (shift + insert + dot product + SiLU).
+ *   - the Mamba-1 selective-scan decode step: "Triton decode kernel + MBU analysis", section
+ *     "Kernel design" (the per-element math block).
+ *   - the decode projection y = x W^T: "Optimization Log", section "Kernel 3: BF16 GEMV with
+ *     Split-K" (one sum over all inputs per output here; the split-K order is the kernels' choice).
  * No single-pass or low-rank rewrite of the step appears here: those identities are what the
  * tests check this code against.
  *
