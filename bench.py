@@ -364,6 +364,50 @@ def cpu_baseline_fused(heads, D, seed, budget_s=10.0):
                       f"gated RMSNorm), fp64 C oracle, one thread, {spent:.1f} s"}
 
 
+def _oracle_calls(call, budget_s):
+    """Times `call()` (one oracle invocation) repeatedly until budget_s seconds of oracle time,
+    at least once; returns (calls, seconds)."""
+    calls, spent = 0, 0.0
+    while spent < budget_s or calls == 0:
+        t0 = time.perf_counter()
+        call()
+        spent += time.perf_counter() - t0
+        calls += 1
+    return calls, spent
+
+
+def cpu_baseline_mamba(D, N, seed, budget_s=10.0):
+    """The fp64 oracle's Mamba-1 decode on one host thread: one request row (D channels, fp32
+    inputs) per call until budget_s seconds, counted with the line's bytes model B D (20 N + 24)."""
+    import gdn_synth as syn
+    import oracle
+    m = syn.mamba_inputs(1, D, N, "f32", seed)
+    h = m["h"].astype(np.float64)
+    calls, spent = _oracle_calls(lambda: oracle.mamba_decode(m["x"], m["dt"], m["A"], m["Bm"], m["Cm"], h,
+                                                            Dskip=m["Dskip"], z=m["z"]), budget_s)
+    return {"value": round(calls * mamba_page_bytes(1, D, N) / spent / 1e9, 4), "unit": "GB/s",
+            "cores": 1, "kind": "oracle", "cpu": cpu_model(),
+            "sample": f"{calls} single-row calls (D={D}, N={N}, fp32, D skip and silu(z) gate), fp64 C "
+                      f"oracle, one thread, {spent:.1f} s"}
+
+
+def cpu_baseline_gemv(T, N, Kd, seed, budget_s=10.0, rows=256):
+    """The fp64 oracle's projection on one host thread: `rows` of the N weight rows (a bounded
+    sample; the full fp64 matrix would take N Kd 8 bytes) against T token rows per call until
+    budget_s seconds, counted with the line's bf16 weight bytes for those rows."""
+    import gdn_synth as syn
+    import oracle
+    rows = min(rows, N)
+    x = syn.bf16_bits_to_f32(syn.f32_to_bf16_bits(syn.normal_f32(seed, syn.Tag.X, 0, (T, Kd), 1.0)))
+    W = syn.bf16_bits_to_f32(syn.f32_to_bf16_bits(syn.normal_f32(seed, syn.Tag.CONV_W, 0, (rows, Kd), 0.02)))
+    x, W = x.astype(np.float64), W.astype(np.float64)
+    calls, spent = _oracle_calls(lambda: oracle.gemv(x, W), budget_s)
+    return {"value": round(calls * gemv_weight_bytes(rows, Kd) / spent / 1e9, 4), "unit": "GB/s",
+            "cores": 1, "kind": "oracle", "cpu": cpu_model(),
+            "sample": f"{calls} calls on {rows} of the {N} weight rows (Kd={Kd}, T={T}), fp64 C oracle, "
+                      f"one thread, {spent:.1f} s"}
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -975,6 +1019,7 @@ def run_mamba(args):
                                      "B = 1 / 4 / 8, D = 1536, N = 16 (launch-bound)"}, steps)
     min_bytes = 2 * B * D * N * 4 + D * N * 4 + 2 * B * N * 4 + 4 * B * D * 4 + D * 4
     line["roofline"] = roofline(min_bytes, ms, "mamba", f"mamba_B{B}_D{D}_N{N}")
+    line["cpu_baseline"] = cpu_baseline_mamba(D, N, seed=78, budget_s=args.cpu_budget)
     line["clocks"] = clk
     return h.finish(line)
 
@@ -1025,6 +1070,7 @@ def run_gemv(args):
     # algorithmic bytes: W once, x, y (any split-K exchange is the kernel's overhead)
     io = T * Kd * 2 + T * N * 2
     line["roofline"] = roofline(w_bytes + io, ms, "gemv", f"gemv_T{T}_N{N}_K{Kd}")
+    line["cpu_baseline"] = cpu_baseline_gemv(T, N, Kd, seed=92, budget_s=args.cpu_budget)
     line["clocks"] = clk
     return h.finish(line)
 

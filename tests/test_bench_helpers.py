@@ -49,3 +49,10 @@ def test_oracle_baselines_of_the_buffered_and_fused_lines():
     assert "whole 4-step cycles" in b["sample"]
     f = bench.cpu_baseline_fused(4, 16, seed=1, budget_s=0.05)
     assert f["value"] > 0 and f["kind"] == "oracle" and "single-token" in f["sample"]
+
+
+def test_oracle_baselines_of_the_mamba_and_projection_lines():
+    m = bench.cpu_baseline_mamba(64, 16, seed=1, budget_s=0.05)
+    assert m["value"] > 0 and m["kind"] == "oracle" and "single-row" in m["sample"]
+    g = bench.cpu_baseline_gemv(2, 300, 128, seed=1, budget_s=0.05, rows=64)
+    assert g["value"] > 0 and "64 of the 300 weight rows" in g["sample"]
