@@ -42,6 +42,15 @@ MUTANTS = [
     ("silu as sigmoid", "double a = act == 0 ? gt * sigmoid(gt) : sigmoid(gt);",
      "double a = sigmoid(gt);"),
     ("per-key decay index", "decay_log[kk] : decay_log[0]", "decay_log[0] : decay_log[0]"),
+    ("kda form 1 without exp(A_log)", "val = lower_bound * sigmoid(exp(A_log[h]) * x);",
+     "val = lower_bound * sigmoid(x);"),
+    ("kda form 1 with head 0's A_log", "val = lower_bound * sigmoid(exp(A_log[h]) * x);",
+     "val = lower_bound * sigmoid(exp(A_log[0]) * x);"),
+    ("kda form 0 with head 0's A_log", "val = -exp(A_log[h]) * softplus(x);",
+     "val = -exp(A_log[0]) * softplus(x);"),
+    ("kda dt_bias per channel only", "double x = raw_g[o] + dt_bias[(size_t)h * D + d];",
+     "double x = raw_g[o] + dt_bias[d];"),
+    ("kda bound not applied", "if (val < lower_bound) val = lower_bound;", ";"),
     ("bf16 rounding by truncation", "return ldexp(nearbyint(ldexp(m, 8)), e - 8);",
      "return ldexp(trunc(ldexp(m, 8)), e - 8);"),
     ("mamba decay sign", "double dA = exp(dt[r] * A[(size_t)d * N + n]);", "double dA = exp(-dt[r] * A[(size_t)d * N + n]);"),

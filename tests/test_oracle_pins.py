@@ -114,6 +114,14 @@ def test_gdn_gates():
 
 
 def check_kda_gate_reading():
+    """The KDA microbenchmark page ("Microbenchmark for the fused Kimi-K3 KDA decode kernel on
+    ROCm", `Inputs`) names raw_g, A_log [heads], dt_bias [heads * D] and lower_bound = -5 but
+    prints no formula; the oracle implements two readings, each pinned here to its own formula:
+      form 0: g[t,h,d] = max(lb, -exp(A_log[h]) * softplus(raw_g[t,h,d] + dt_bias[h*D + d]))
+      form 1: g[t,h,d] = lb * sigmoid(exp(A_log[h]) * (raw_g[t,h,d] + dt_bias[h*D + d]))
+    Pins: both forms lie in [lb, 0] and do not increase with raw_g; form 1 at x = 0 is lb/2;
+    form 0 saturates at lb; form 0 with the bound inactive equals the GDN gate; closed values
+    where exp(A_log[h]) differs between heads and dt_bias between channels (below)."""
     T, heads, D = 2, 3, 8
     rng = np.random.default_rng(3)
     raw = rng.normal(0, 2, (T, heads, D)); A_log = rng.normal(0, 1, heads)
@@ -134,6 +142,23 @@ def check_kda_gate_reading():
     gk = oracle.kda_gate(small, np.array([0.1]), np.zeros(4), -5.0, 0)
     gg, _ = oracle.gdn_gates(small.reshape(4, 1), np.zeros((4, 1)), np.array([0.1]), np.zeros(1))
     assert rel_err(gk.reshape(4), gg.reshape(4)) < 1e-15
+    # Closed values with exp(A_log[h]) = 2 and 4 on two heads, so the scale on x matters and a
+    # head-0 lookup is visible. Form 1: x = ln(3)/2 split between raw_g and dt_bias gives
+    # sigmoid(2 x) = sigmoid(ln 3) = 3/4 and sigmoid(4 x) = sigmoid(2 ln 3) = 9/10.
+    A2 = np.array([math.log(2.0), math.log(4.0)])
+    x1 = math.log(3.0) / 2
+    raw1 = np.full((1, 2, 2), x1 / 4)
+    dtb1 = np.full(4, 3 * x1 / 4)
+    g1 = oracle.kda_gate(raw1, A2, dtb1, -5.0, 1)
+    assert np.max(np.abs(g1[0, 0] - (-5.0 * 0.75))) < 1e-14
+    assert np.max(np.abs(g1[0, 1] - (-5.0 * 0.9))) < 1e-14
+    # Form 0: dt_bias[h*D + d] = ln(e^c - 1) with a different c per channel makes
+    # softplus(0 + dt_bias) = c, so g = -exp(A_log[h]) * c (all above the bound).
+    c = 0.05 * np.arange(1, 5, dtype=np.float64)
+    dtb0 = np.log(np.expm1(c))
+    g0 = oracle.kda_gate(np.zeros((1, 2, 2)), A2, dtb0, -5.0, 0)
+    want0 = -np.array([[2.0 * c[0], 2.0 * c[1]], [4.0 * c[2], 4.0 * c[3]]])
+    assert np.max(np.abs(g0[0] - want0)) < 1e-14
 
 
 def test_kda_gate_reading():
