@@ -40,7 +40,8 @@ typedef struct gdn_gemv_args {
                                split count is above 8; unused (may be NULL) otherwise */
     size_t workspace_bytes;
     int32_t *err_flags;     /* optional device word; a kernel that gives up a bounded wait ORs
-                               GDN_DEVERR_TIMEOUT into it and leaves its outputs unwritten */
+                               GDN_DEVERR_TIMEOUT into it and leaves its outputs unwritten (with
+                               more than 8 K ranges: sets them to NaN) */
 } gdn_gemv_args;
 
 /* The split count gdn_gemv_bf16 uses when args->splits == 0: a power of two up to 8 (so no
@@ -60,9 +61,22 @@ size_t gdn_gemv_workspace_bytes(int32_t T, int32_t N, int32_t splits);
  * GDN_ERR_SHAPE (negative sizes, Kd not a multiple of 8, workspace too small, splits > 64),
  * GDN_ERR_DTYPE, GDN_ERR_ALIGN or GDN_ERR_LAUNCH. From 2 token rows on the library's tensor-core
  * kernel waits on mbarriers with a bound; a wait that gives up ORs GDN_DEVERR_TIMEOUT into
- * args->err_flags (when given) and leaves that CTA's outputs unwritten.
+ * args->err_flags (when given) and leaves that CTA's outputs of y unwritten, or, with more than 8
+ * K ranges (a workspace), writes NaN into its partial sums so that those outputs of y come out
+ * NaN rather than sums of stale workspace values.
  */
 int gdn_gemv_bf16(const gdn_gemv_args *args, gdn_stream_t stream);
+
+/*
+ * gdn_gemv_set_wait_limit -- test hook, not for production use: sets, for the whole process, the
+ * number of SM clock cycles after which a wait of the tensor-core projection (T >= 2) gives up;
+ * 0 restores the default (2^31 cycles, about one second). With a limit far below a copy's latency
+ * a test can make the waits run out and check that the call returns normally, reports
+ * GDN_DEVERR_TIMEOUT and leaves y unwritten or NaN; the waits that let copies and MMAs in flight
+ * finish after a give-up keep the default limit. Returns the previous setting. Launches nothing.
+ * No counterpart on the source pages.
+ */
+int64_t gdn_gemv_set_wait_limit(int64_t cycles);
 
 /* Size of the fixed buffer behind gdn_gemv_bf16_noalloc, in fp32 values (4 MiB). */
 #define GDN_GEMV_NOALLOC_MAX_FLOATS (1 << 20)
@@ -78,12 +92,17 @@ int gdn_gemv_bf16(const gdn_gemv_args *args, gdn_stream_t stream);
  * call needs a workspace (more than 8 K ranges), its fp32 partial sums go to a buffer of
  * GDN_GEMV_NOALLOC_MAX_FLOATS values that the library keeps on every GPU that loads it, until the
  * process exits. A call whose splits * T * N exceeds that size is rejected with GDN_ERR_SCRATCH
- * before anything is launched (pass 8 or fewer ranges, which need no buffer, or use gdn_gemv_bf16
- * with your own workspace). Nothing here allocates: the first call on a device that uses the
- * buffer looks up that device's buffer address (cudaGetSymbolAddress) with the device current, so
- * make that first call before any stream capture. Every call on a device shares the one buffer, which keeps the last call's
- * partial sums (each call writes all the sums it reads, so no clearing is needed); calls that can
- * run at the same time on the GPU, e.g. on two streams, race on it and must be ordered.
+ * before anything is launched, after the argument checks of gdn_gemv_bf16 (pass 8 or fewer
+ * ranges, which need no buffer, or use gdn_gemv_bf16 with your own workspace). Nothing here
+ * allocates: the first call in a CUDA context that uses the buffer looks up that context's buffer
+ * address (cudaGetSymbolAddress) with the device current, so make that first call before any
+ * stream capture. With lazy module loading (CUDA's default) that first lookup may also be what
+ * makes the driver load this library's device code, and with it the 4 MiB array, on that device;
+ * later calls change no device memory reservation. The address is remembered per context: after
+ * cudaDeviceReset (a new primary context) the next call looks it up again. Every call in a context
+ * shares the one buffer, which keeps the last call's partial sums (each call writes all the sums
+ * it reads, so no clearing is needed); calls that can run at the same time on the GPU, e.g. on two
+ * streams, race on it and must be ordered.
  * Returns the codes of gdn_gemv_bf16, and GDN_ERR_SCRATCH.
  */
 int gdn_gemv_bf16_noalloc(const gdn_gemv_args *args, gdn_stream_t stream);

@@ -45,7 +45,7 @@ EXPORTS = ("gdn_decode_step", "gdn_decode_step_indexed", "gdn_decode_buffered", 
            "gdn_strerror", "gdn_abi_struct_size", "gdn_abi_version", "mamba_selective_scan_decode",
            "gdn_selftest_bounded_wait", "gdn_gemv_bf16", "gdn_gemv_default_splits",
            "gdn_gemv_workspace_bytes", "gdn_gemv_bf16_noalloc", "gdn_decode_front",
-           "gdn_front_proj_width")
+           "gdn_front_proj_width", "gdn_gemv_set_wait_limit")
 
 _i32, _i64, _f32, _vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
 
@@ -139,6 +139,10 @@ def lib():
             L.gdn_gemv_default_splits.restype = _i32
             L.gdn_gemv_workspace_bytes.argtypes = [_i32, _i32, _i32]
             L.gdn_gemv_workspace_bytes.restype = ctypes.c_size_t
+            L.gdn_gemv_bf16_noalloc.argtypes = [ctypes.POINTER(GemvArgs), _vp]
+            L.gdn_gemv_bf16_noalloc.restype = ctypes.c_int
+            L.gdn_gemv_set_wait_limit.argtypes = [_i64]
+            L.gdn_gemv_set_wait_limit.restype = _i64
             L.gdn_selftest_bounded_wait.restype = ctypes.c_int
             for name in ("gdn_decode_step", "gdn_decode_step_indexed", "gdn_decode_buffered",
                          "gdn_decode_fused", "gdn_abi_version"):

@@ -19,12 +19,14 @@
 // the MMAs on one lane, warps 2 .. 5 (one per quarter of the tensor-memory lanes) are the epilogue.
 // Every mbarrier wait is bounded. A wait that gives up raises GDN_DEVERR_TIMEOUT and a CTA-wide
 // abort flag; the producer then waits (bounded) for its copies in flight, the MMA thread waits
-// (bounded) for the MMAs it issued, the CTA frees its tensor memory and writes no output.
+// (bounded) for the MMAs it issued, the CTA frees its tensor memory and writes no output (with a
+// workspace, it writes NaN into its partial-sum slots, so that the sums added later are NaN).
 //
 // Source: "Optimization Log: Qwen3.5-27B Dense on B200", Kernel 3 (BF16 GEMV with split-K).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 
@@ -45,6 +47,9 @@ constexpr uint32_t kTcBBytes = kTcTok * kTcK * 2;           // token tile, 2 KB
 constexpr uint32_t kTcStageBytes = kTcChunks * (kTcABytes + kTcBBytes);   // a multiple of 1024
 constexpr uint32_t kTcTmemCols = 32;                        // two 16-column accumulators
 constexpr long long kTcWaitLimit = 1LL << 31;               // SM clock cycles, about one second
+// The limit of the waits that can give up (0: kTcWaitLimit); set only by the test hook below. The
+// waits for copies and MMAs still in flight after a give-up always use kTcWaitLimit.
+std::atomic<long long> g_wait_limit{0};
 
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1), A and B bf16 (bits 7-9
 // and 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
@@ -130,7 +135,7 @@ __global__ void __launch_bounds__(kTcThreads) gemv_tc_kernel(const __grid_consta
                                                              const __grid_constant__ CUtensorMap wmap,
                                                              const __grid_constant__ CUtensorMap xmap, int t0, int nt,
                                                              int k_per_split, int stages, int mode,
-                                                             int prefetch_w)
+                                                             int prefetch_w, long long wait_limit)
 {
     extern __shared__ unsigned char tc_sm[];
     __shared__ __align__(8) uint64_t full[kTcMaxStages];    // stage filled (TMA bytes landed)
@@ -193,7 +198,7 @@ __global__ void __launch_bounds__(kTcThreads) gemv_tc_kernel(const __grid_consta
             for (; it < nk; ++it) {
                 const int s = it % stages;
                 const uint32_t ph = (uint32_t)(it / stages) & 1u;
-                if (it >= stages && !mbar_wait(&empty[s], ph ^ 1u, &abort_flag, kTcWaitLimit)) {
+                if (it >= stages && !mbar_wait(&empty[s], ph ^ 1u, &abort_flag, wait_limit)) {
                     *(volatile int *)&abort_flag = 1;
                     raise_flag(P.err_flags, GDN_DEVERR_TIMEOUT);
                     break;
@@ -224,7 +229,7 @@ __global__ void __launch_bounds__(kTcThreads) gemv_tc_kernel(const __grid_consta
             bool ok = true;
             for (int g = 0; g < ngroups && ok; ++g) {
                 const int buf = g & 1;
-                if (g >= 2 && !mbar_wait(&acc_empty[buf], (uint32_t)((g >> 1) - 1) & 1u, &abort_flag, kTcWaitLimit)) {
+                if (g >= 2 && !mbar_wait(&acc_empty[buf], (uint32_t)((g >> 1) - 1) & 1u, &abort_flag, wait_limit)) {
                     ok = false;
                     break;
                 }
@@ -234,7 +239,7 @@ __global__ void __launch_bounds__(kTcThreads) gemv_tc_kernel(const __grid_consta
                 for (int it = g * kTcGroupStages; it < it_end; ++it) {
                     const int s = it % stages;
                     const uint32_t ph = (uint32_t)(it / stages) & 1u;
-                    if (!mbar_wait(&full[s], ph, &abort_flag, kTcWaitLimit)) {
+                    if (!mbar_wait(&full[s], ph, &abort_flag, wait_limit)) {
                         ok = false;
                         break;
                     }
@@ -274,7 +279,7 @@ __global__ void __launch_bounds__(kTcThreads) gemv_tc_kernel(const __grid_consta
         bool ok = true;
         for (int g = 0; g < ngroups; ++g) {
             const int buf = g & 1;
-            if (!mbar_wait(&acc_full[buf], (uint32_t)(g >> 1) & 1u, &abort_flag, kTcWaitLimit)) ok = false;
+            if (!mbar_wait(&acc_full[buf], (uint32_t)(g >> 1) & 1u, &abort_flag, wait_limit)) ok = false;
             if (!__all_sync(0xFFFFFFFFu, ok)) {
                 ok = false;
                 break;
@@ -307,6 +312,10 @@ __global__ void __launch_bounds__(kTcThreads) gemv_tc_kernel(const __grid_consta
                 else
                     gemv_store(P, t0 + t, n, acc[t]);
             }
+        } else if (!ok && mode == kGemvReduceWorkspace && n < P.N) {
+            // The reduction kernel adds every range's slot; a range that gave up leaves NaN there
+            // (not the buffer's previous contents), so the affected outputs of y come out NaN.
+            for (int t = 0; t < nt; ++t) P.workspace[((size_t)split * P.T + t0 + t) * P.N + n] = __int_as_float(0x7fc00000);
         }
     }
     if (mode == kGemvReduceCluster) {
@@ -449,13 +458,20 @@ int gemv_tc_launch(const gdn_gemv_args &p, int splits, int k_per_split, int stag
     }
     if (chained) set_programmatic(attr[cfg.numAttrs++]);
     const int prefetch_w = chained && gemv_prefetch_fits(p) ? 1 : 0;
+    const long long limit_set = g_wait_limit.load(std::memory_order_relaxed);
+    const long long wait_limit = limit_set > 0 ? limit_set : kTcWaitLimit;
     for (int t0 = 0; t0 < p.T; t0 += kTcTok) {
         const int nt = p.T - t0 < kTcTok ? p.T - t0 : kTcTok;
         if (cudaLaunchKernelEx(&cfg, gemv_tc_kernel, p, wmap, xmap, t0, nt, k_per_split, stages, mode,
-                               prefetch_w) != cudaSuccess)
+                               prefetch_w, wait_limit) != cudaSuccess)
             return GDN_ERR_LAUNCH;
     }
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
 }
 
 }  // namespace gdn
+
+extern "C" int64_t gdn_gemv_set_wait_limit(int64_t cycles)
+{
+    return gdn::g_wait_limit.exchange(cycles > 0 ? cycles : 0);
+}

@@ -130,6 +130,41 @@ def test_gemv_checks():
         assert 1 <= L.gdn_gemv_default_splits(T, N, Kd) <= 8
 
 
+def test_gemv_noalloc_checks_arguments_before_its_buffer_size():
+    """gdn_gemv_bf16_noalloc returns gdn_gemv_bf16's codes for invalid calls, even when the
+    request would also exceed its fixed buffer; GDN_ERR_SCRATCH only for valid calls that do. All
+    of these return before any CUDA call."""
+    L = gdn.lib()
+    fn = L.gdn_gemv_bf16_noalloc
+    g = gdn.GemvArgs()
+    g.T, g.N, g.Kd, g.out_dtype = 8, 65536, 1024, 0     # 16 ranges: 8 Mi partial sums > 1 Mi
+    g.x, g.W, g.y, g.x_stride, g.y_stride = 1 << 40, 1 << 41, 1 << 42, 1024, 65536
+    g.splits = 65
+    assert fn(ctypes.byref(g), None) == -2               # splits > 64: a shape error
+    g.splits = -1
+    assert fn(ctypes.byref(g), None) == -2
+    g.splits = 16
+    g.x = None
+    assert fn(ctypes.byref(g), None) == -1               # a missing pointer
+    g.x = (1 << 40) + 8
+    assert fn(ctypes.byref(g), None) == -4               # misaligned x
+    g.x = 1 << 40
+    g.Kd = 1020
+    assert fn(ctypes.byref(g), None) == -2               # Kd not a multiple of 8
+    g.Kd = 1024
+    assert fn(ctypes.byref(g), None) == -7               # valid, but larger than the buffer
+    assert fn(None, None) == -1
+
+
+def test_gemv_wait_limit_hook_round_trips():
+    L = gdn.lib()
+    before = L.gdn_gemv_set_wait_limit(0)
+    assert before == 0
+    assert L.gdn_gemv_set_wait_limit(4096) == 0
+    assert L.gdn_gemv_set_wait_limit(-5) == 4096         # non-positive restores the default
+    assert L.gdn_gemv_set_wait_limit(0) == 0
+
+
 def test_empty_batch_launches_nothing():
     s = _valid_args()
     s.B = 0

@@ -80,3 +80,46 @@ def test_no_alloc_gemv_refuses_more_than_its_buffer():
     assert "scratch" in gdn.gdn_strerror(GDN_ERR_SCRATCH)
     # with one K range the call needs no buffer and runs
     assert _noalloc(x[:1], W[:1024], y[:1, :1024], splits=1) == 0
+
+
+def test_no_alloc_gemv_reserves_no_device_memory_after_its_first_call():
+    """The first call in a process may make the driver load this library's device code (with
+    lazy module loading) and so place the fixed buffer; a later call changes no device memory
+    reservation: the free bytes cudaMemGetInfo reports stay the same across it."""
+    T, N, Kd, splits = 4, 17408, 5120, 12
+    x, W = _inputs(T, N, Kd, 35)
+    y = torch.empty((T, N), device="cuda")
+    assert _noalloc(x, W, y, splits) == 0
+    torch.cuda.synchronize()
+    free_before, _ = torch.cuda.mem_get_info()
+    assert _noalloc(x, W, y, splits) == 0
+    torch.cuda.synchronize()
+    free_after, _ = torch.cuda.mem_get_info()
+    assert free_after == free_before
+
+
+def test_no_alloc_gemv_that_gives_up_a_wait_writes_nan_not_the_previous_sums():
+    """The shared buffer keeps the previous call's partial sums. When the tensor-core kernel gives
+    up a bounded wait (its limit cut to 64 cycles with the library's test hook), the affected
+    outputs must come out NaN, not sums of that previous call's contents."""
+    T, N, Kd, splits = 2, 5120, 17408, 16
+    x, W = _inputs(T, N, Kd, 36)
+    want = torch.empty((T, N), device="cuda")
+    assert _noalloc(x, W, want, splits) == 0      # fills the buffer with this call's sums
+    x2 = x * 2                                      # a different call: every sum doubles
+    L = gdn.lib()
+    y = torch.full((T, N), 7.0, device="cuda")
+    old = L.gdn_gemv_set_wait_limit(64)
+    try:
+        assert _noalloc(x2, W, y, splits) == 0
+        torch.cuda.synchronize()
+    finally:
+        L.gdn_gemv_set_wait_limit(old)
+    got, ref = y.cpu().numpy(), 2 * want.cpu().numpy()
+    done = np.abs(got - ref) <= 1e-5 * np.maximum(1.0, np.abs(ref))
+    assert np.all(done | np.isnan(got))
+    assert np.any(np.isnan(got))
+    # default limit: exact again
+    assert _noalloc(x2, W, y, splits) == 0
+    torch.cuda.synchronize()
+    assert rel_err(y.cpu().numpy(), ref) <= 1e-5
