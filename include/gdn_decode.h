@@ -70,6 +70,9 @@ typedef enum gdn_status {
 #define GDN_DEVERR_BAD_WRITE_POS 0x2  /* a ring cursor outside [0, L) */
 #define GDN_DEVERR_TIMEOUT 0x4        /* a bounded wait inside a pipelined kernel gave up; the CTA
                                          stopped early and its remaining rows were not computed */
+#define GDN_DEVERR_RANGE 0x8          /* debug build only (libgdn_decode_debug.so, compiled with
+                                         -DGDN_DEBUG): a kernel computed a global-memory index outside
+                                         the buffer its arguments describe; that access was skipped */
 
 /* Arguments of one decode step (all entry points but gdn_decode_fused). */
 typedef struct gdn_step_args {
@@ -191,6 +194,26 @@ int gdn_decode_step(const gdn_step_args *args, gdn_stream_t stream);
  */
 int gdn_decode_step_indexed(const gdn_step_args *args, const int32_t *cache_indices,
                             int32_t pad_slot_id, gdn_stream_t stream);
+
+/*
+ * gdn_decode_step_indexed_chained -- gdn_decode_step_indexed for the layers of a multi-layer
+ * decode (one call per layer, each with its own state pool, e.g. under one CUDA graph). The
+ * kernel is a programmatic dependent launch: it may start while the kernel before it on `stream`
+ * is still running, reads cache_indices and loads its state tiles, and waits for that kernel to
+ * complete before it reads q, k, v, the gate inputs or the gates and before it writes anything.
+ * Every other buffer may be that kernel's output. Because each chained kernel lets the next one
+ * start at once, a chained call may overlap any kernel of the run of consecutive chained calls
+ * before it: no kernel in that run may write this call's state tiles or cache_indices. Give every
+ * chained layer its own state pool, and make the first call of each step an ordinary call, so that
+ * two calls on the same pool are never in one run. The overlap takes one launch gap and the
+ * previous layer's tail off each layer. A bf16 state at K = V = 128 from four tiles per SM runs
+ * the ordinary kernel (no overlap). Arguments, results and status codes as for
+ * gdn_decode_step_indexed. Source: as gdn_decode_step_indexed; the layer loop is the model of
+ * "Optimization Log: Qwen3.5-27B Dense on B200" (decode is launch-bound at small batch, "Triton
+ * decode kernel + MBU analysis", Kernel design).
+ */
+int gdn_decode_step_indexed_chained(const gdn_step_args *args, const int32_t *cache_indices,
+                                    int32_t pad_slot_id, gdn_stream_t stream);
 
 /*
  * gdn_decode_buffered -- the buffered, output-only decode. The state pool holds checkpoints S_c.

@@ -17,6 +17,7 @@ of "Microbenchmark: buffered output-only GDN decode (ReplaySSM Part A)" (_bench_
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import threading
 
@@ -29,6 +30,7 @@ __all__ = [
     "MambaArgs", "mamba_selective_scan_decode", "gdn_selftest_bounded_wait",
     "GemvArgs", "gdn_gemv_bf16", "gemv_workspace",
     "GDN_F32", "GDN_BF16", "GDN_DEVERR_BAD_INDEX", "GDN_DEVERR_BAD_WRITE_POS", "GDN_DEVERR_TIMEOUT",
+    "GDN_DEVERR_RANGE", "debug_lib", "using_debug_build",
     "EXPORTS",
 ]
 
@@ -37,6 +39,7 @@ GDN_GATE_RAW, GDN_GATE_DIRECT = 0, 1
 GDN_FUSED_GATE_KDA, GDN_FUSED_GATE_GDN = 0, 1
 GDN_ACT_SILU, GDN_ACT_SIGMOID = 0, 1
 GDN_DEVERR_BAD_INDEX, GDN_DEVERR_BAD_WRITE_POS, GDN_DEVERR_TIMEOUT = 0x1, 0x2, 0x4
+GDN_DEVERR_RANGE = 0x8
 GDN_KERNEL = {"auto": 0, "tile": 1, "pipe": 2}
 ABI_VERSION = 6
 
@@ -45,7 +48,7 @@ EXPORTS = ("gdn_decode_step", "gdn_decode_step_indexed", "gdn_decode_buffered", 
            "gdn_strerror", "gdn_abi_struct_size", "gdn_abi_version", "mamba_selective_scan_decode",
            "gdn_selftest_bounded_wait", "gdn_gemv_bf16", "gdn_gemv_default_splits",
            "gdn_gemv_workspace_bytes", "gdn_gemv_bf16_noalloc", "gdn_decode_front",
-           "gdn_front_proj_width", "gdn_gemv_set_wait_limit")
+           "gdn_front_proj_width", "gdn_gemv_set_wait_limit", "gdn_decode_step_indexed_chained")
 
 _i32, _i64, _f32, _vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
 
@@ -113,51 +116,87 @@ def build(force: bool = False) -> str:
     return _build.build(force=force)
 
 
+def _load(path: str):
+    """Open one build of the library and declare its entry points' signatures."""
+    L = ctypes.CDLL(path)
+    for name in ("gdn_decode_step",):
+        getattr(L, name).argtypes = [ctypes.POINTER(GdnStepArgs), _vp]
+    L.gdn_decode_step_indexed.argtypes = [ctypes.POINTER(GdnStepArgs), _vp, _i32, _vp]
+    L.gdn_decode_step_indexed_chained.argtypes = [ctypes.POINTER(GdnStepArgs), _vp, _i32, _vp]
+    L.gdn_decode_buffered.argtypes = [ctypes.POINTER(GdnStepArgs), _vp, _i32,
+                                      ctypes.POINTER(GdnRingArgs), _vp]
+    L.gdn_decode_fused.argtypes = [ctypes.POINTER(GdnFusedArgs), _vp]
+    L.mamba_selective_scan_decode.argtypes = [ctypes.POINTER(MambaArgs), _vp]
+    L.mamba_selective_scan_decode.restype = ctypes.c_int
+    L.gdn_selftest_bounded_wait.argtypes = [_vp, _i64, _i32, _vp]
+    L.gdn_decode_front.argtypes = [ctypes.POINTER(GdnFrontArgs), _vp]
+    L.gdn_decode_front.restype = ctypes.c_int
+    L.gdn_front_proj_width.argtypes = [_i32, _i32, _i32]
+    L.gdn_front_proj_width.restype = _i64
+    L.gdn_gemv_bf16.argtypes = [ctypes.POINTER(GemvArgs), _vp]
+    L.gdn_gemv_bf16.restype = ctypes.c_int
+    L.gdn_gemv_default_splits.argtypes = [_i32, _i32, _i32]
+    L.gdn_gemv_default_splits.restype = _i32
+    L.gdn_gemv_workspace_bytes.argtypes = [_i32, _i32, _i32]
+    L.gdn_gemv_workspace_bytes.restype = ctypes.c_size_t
+    L.gdn_gemv_bf16_noalloc.argtypes = [ctypes.POINTER(GemvArgs), _vp]
+    L.gdn_gemv_bf16_noalloc.restype = ctypes.c_int
+    L.gdn_gemv_set_wait_limit.argtypes = [_i64]
+    L.gdn_gemv_set_wait_limit.restype = _i64
+    L.gdn_selftest_bounded_wait.restype = ctypes.c_int
+    for name in ("gdn_decode_step", "gdn_decode_step_indexed", "gdn_decode_buffered",
+                 "gdn_decode_fused", "gdn_abi_version", "gdn_decode_step_indexed_chained"):
+        getattr(L, name).restype = ctypes.c_int
+    L.gdn_strerror.argtypes = [ctypes.c_int]
+    L.gdn_strerror.restype = ctypes.c_char_p
+    L.gdn_abi_struct_size.argtypes = [ctypes.c_int]
+    L.gdn_abi_struct_size.restype = ctypes.c_size_t
+    sizes = [L.gdn_abi_struct_size(i) for i in range(5)]
+    want = [ctypes.sizeof(GdnStepArgs), ctypes.sizeof(GdnRingArgs), ctypes.sizeof(GdnFusedArgs),
+            ctypes.sizeof(GemvArgs), ctypes.sizeof(GdnFrontArgs)]
+    if sizes != want or L.gdn_abi_version() != ABI_VERSION:
+        raise RuntimeError(f"libgdn_decode.so ABI mismatch: struct sizes {sizes} vs {want}")
+    return L
+
+
 def lib():
     """The loaded library (built first if it is missing or stale)."""
     global _lib
     with _lock:
         if _lib is None:
-            path = _build.build()
-            L = ctypes.CDLL(path)
-            for name in ("gdn_decode_step",):
-                getattr(L, name).argtypes = [ctypes.POINTER(GdnStepArgs), _vp]
-            L.gdn_decode_step_indexed.argtypes = [ctypes.POINTER(GdnStepArgs), _vp, _i32, _vp]
-            L.gdn_decode_buffered.argtypes = [ctypes.POINTER(GdnStepArgs), _vp, _i32,
-                                              ctypes.POINTER(GdnRingArgs), _vp]
-            L.gdn_decode_fused.argtypes = [ctypes.POINTER(GdnFusedArgs), _vp]
-            L.mamba_selective_scan_decode.argtypes = [ctypes.POINTER(MambaArgs), _vp]
-            L.mamba_selective_scan_decode.restype = ctypes.c_int
-            L.gdn_selftest_bounded_wait.argtypes = [_vp, _i64, _i32, _vp]
-            L.gdn_decode_front.argtypes = [ctypes.POINTER(GdnFrontArgs), _vp]
-            L.gdn_decode_front.restype = ctypes.c_int
-            L.gdn_front_proj_width.argtypes = [_i32, _i32, _i32]
-            L.gdn_front_proj_width.restype = _i64
-            L.gdn_gemv_bf16.argtypes = [ctypes.POINTER(GemvArgs), _vp]
-            L.gdn_gemv_bf16.restype = ctypes.c_int
-            L.gdn_gemv_default_splits.argtypes = [_i32, _i32, _i32]
-            L.gdn_gemv_default_splits.restype = _i32
-            L.gdn_gemv_workspace_bytes.argtypes = [_i32, _i32, _i32]
-            L.gdn_gemv_workspace_bytes.restype = ctypes.c_size_t
-            L.gdn_gemv_bf16_noalloc.argtypes = [ctypes.POINTER(GemvArgs), _vp]
-            L.gdn_gemv_bf16_noalloc.restype = ctypes.c_int
-            L.gdn_gemv_set_wait_limit.argtypes = [_i64]
-            L.gdn_gemv_set_wait_limit.restype = _i64
-            L.gdn_selftest_bounded_wait.restype = ctypes.c_int
-            for name in ("gdn_decode_step", "gdn_decode_step_indexed", "gdn_decode_buffered",
-                         "gdn_decode_fused", "gdn_abi_version"):
-                getattr(L, name).restype = ctypes.c_int
-            L.gdn_strerror.argtypes = [ctypes.c_int]
-            L.gdn_strerror.restype = ctypes.c_char_p
-            L.gdn_abi_struct_size.argtypes = [ctypes.c_int]
-            L.gdn_abi_struct_size.restype = ctypes.c_size_t
-            sizes = [L.gdn_abi_struct_size(i) for i in range(5)]
-            want = [ctypes.sizeof(GdnStepArgs), ctypes.sizeof(GdnRingArgs), ctypes.sizeof(GdnFusedArgs),
-                    ctypes.sizeof(GemvArgs), ctypes.sizeof(GdnFrontArgs)]
-            if sizes != want or L.gdn_abi_version() != ABI_VERSION:
-                raise RuntimeError(f"libgdn_decode.so ABI mismatch: struct sizes {sizes} vs {want}")
-            _lib = L
+            _lib = _load(_build.build())
     return _lib
+
+
+_debug_lib = None
+
+
+@contextlib.contextmanager
+def using_debug_build():
+    """Inside the with-block every entry point of this module calls the index-checking debug
+    build (debug_lib) instead of the release library; prepared calls keep the library they were
+    made with. For tests."""
+    global _lib
+    L = debug_lib()
+    prev = lib()
+    with _lock:
+        _lib = L
+    try:
+        yield L
+    finally:
+        with _lock:
+            _lib = prev
+
+
+def debug_lib():
+    """The index-checking debug build, libgdn_decode_debug.so (built first if needed): the same
+    entry points, whose kernels report an out-of-range computed index through the error word
+    (GDN_DEVERR_RANGE) instead of making the access. For tests; not for timing."""
+    global _debug_lib
+    with _lock:
+        if _debug_lib is None:
+            _debug_lib = _load(_build.build(debug=True))
+    return _debug_lib
 
 
 def gdn_strerror(status: int) -> str:
@@ -310,14 +349,17 @@ def gdn_decode_step(q, k, v, state, out, *, H=None, a=None, b=None, A_log=None, 
 
 def gdn_decode_step_indexed(q, k, v, state, out, cache_indices, *, pad_slot_id=-1, H=None, a=None,
                             b=None, A_log=None, dt_bias=None, g=None, beta=None, scale=None,
-                            use_qk_l2norm=True, err_flags=None, stream=None, prepare=False):
+                            use_qk_l2norm=True, err_flags=None, chained=False, stream=None,
+                            prepare=False):
     """As gdn_decode_step, with row b on slot cache_indices[b] (int32 [B] on the device); rows
-    whose index is pad_slot_id are skipped (state untouched, out zeroed)."""
+    whose index is pad_slot_id are skipped (state untouched, out zeroed). chained=True calls
+    gdn_decode_step_indexed_chained (a layer of a multi-layer decode: the launch may overlap the
+    kernel before it on the stream, which must not write this call's state or cache_indices)."""
     torch = _torch()
     s = _step_args(q, k, v, state, out, H=H, a=a, b=b, A_log=A_log, dt_bias=dt_bias, g=g,
                    beta=beta, scale=scale, use_qk_l2norm=use_qk_l2norm, err_flags=err_flags)
     idx = _ptr(_dense(cache_indices, "cache_indices"), "cache_indices", torch.int32)
-    return _run_or_prepare("gdn_decode_step_indexed",
+    return _run_or_prepare("gdn_decode_step_indexed_chained" if chained else "gdn_decode_step_indexed",
                            (ctypes.byref(s), ctypes.c_void_p(idx), ctypes.c_int32(int(pad_slot_id))),
                            (s,), stream, prepare, out)
 

@@ -166,6 +166,16 @@ int gdn_decode_step_indexed(const gdn_step_args *args, const int32_t *cache_indi
                             reinterpret_cast<cudaStream_t>(stream));
 }
 
+int gdn_decode_step_indexed_chained(const gdn_step_args *args, const int32_t *cache_indices,
+                                    int32_t pad_slot_id, gdn_stream_t stream)
+{
+    int rc = check_step(args, true);
+    if (rc != GDN_OK || args->B == 0) return rc;
+    if (!cache_indices) return GDN_ERR_NULL;
+    return gdn::launch_step(make_step(args, cache_indices, pad_slot_id),
+                            reinterpret_cast<cudaStream_t>(stream), true);
+}
+
 int gdn_decode_buffered(const gdn_step_args *args, const int32_t *cache_indices,
                         int32_t pad_slot_id, const gdn_ring_args *ring, gdn_stream_t stream)
 {

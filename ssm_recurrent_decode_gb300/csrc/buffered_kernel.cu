@@ -64,6 +64,7 @@ __global__ void __launch_bounds__(kThreads, 2) buffered_kernel(const __grid_cons
         for (int r = threadIdx.x; r < V; r += kThreads) store_out(a.out, a.out_dtype, out_base + r, 0.f);
         return;
     }
+    if (!step_tile_in_range(a, b, hv, h, slot) || !ring_in_range(a, L, slot, hv, h, p)) return;   // debug build
     const bool flush = p == L - 1;
     float *S = static_cast<float *>(a.state) + ((size_t)slot * HV + hv) * (size_t)V * K;
 

@@ -39,7 +39,7 @@ constexpr long long kWaitLimit = 1LL << 31;           // SM clock cycles, about 
 // it is 16-byte aligned); status .. beta by the producer; c, alpha, gamma are consumer scratch.
 struct PipeMeta {
     float gr[kPipeLMax];        // log-decays of records j < p
-    int status;                 // 0 run, 1 pad row, 2 bad slot index, 3 bad cursor
+    int status;                 // 0 run, 1 pad row, 2 bad slot index, 3 bad cursor, 4 out of range (debug)
     int slot, p;
     float g, beta;              // this step's log-decay and beta
     float c[kPipeLMax];         // c_j = exp(g_{j+1} + ... + g_p)
@@ -142,6 +142,9 @@ __global__ void __launch_bounds__(kPipeThreads, 1) buffered_pipe_kernel(const __
                 }
                 my_p = P.write_pos[b];
                 if (my_status == 0 && (my_p < 0 || my_p >= L)) my_status = 3;
+                if (my_status == 0 && (!step_tile_in_range(a, b, hv, hv / G, my_slot) ||
+                                       !ring_in_range(a, L, my_slot, hv, hv / G, my_p)))
+                    my_status = 4;   // an index out of range (debug build): skipped, nothing written
                 if (my_status != 0) my_p = 0;
                 step_gates<Tin>(a, b, hv, my_g, my_beta);
             }
@@ -150,7 +153,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1) buffered_pipe_kernel(const __
                 if (tile >= ntiles) break;
                 const int st = n % NST;
                 const uint32_t ph = (uint32_t)(n / NST) & 1u;
-                if (n >= NST && !mbar_wait(&empty[st], ph ^ 1u, &abort_flag, kWaitLimit)) {
+                if (n >= NST && !mbar_wait_warp(&empty[st], ph ^ 1u, &abort_flag, kWaitLimit)) {
                     if (lane == 0) {
                         *(volatile int *)&abort_flag = 1;
                         raise_flag(a.err_flags, GDN_DEVERR_TIMEOUT);
@@ -220,8 +223,8 @@ __global__ void __launch_bounds__(kPipeThreads, 1) buffered_pipe_kernel(const __
         // other group still holds tile n - NST on the same stage. A parity wait can only tell
         // apart a phase from the one before it, so first wait for that earlier use to be released
         // (after which the stage's barriers are at most one phase away from tile n's).
-        if ((n >= NST && !mbar_wait(&empty[st], ph ^ 1u, &abort_flag, kWaitLimit)) ||
-            !mbar_wait(&full[st], ph, &abort_flag, kWaitLimit)) {
+        if ((n >= NST && !mbar_wait_warp(&empty[st], ph ^ 1u, &abort_flag, kWaitLimit)) ||
+            !mbar_wait_warp(&full[st], ph, &abort_flag, kWaitLimit)) {
             if (lane == 0) {
                 *(volatile int *)&abort_flag = 1;
                 raise_flag(a.err_flags, GDN_DEVERR_TIMEOUT);
@@ -234,9 +237,9 @@ __global__ void __launch_bounds__(kPipeThreads, 1) buffered_pipe_kernel(const __
         const int b = tile / HV, hv = tile - b * HV;
         const size_t out_base = ((size_t)b * HV + hv) * V;
         if (status != 0) {
-            if (status >= 2 && tid == 0)
+            if ((status == 2 || status == 3) && tid == 0)
                 raise_flag(a.err_flags, status == 2 ? GDN_DEVERR_BAD_INDEX : GDN_DEVERR_BAD_WRITE_POS);
-            if (tid < V) store_out(a.out, a.out_dtype, out_base + tid, 0.f);
+            if (status != 4 && tid < V) store_out(a.out, a.out_dtype, out_base + tid, 0.f);
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&scr[st]);
@@ -293,7 +296,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1) buffered_pipe_kernel(const __
         }
         t.reduce_scatter(x);
 
-        if (!mbar_wait(&scr[st], ph, &abort_flag, kWaitLimit)) {
+        if (!mbar_wait_warp(&scr[st], ph, &abort_flag, kWaitLimit)) {
             if (lane == 0) {
                 *(volatile int *)&abort_flag = 1;
                 raise_flag(a.err_flags, GDN_DEVERR_TIMEOUT);

@@ -47,13 +47,15 @@ __global__ void __launch_bounds__(kThreads, 2) fused_kernel(const __grid_constan
     if constexpr (CHAIN) grid_launch_dependents();
     const int slot = a.state_indices[t_];
     const bool skip = slot == a.pad_slot_id || slot < 0 || slot >= a.num_slots;   // uniform over the CTA
+    const bool out_of_range = !skip && !fused_tile_in_range(a, t_, h, slot);      // debug build only
     float *S = a.state + ((size_t)(skip ? 0 : slot) * heads + h) * (size_t)D * D;
     TL t;
     t.init();
-    if (!skip) t.load(S, D, 0);
+    if (!skip && !out_of_range) t.load(S, D, 0);
     // In a chained layer call the previous kernel (the input projection) writes x and the gate
     // rows, never the state or the slot indices: the state tile is already in flight here.
     if constexpr (CHAIN) grid_dependency_wait();
+    if (out_of_range) return;
     if (skip) {
         if (slot != a.pad_slot_id && threadIdx.x == 0) raise_flag(a.err_flags, GDN_DEVERR_BAD_INDEX);
         for (int r = threadIdx.x; r < D; r += kThreads) out[r] = __float2bfloat16_rn(0.f);

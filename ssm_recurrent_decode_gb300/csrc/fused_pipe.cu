@@ -29,7 +29,7 @@ constexpr int kFThreads = (kFCW + 1) * 32;
 constexpr long long kFWaitLimit = 1LL << 31;  // SM clock cycles, about one second
 
 struct FusedMeta {
-    int status;       // 0 run, 1 pad row, 2 bad slot
+    int status;       // 0 run, 1 pad row, 2 bad slot, 3 an index out of range (debug build)
     int slot;
     float beta;
     float g_head;     // GDN gate: the head's log-decay
@@ -104,6 +104,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_pipe_kernel(const __grid_c
                 const int t = my_tile / heads, h = my_tile - t * heads;
                 my_slot = a.state_indices[t];
                 my_status = my_slot == a.pad_slot_id ? 1 : (my_slot < 0 || my_slot >= a.num_slots) ? 2 : 0;
+                if (my_status == 0 && !fused_tile_in_range(a, t, h, my_slot)) my_status = 3;   // debug build
                 my_beta = sigmoid_f(__bfloat162float(static_cast<const bf16 *>(a.raw_beta)[(size_t)t * a.raw_beta_stride + h]));
                 my_A = expf(a.A_log[h]);
                 if (a.gate_kind == GDN_FUSED_GATE_GDN)
@@ -114,7 +115,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_pipe_kernel(const __grid_c
                 if (tile >= ntiles) break;
                 const int st = n % NST;
                 const uint32_t ph = (uint32_t)(n / NST) & 1u;
-                if (n >= NST && !mbar_wait(&empty[st], ph ^ 1u, &abort_flag, kFWaitLimit)) {
+                if (n >= NST && !mbar_wait_warp(&empty[st], ph ^ 1u, &abort_flag, kFWaitLimit)) {
                     if (lane == 0) {
                         *(volatile int *)&abort_flag = 1;
                         raise_flag(a.err_flags, GDN_DEVERR_TIMEOUT);
@@ -212,8 +213,8 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_pipe_kernel(const __grid_c
         const int st = n % NST;
         const uint32_t ph = (uint32_t)(n / NST) & 1u;
         // wait for the previous use of the stage to be released first (the groups alternate)
-        if ((n >= NST && !mbar_wait(&empty[st], ph ^ 1u, &abort_flag, kFWaitLimit)) ||
-            !mbar_wait(&full[st], ph, &abort_flag, kFWaitLimit)) {
+        if ((n >= NST && !mbar_wait_warp(&empty[st], ph ^ 1u, &abort_flag, kFWaitLimit)) ||
+            !mbar_wait_warp(&full[st], ph, &abort_flag, kFWaitLimit)) {
             if (lane == 0) {
                 *(volatile int *)&abort_flag = 1;
                 raise_flag(a.err_flags, GDN_DEVERR_TIMEOUT);
@@ -227,7 +228,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_pipe_kernel(const __grid_c
         bf16 *out = static_cast<bf16 *>(a.out) + ((size_t)tt * heads + h) * D;
         if (status != 0) {
             if (status == 2 && tid == 0) raise_flag(a.err_flags, GDN_DEVERR_BAD_INDEX);
-            if (tid < D) out[tid] = __float2bfloat16_rn(0.f);
+            if (status != 3 && tid < D) out[tid] = __float2bfloat16_rn(0.f);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[st]);
             continue;
@@ -288,7 +289,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_pipe_kernel(const __grid_c
         float gate[2];
 #pragma unroll
         for (int c = 0; c < 2; ++c) gate[c] = bfs(stage, FL::og, row0 + 8 * c + rsub);
-        if (!mbar_wait(&gbar[group][0], gp, &abort_flag, kFWaitLimit)) {
+        if (!mbar_wait_warp(&gbar[group][0], gp, &abort_flag, kFWaitLimit)) {
             if (lane == 0) {
                 *(volatile int *)&abort_flag = 1;
                 raise_flag(a.err_flags, GDN_DEVERR_TIMEOUT);
@@ -349,7 +350,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_pipe_kernel(const __grid_c
             mbar_arrive(&empty[st]);
             mbar_arrive(&gbar[group][1]);
         }
-        if (!mbar_wait(&gbar[group][1], gp, &abort_flag, kFWaitLimit)) {
+        if (!mbar_wait_warp(&gbar[group][1], gp, &abort_flag, kFWaitLimit)) {
             if (lane == 0) {
                 *(volatile int *)&abort_flag = 1;
                 raise_flag(a.err_flags, GDN_DEVERR_TIMEOUT);

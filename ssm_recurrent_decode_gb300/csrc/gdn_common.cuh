@@ -5,6 +5,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "gdn_decode.h"
+
 namespace gdn {
 
 using bf16 = __nv_bfloat16;
@@ -121,5 +123,22 @@ __device__ __forceinline__ void raise_flag(int32_t *err, int32_t bit)
 {
     if (err) atomicOr(err, bit);
 }
+
+// ---------------------------------------------------------------------------------------------
+// index checks of the debug build (-DGDN_DEBUG): GDN_IN(err, i, n) is true when 0 <= i < n;
+// otherwise it ORs GDN_DEVERR_RANGE into err and is false, and the caller skips the access. In
+// the release build it is the constant true and costs nothing.
+// ---------------------------------------------------------------------------------------------
+#ifdef GDN_DEBUG
+__device__ __forceinline__ bool index_in_range(int32_t *err, long long i, long long n)
+{
+    if (i >= 0 && i < n) return true;
+    raise_flag(err, GDN_DEVERR_RANGE);
+    return false;
+}
+#define GDN_IN(err, i, n) (::gdn::index_in_range((err), (long long)(i), (long long)(n)))
+#else
+#define GDN_IN(err, i, n) (true)
+#endif
 
 }  // namespace gdn

@@ -47,9 +47,16 @@ int launch_fused_plan(const FusedPlan &plan, cudaStream_t stream, bool chained =
 
 // Host launchers, one per kernel family; each dispatches on K and the dtypes. They return
 // GDN_OK or GDN_ERR_LAUNCH / GDN_ERR_SHAPE and never synchronise.
-int launch_step(const StepLaunch &p, cudaStream_t stream);
+// launch_step with chained: the row kernels run their chained instance as a programmatic
+// dependent launch (gdn_decode_step_indexed_chained); the bf16-state kernels launch as usual.
+int launch_step(const StepLaunch &p, cudaStream_t stream, bool chained = false);
 int launch_buffered(const StepLaunch &p, int ring_dtype, cudaStream_t stream);
 int launch_fused(const FusedLaunch &p, cudaStream_t stream, bool chained = false);
+
+// The persistent, warp-specialised step for a bf16 state at K = V = 128, and whether a call
+// qualifies for it (bf16 state, K = V = 128, 16-byte aligned state and q/k/v rows).
+bool step_pipe_bf16_ok(const gdn_step_args &a);
+int launch_step_pipe_bf16(const StepLaunch &p, cudaStream_t stream);
 
 // Dynamic shared memory the buffered kernel needs for ring length L, value dim V and key dim K.
 size_t buffered_smem_bytes(int L, int V, int K);

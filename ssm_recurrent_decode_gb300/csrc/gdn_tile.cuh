@@ -156,6 +156,60 @@ __device__ __forceinline__ void store_out(void *out, int dtype, size_t i, float 
         static_cast<float *>(out)[i] = x;
 }
 
+// Debug build: the buffers one step tile (request row b, value head hv, q/k head h, state slot)
+// reads and writes lie inside the extents its arguments describe: the state tile, the q, k and v
+// rows, the gate inputs and the output row. A failed check has raised GDN_DEVERR_RANGE and the
+// caller skips the tile. The release build compiles this to the constant true.
+__device__ __forceinline__ bool step_tile_in_range(const gdn_step_args &a, int b, int hv, int h, int slot)
+{
+    const long long VK = (long long)a.V * a.K, B1 = (long long)a.B - 1;
+    bool ok = GDN_IN(a.err_flags, ((long long)slot * a.HV + hv) * VK + VK - 1, (long long)a.num_slots * a.HV * VK);
+    ok = ok && GDN_IN(a.err_flags, (long long)b * a.q_stride + (long long)(h + 1) * a.K - 1, B1 * a.q_stride + (long long)a.H * a.K);
+    ok = ok && GDN_IN(a.err_flags, (long long)b * a.k_stride + (long long)(h + 1) * a.K - 1, B1 * a.k_stride + (long long)a.H * a.K);
+    ok = ok && GDN_IN(a.err_flags, (long long)b * a.v_stride + (long long)(hv + 1) * a.V - 1, B1 * a.v_stride + (long long)a.HV * a.V);
+    ok = ok && GDN_IN(a.err_flags, (long long)b * a.HV + hv, (long long)a.B * a.HV);
+    ok = ok && GDN_IN(a.err_flags, ((long long)b * a.HV + hv + 1) * a.V - 1, (long long)a.B * a.HV * a.V);
+    return ok;
+}
+
+// Debug build: the ring records of a tile at cursor p lie inside the rings (d_cache [slots, HV,
+// L, V], k_cache [slots, H, L, K], g_cache [slots, HV, L]).
+__device__ __forceinline__ bool ring_in_range(const gdn_step_args &a, int L, int slot, int hv, int h, int p)
+{
+    bool ok = GDN_IN(a.err_flags, p, L);
+    ok = ok && GDN_IN(a.err_flags, (((long long)slot * a.HV + hv) * L + p + 1) * a.V - 1, (long long)a.num_slots * a.HV * L * a.V);
+    ok = ok && GDN_IN(a.err_flags, (((long long)slot * a.H + h) * L + p + 1) * a.K - 1, (long long)a.num_slots * a.H * L * a.K);
+    ok = ok && GDN_IN(a.err_flags, ((long long)slot * a.HV + hv) * L + p, (long long)a.num_slots * a.HV * L);
+    return ok;
+}
+
+// Debug build: the buffers one fused tile (token t, head h, slot) reads and writes lie inside the
+// extents its arguments describe: the state tile, the conv state of the head's q, k and v channels
+// (all three taps), the x row, the output gate, raw_g, raw_beta, dt_bias and the output row.
+__device__ __forceinline__ bool fused_tile_in_range(const gdn_fused_args &a, int t, int h, int slot)
+{
+    const long long D = a.head_dim, dim = (long long)a.heads * D, T1 = (long long)a.T - 1;
+    bool ok = GDN_IN(a.err_flags, (((long long)slot * a.heads + h + 1) * D) * D - 1, (long long)a.num_slots * a.heads * D * D);
+    const long long cs_end = (long long)(a.num_slots - 1) * a.cs_stride_slot + (3 * dim - 1) * a.cs_stride_chan +
+                             2 * a.cs_stride_tap + 1;
+    for (int part = 0; part < 3; ++part) {
+        const long long c0 = part * dim + (long long)h * D;
+        ok = ok && GDN_IN(a.err_flags, slot * a.cs_stride_slot + c0 * a.cs_stride_chan, cs_end);
+        ok = ok && GDN_IN(a.err_flags, slot * a.cs_stride_slot + (c0 + D - 1) * a.cs_stride_chan + 2 * a.cs_stride_tap, cs_end);
+    }
+    ok = ok && GDN_IN(a.err_flags, t * a.x_stride + 2 * dim + (h + 1) * D - 1, T1 * a.x_stride + 3 * dim);
+    ok = ok && GDN_IN(a.err_flags, t * a.out_gate_stride + (h + 1) * D - 1, T1 * a.out_gate_stride + dim);
+    ok = ok && GDN_IN(a.err_flags, t * a.raw_beta_stride + h, T1 * a.raw_beta_stride + a.heads);
+    if (a.gate_kind == GDN_FUSED_GATE_KDA) {
+        ok = ok && GDN_IN(a.err_flags, t * a.raw_g_stride + (h + 1) * D - 1, T1 * a.raw_g_stride + dim);
+        ok = ok && GDN_IN(a.err_flags, (h + 1) * D - 1, dim);
+    } else {
+        ok = ok && GDN_IN(a.err_flags, t * a.raw_g_stride + h, T1 * a.raw_g_stride + a.heads);
+    }
+    ok = ok && GDN_IN(a.err_flags, ((long long)t * a.heads + h + 1) * D - 1, (long long)a.T * dim);
+    return ok;
+}
+
 // g = -exp(A_log) softplus(a + dt_bias), beta = sigmoid(b) (raw mode) or the given values
 template <typename Tin>
 __device__ __forceinline__ void step_gates(const gdn_step_args &a, int b, int hv, float &g,

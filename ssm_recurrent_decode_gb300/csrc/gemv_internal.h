@@ -7,6 +7,7 @@
 
 #include <cstddef>
 
+#include "gdn_common.cuh"
 #include "gdn_gemv.h"
 
 namespace gdn {
@@ -25,9 +26,22 @@ inline int gemv_reduce_mode(int splits)
     return splits <= 1 ? kGemvReduceNone : (splits <= kGemvMaxCluster ? kGemvReduceCluster : kGemvReduceWorkspace);
 }
 
+// Debug build: y[t, n] and the workspace slot (split, t, n) lie inside y [T, y_stride] and the
+// workspace the arguments describe (GDN_IN of gdn_common.cuh; the constant true in release).
+__device__ __forceinline__ bool gemv_y_in_range(const gdn_gemv_args &P, int t, int n)
+{
+    return GDN_IN(P.err_flags, (long long)t * P.y_stride + n, (long long)(P.T - 1) * P.y_stride + P.N) &&
+           GDN_IN(P.err_flags, n, P.N);
+}
+__device__ __forceinline__ bool gemv_ws_in_range(const gdn_gemv_args &P, long long i)
+{
+    return GDN_IN(P.err_flags, i, (long long)(P.workspace_bytes / 4));
+}
+
 // y[t, n] = v, rounded to y's dtype
 __device__ __forceinline__ void gemv_store(const gdn_gemv_args &P, int t, int n, float v)
 {
+    if (!gemv_y_in_range(P, t, n)) return;   // debug build only
     if (P.out_dtype == GDN_BF16)
         static_cast<__nv_bfloat16 *>(P.y)[(size_t)t * P.y_stride + n] = __float2bfloat16_rn(v);
     else

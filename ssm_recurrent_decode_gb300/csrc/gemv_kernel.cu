@@ -186,10 +186,12 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const __grid_constan
     if (lane >= kRows * TOK || n0 >= P.N) return;
     const int r = lane / TOK, t = lane - r * TOK, n = n0 + r;
     if (t >= nt || n >= P.N) return;
-    if (mode == kGemvReduceWorkspace)
-        P.workspace[((size_t)split * P.T + t0 + t) * P.N + n] = sum;
-    else
+    if (mode == kGemvReduceWorkspace) {
+        const size_t wi = ((size_t)split * P.T + t0 + t) * P.N + n;
+        if (gemv_ws_in_range(P, (long long)wi)) P.workspace[wi] = sum;   // (range: debug build)
+    } else {
         gemv_store(P, t0 + t, n, sum);
+    }
 }
 
 // y[t, n] = sum over the splits, in order
@@ -198,12 +200,10 @@ __global__ void gemv_reduce_kernel(const __grid_constant__ gdn_gemv_args P, int 
     const long long total = (long long)P.T * P.N;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total; i += (long long)gridDim.x * blockDim.x) {
         float s = 0.f;
-        for (int j = 0; j < splits; ++j) s += P.workspace[(size_t)j * total + i];
+        for (int j = 0; j < splits; ++j)
+            if (gemv_ws_in_range(P, (long long)j * total + i)) s += P.workspace[(size_t)j * total + i];
         const int t = (int)(i / P.N), n = (int)(i - (long long)t * P.N);
-        if (P.out_dtype == GDN_BF16)
-            static_cast<bf16 *>(P.y)[(size_t)t * P.y_stride + n] = __float2bfloat16_rn(s);
-        else
-            static_cast<float *>(P.y)[(size_t)t * P.y_stride + n] = s;
+        gemv_store(P, t, n, s);
     }
 }
 

@@ -307,15 +307,20 @@ __global__ void __launch_bounds__(kTcThreads) gemv_tc_kernel(const __grid_consta
 #pragma unroll
             for (int t = 0; t < kTcTok; ++t) {
                 if (t >= nt) break;
-                if (mode == kGemvReduceWorkspace)
-                    P.workspace[((size_t)split * P.T + t0 + t) * P.N + n] = acc[t];
-                else
+                if (mode == kGemvReduceWorkspace) {
+                    const size_t wi = ((size_t)split * P.T + t0 + t) * P.N + n;
+                    if (gemv_ws_in_range(P, (long long)wi)) P.workspace[wi] = acc[t];   // (range: debug build)
+                } else {
                     gemv_store(P, t0 + t, n, acc[t]);
+                }
             }
         } else if (!ok && mode == kGemvReduceWorkspace && n < P.N) {
             // The reduction kernel adds every range's slot; a range that gave up leaves NaN there
             // (not the buffer's previous contents), so the affected outputs of y come out NaN.
-            for (int t = 0; t < nt; ++t) P.workspace[((size_t)split * P.T + t0 + t) * P.N + n] = __int_as_float(0x7fc00000);
+            for (int t = 0; t < nt; ++t) {
+                const size_t wi = ((size_t)split * P.T + t0 + t) * P.N + n;
+                if (gemv_ws_in_range(P, (long long)wi)) P.workspace[wi] = __int_as_float(0x7fc00000);
+            }
         }
     }
     if (mode == kGemvReduceCluster) {

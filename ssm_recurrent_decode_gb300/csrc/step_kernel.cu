@@ -17,6 +17,7 @@
 // A)", _bench_cfg / run_packed (packed mixed_qkv, gates from a, b, A_log, dt_bias, in-kernel q/k
 // L2 norm with scale K^-1/2, ssm_state_indices, state [num_slots, HV, V, K] updated in place,
 // out [B, 1, HV, V]); _state_bytes_per_step (k [H, K] shared across HV // H value heads).
+#include "gdn_chain.cuh"
 #include "gdn_launch.h"
 #include "gdn_tile.cuh"
 
@@ -26,7 +27,13 @@ namespace gdn {
 // than 128); R = 8, 4 or 2 split a tile's rows over `splits` CTAs (R = 8 at K = 128 with an fp32
 // state, and smaller R for batches with too few tiles to fill the GPU). Row dots are complete within a row, so the
 // split needs no exchange between CTAs; each CTA normalises q and k itself.
-template <int K, typename Tin, typename TS, int R>
+//
+// CHAIN: the instance behind gdn_decode_step_indexed_chained, launched as a programmatic dependent
+// launch (a layer of a multi-layer graph). It lets the next kernel start its CTAs at once, reads
+// the slot index and issues its state loads, and only then waits for the kernel before it on the
+// stream to complete; every other input is read, and every output written, after that wait. The
+// ordinary instance has no wait: a wait after outstanding loads slowed ordinary launches.
+template <int K, typename Tin, typename TS, int R, bool CHAIN>
 __global__ void __launch_bounds__(kThreads, R >= 16 ? 2 : 4) step_kernel(const __grid_constant__ StepLaunch P, int splits)
 {
     using TL = Tile<K, R>;
@@ -36,23 +43,27 @@ __global__ void __launch_bounds__(kThreads, R >= 16 ? 2 : 4) step_kernel(const _
     const int b = tile / HV, hv = tile - b * HV, h = hv / P.G;
     const size_t out_base = ((size_t)b * HV + hv) * V;
     const int first_row = blk * TL::ROWS_PASS, row_step = splits * TL::ROWS_PASS;
+    if constexpr (CHAIN) grid_launch_dependents();
 
     int slot = b;
     if (P.idx) {
         slot = P.idx[b];
         const bool pad = slot == P.pad;
         if (pad || slot < 0 || slot >= a.num_slots) {   // uniform over the CTA
+            if constexpr (CHAIN) grid_dependency_wait();
             if (!pad && blk == 0 && threadIdx.x == 0) raise_flag(a.err_flags, GDN_DEVERR_BAD_INDEX);
             for (int r = threadIdx.x; r < V; r += kThreads)
                 if ((r / TL::ROWS_PASS) % splits == blk) store_out(a.out, a.out_dtype, out_base + r, 0.f);
             return;
         }
     }
+    if (!step_tile_in_range(a, b, hv, h, slot)) return;   // debug build only
     TS *S = static_cast<TS *>(a.state) + ((size_t)slot * HV + hv) * (size_t)V * K;
 
     TL t;
     t.init();
     t.load(S, V, first_row);   // the tile's loads go out first; everything below overlaps them
+    if constexpr (CHAIN) grid_dependency_wait();
 
     const Tin *qp = static_cast<const Tin *>(a.q) + (size_t)b * a.q_stride + (size_t)h * K;
     const Tin *kp = static_cast<const Tin *>(a.k) + (size_t)b * a.k_stride + (size_t)h * K;
@@ -141,7 +152,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) step_kernel_bf16(co
                     skip = true;
                 }
             }
-            if (!skip) {
+            if (!skip && step_tile_in_range(a, b, hv, hv / P.G, slot)) {   // (range: debug build)
                 run[u] = true;
                 slots[u] = slot;
                 const bf16 *S = static_cast<const bf16 *>(a.state) + ((size_t)slot * HV + hv) * (size_t)V * K;
@@ -213,14 +224,26 @@ static int sm_count()
 }
 
 template <int K, typename Tin, typename TS, int R>
-static void launch_rows(const StepLaunch &p, unsigned tiles, cudaStream_t stream)
+static void launch_rows(const StepLaunch &p, unsigned tiles, cudaStream_t stream, bool chained)
 {
     const int splits = R >= 16 ? 1 : (p.a.V + Tile<K, R>::ROWS_PASS - 1) / Tile<K, R>::ROWS_PASS;
-    step_kernel<K, Tin, TS, R><<<tiles * (unsigned)splits, kThreads, 0, stream>>>(p, splits);
+    if (!chained) {
+        step_kernel<K, Tin, TS, R, false><<<tiles * (unsigned)splits, kThreads, 0, stream>>>(p, splits);
+        return;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    set_programmatic(attr[0]);
+    cfg.gridDim = dim3(tiles * (unsigned)splits);
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, step_kernel<K, Tin, TS, R, true>, p, splits);
 }
 
 template <int K, typename Tin, typename TS>
-static int launch_step_t(const StepLaunch &p, cudaStream_t stream)
+static int launch_step_t(const StepLaunch &p, cudaStream_t stream, bool chained)
 {
     const unsigned tiles = (unsigned)p.a.B * (unsigned)p.a.HV;
     // Enough CTAs to cover every SM about four times over: whole tiles when the batch allows it,
@@ -231,8 +254,13 @@ static int launch_step_t(const StepLaunch &p, cudaStream_t stream)
     // measured faster than whole-tile CTAs at every batch size on GB300 (156.1 against 157.4 us at
     // B = 256, 22.6 against 24.0 at B = 32)
     if (sizeof(TS) == 4 && K == 128 && ctas(Tile<K, 8>::ROWS_PASS) >= target) {
-        launch_rows<K, Tin, TS, 8>(p, tiles, stream);
+        launch_rows<K, Tin, TS, 8>(p, tiles, stream, chained);
         return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
+    }
+    if constexpr (sizeof(TS) == 2 && K == 128) {
+        // bf16 state at K = V = 128: tiles staged through shared memory by a persistent kernel
+        // (step_pipe_bf16.cu) once every SM has several tiles
+        if (tiles >= target && step_pipe_bf16_ok(p.a)) return launch_step_pipe_bf16(p, stream);
     }
     if (tiles >= target) {
         bool paired = false;
@@ -242,34 +270,36 @@ static int launch_step_t(const StepLaunch &p, cudaStream_t stream)
                 paired = true;
             }
         }
-        if (!paired) launch_rows<K, Tin, TS, 16>(p, tiles, stream);
+        if (!paired) launch_rows<K, Tin, TS, 16>(p, tiles, stream, chained);
     } else if (ctas(Tile<K, 8>::ROWS_PASS) >= target) {
-        launch_rows<K, Tin, TS, 8>(p, tiles, stream);
+        launch_rows<K, Tin, TS, 8>(p, tiles, stream, chained);
     } else if (ctas(Tile<K, 4>::ROWS_PASS) >= target) {
-        launch_rows<K, Tin, TS, 4>(p, tiles, stream);
+        launch_rows<K, Tin, TS, 4>(p, tiles, stream, chained);
     } else {
-        launch_rows<K, Tin, TS, 2>(p, tiles, stream);
+        launch_rows<K, Tin, TS, 2>(p, tiles, stream, chained);
     }
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
 }
 
 template <typename Tin, typename TS>
-static int launch_step_k(const StepLaunch &p, cudaStream_t stream)
+static int launch_step_k(const StepLaunch &p, cudaStream_t stream, bool chained)
 {
     switch (p.a.K) {
-    case 16: return launch_step_t<16, Tin, TS>(p, stream);
-    case 32: return launch_step_t<32, Tin, TS>(p, stream);
-    case 64: return launch_step_t<64, Tin, TS>(p, stream);
-    case 128: return launch_step_t<128, Tin, TS>(p, stream);
+    case 16: return launch_step_t<16, Tin, TS>(p, stream, chained);
+    case 32: return launch_step_t<32, Tin, TS>(p, stream, chained);
+    case 64: return launch_step_t<64, Tin, TS>(p, stream, chained);
+    case 128: return launch_step_t<128, Tin, TS>(p, stream, chained);
     default: return GDN_ERR_SHAPE;
     }
 }
 
-int launch_step(const StepLaunch &p, cudaStream_t stream)
+int launch_step(const StepLaunch &p, cudaStream_t stream, bool chained)
 {
     if (p.a.state_dtype == GDN_BF16)
-        return p.a.in_dtype == GDN_BF16 ? launch_step_k<bf16, bf16>(p, stream) : launch_step_k<float, bf16>(p, stream);
-    return p.a.in_dtype == GDN_BF16 ? launch_step_k<bf16, float>(p, stream) : launch_step_k<float, float>(p, stream);
+        return p.a.in_dtype == GDN_BF16 ? launch_step_k<bf16, bf16>(p, stream, chained)
+                                        : launch_step_k<float, bf16>(p, stream, chained);
+    return p.a.in_dtype == GDN_BF16 ? launch_step_k<bf16, float>(p, stream, chained)
+                                    : launch_step_k<float, float>(p, stream, chained);
 }
 
 }  // namespace gdn

@@ -255,3 +255,27 @@ def test_guard_helper_detects_a_write_into_the_band():
     assert g.intact()
     g.raw[GUARD + 64] = 0
     assert not g.intact()
+
+
+# ------------------------------------------------------------------------------------------------
+# Mamba-1 decode (the second recurrence)
+# ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("B,D,N,in_place", [(3, 96, 64, True), (5, 40, 16, False), (2, 33, 48, True),
+                                            (4, 64, 128, False)])
+def test_mamba_writes_only_its_buffers(B, D, N, in_place):
+    m = syn.mamba_inputs(B, D, N, "f32", 900 + N)
+    t = {k: torch.from_numpy(np.ascontiguousarray(v)).cuda() for k, v in m.items()}
+    y0 = torch.full((B, D), 3.0, device="cuda")
+    h_out0 = torch.full((B, D, N), 3.0, device="cuda")
+
+    def call(h, y, h_out):
+        gdn.mamba_selective_scan_decode(t["x"], t["dt"], t["A"], t["Bm"], t["Cm"], h, y, Dskip=t["Dskip"],
+                                        z=t["z"], h_out=None if in_place else h_out)
+
+    plain = [t["h"].clone(), y0.clone(), h_out0.clone()]
+    call(*plain)
+    g = [Guarded(x_) for x_ in (t["h"], y0, h_out0)]
+    call(*(x_.t for x_ in g))
+    assert all(x_.intact() for x_ in g)
+    for x_, p in zip(g, plain):
+        assert _same(x_.t, p)

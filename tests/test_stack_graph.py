@@ -9,10 +9,13 @@ import bench
 pytestmark = pytest.mark.gpu
 
 
-def test_stacked_graph_decode_matches_the_oracle():
+@pytest.mark.parametrize("chained", [True, False])
+def test_stacked_graph_decode_matches_the_oracle(chained):
+    """Chained: layers after the first go through gdn_decode_step_indexed_chained (programmatic
+    dependent launches that overlap the previous layer); unchained: ordinary launches."""
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
     res = bench.stack_decode(layers=3, B=16, H=4, HV=12, K=128, V=128, steps=60, seed=77, pairs=3,
-                             heads_per_pair=1)
+                             heads_per_pair=1, chained=chained)
     assert res["drift"] <= 1e-4, res
     assert res["last_out_err"] <= 2e-2, res
     assert res["dec_ms_per_step"] > 0
