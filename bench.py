@@ -75,6 +75,8 @@ def kernel_sources_hash(files) -> str:
 KERNEL_FILES = {
     "step": ["ssm_recurrent_decode_gb300/csrc/step_kernel.cu", "ssm_recurrent_decode_gb300/csrc/gdn_tile.cuh",
              "ssm_recurrent_decode_gb300/csrc/gdn_common.cuh"],
+    "step_bf16": ["ssm_recurrent_decode_gb300/csrc/step_pipe_bf16.cu", "ssm_recurrent_decode_gb300/csrc/gdn_pipe.cuh",
+                  "ssm_recurrent_decode_gb300/csrc/gdn_tile.cuh", "ssm_recurrent_decode_gb300/csrc/gdn_common.cuh"],
     "buffered": ["ssm_recurrent_decode_gb300/csrc/buffered_pipe.cu", "ssm_recurrent_decode_gb300/csrc/gdn_pipe.cuh",
                  "ssm_recurrent_decode_gb300/csrc/gdn_tile.cuh", "ssm_recurrent_decode_gb300/csrc/gdn_common.cuh"],
     "fused": ["ssm_recurrent_decode_gb300/csrc/fused_pipe.cu", "ssm_recurrent_decode_gb300/csrc/gdn_pipe.cuh",
@@ -553,7 +555,10 @@ class Harness:
 
     def finish(self, line):
         if self.rank == 0 and line is not None:
-            print(json.dumps(line), flush=True)
+            if getattr(self.args, "capture", None) is not None:
+                self.args.capture.append(line)     # a secondary row of the default run
+            else:
+                print(json.dumps(line), flush=True)
         if self.world > 1:
             self.torch.distributed.destroy_process_group()
         return 0
@@ -734,9 +739,11 @@ def run_packed(args):
         steps)
     line["pct_of_peak"] = round(100 * gbs / h.world / peak, 2)            # of the measured copy bandwidth
     line["pct_of_nominal_peak"] = round(100 * gbs / h.world / NOMINAL_HBM_GBS, 2)  # of 7.9 TB/s
-    line["roofline"] = roofline(state_bytes + packed_io_bytes(B, H, HV, K, V), ms, "step",
+    line["roofline"] = roofline(state_bytes + packed_io_bytes(B, H, HV, K, V), ms,
+                                "step_bf16" if args.state_dtype == "bf16" else "step",
                                 f"packed_B{B}" + ("_bf16state" if args.state_dtype == "bf16" else ""))
-    line["cpu_baseline"] = cpu_baseline(H, HV, K, V, seed=7, budget_s=args.cpu_budget)
+    if not getattr(args, "secondary_row", False):
+        line["cpu_baseline"] = cpu_baseline(H, HV, K, V, seed=7, budget_s=args.cpu_budget)
     line["e2e"] = {"value": round(h.world * state_bytes / (ms_e2e * 1e-3) / 1e9, 2), "unit": "GB/s",
                    "us_per_step": round(ms_e2e * 1e3, 3), "h2d_bytes_per_step": h2d,
                    "d2h_bytes_per_step": d2h,
@@ -806,7 +813,8 @@ def run_buffered(args):
         "packed_equivalent_state_GBs": round(2 * S / (ms * 1e-3) / 1e9, 2)}, steps)
     line["roofline"] = roofline(state_traffic + ring_append + ring_read_mean + io, ms, "buffered",
                                 f"buffered_B{B}_L{L}")
-    line["cpu_baseline"] = cpu_baseline_buffered(H, HV, K, V, L, seed=8, budget_s=args.cpu_budget)
+    if not getattr(args, "secondary_row", False):
+        line["cpu_baseline"] = cpu_baseline_buffered(H, HV, K, V, L, seed=8, budget_s=args.cpu_budget)
     line["phase_us"] = [round(p * 1e3, 2) for p in phase_ms]
     line["flush_over_nonflush"] = (round(phase_ms[-1] / statistics.mean(phase_ms[:-1]), 3)
                                    if L > 1 else None)
@@ -883,19 +891,21 @@ def run_fused(args):
          "l2": f"{n_pools} state pool(s) rotated, at least 4x the L2 size per pass",
          "timing": f"CUDA-graph replays of {per_graph} calls"}, steps)
     line["roofline"] = roofline(state_bytes + io, ms, "fused", f"fused_T{T}")
-    line["cpu_baseline"] = cpu_baseline_fused(heads, D, seed=9, budget_s=args.cpu_budget)
+    if not getattr(args, "secondary_row", False):
+        line["cpu_baseline"] = cpu_baseline_fused(heads, D, seed=9, budget_s=args.cpu_budget)
     line["clocks"] = clk
     return h.finish(line)
 
 
 def stack_decode(layers=48, B=256, H=16, HV=48, K=128, V=128, steps=1000, seed=2024, pairs=8,
-                 heads_per_pair=2, device=None, verbose=False):
+                 heads_per_pair=2, device=None, verbose=False, chained=True):
     """The stacked decode under CUDA graphs: `layers` independent state pools, one graph that
     draws fresh seeded inputs for every layer on the device (keyed by seed, layer and a device step
-    counter), and one graph of `layers` decode calls, replayed `steps` times. Afterwards the fp64
-    oracle replays `pairs` sampled (layer, slot) pairs, on `heads_per_pair` q/k heads each (all
-    their value heads), through every step and the drift of the GPU state against it is measured.
-    Returns a dict of timings and errors."""
+    counter), and one graph of `layers` decode calls, replayed `steps` times (chained: every layer
+    after the first through gdn_decode_step_indexed_chained, so that its launch overlaps the
+    previous layer's tail). Afterwards the fp64 oracle replays `pairs` sampled (layer, slot)
+    pairs, on `heads_per_pair` q/k heads each (all their value heads), through every step and the
+    drift of the GPU state against it is measured. Returns a dict of timings and errors."""
     import torch
     import gdn_synth as syn
     import oracle
@@ -921,9 +931,10 @@ def stack_decode(layers=48, B=256, H=16, HV=48, K=128, V=128, steps=1000, seed=2
 
     def decode():
         sid = torch.cuda.current_stream(dev).cuda_stream
-        for (q, k, v), w in zip(views, L):
+        for l, ((q, k, v), w) in enumerate(zip(views, L)):
             gdn.gdn_decode_step_indexed(q, k, v, w["state"], w["out"], w["idx"], H=H, a=w["a"],
-                                        b=w["b"], A_log=w["A_log"], dt_bias=w["dt_bias"], stream=sid)
+                                        b=w["b"], A_log=w["A_log"], dt_bias=w["dt_bias"], stream=sid,
+                                        chained=chained and l > 0)
 
     # one eager pass loads every kernel before capture; then the pools are reset to step 0
     gen()
@@ -994,7 +1005,8 @@ def run_stack(args):
     gdn.lib()
     layers, B, H, HV, K, V = args.layers, args.B, 16, 48, 128, 128
     steps = args.steps
-    res = stack_decode(layers, B, H, HV, K, V, steps=steps, device=h.dev, pairs=args.pairs)
+    res = stack_decode(layers, B, H, HV, K, V, steps=steps, device=h.dev, pairs=args.pairs,
+                       chained=not args.no_chain)
     ms = res["dec_ms_median"]
     (ms,) = max_over_ranks([ms], h.world)
     if h.rank != 0:
@@ -1006,7 +1018,8 @@ def run_stack(args):
         f"{layers}-layer stacked gdn decode under CUDA graphs: B={B} H={H} HV={HV} K=V={K}, an "
         f"fp32 state pool per layer ({layers * B * HV * V * K * 4 / 1e9:.1f} GB), fresh device-drawn "
         f"bf16 inputs every step", {"layers": layers, "B": B, "H": H, "HV": HV, "K": K, "V": V,
-                                     "state_bytes_per_step": state_bytes}, steps * layers)
+                                     "state_bytes_per_step": state_bytes,
+                                     "chained_layers": not args.no_chain}, steps * layers)
     line["per_layer_us"] = round(ms * 1e3 / layers, 3)
     line["with_input_generation_ms_per_step"] = round(res["total_ms_per_step"], 4)
     line["drift_vs_oracle"] = {"max_rel_state_err": res["drift"], "last_step_out_err": res["last_out_err"],
@@ -1055,7 +1068,8 @@ def run_mamba(args):
                                      "B = 1 / 4 / 8, D = 1536, N = 16 (launch-bound)"}, steps)
     min_bytes = 2 * B * D * N * 4 + D * N * 4 + 2 * B * N * 4 + 4 * B * D * 4 + D * 4
     line["roofline"] = roofline(min_bytes, ms, "mamba", f"mamba_B{B}_D{D}_N{N}")
-    line["cpu_baseline"] = cpu_baseline_mamba(D, N, seed=78, budget_s=args.cpu_budget)
+    if not getattr(args, "secondary_row", False):
+        line["cpu_baseline"] = cpu_baseline_mamba(D, N, seed=78, budget_s=args.cpu_budget)
     line["clocks"] = clk
     return h.finish(line)
 
@@ -1106,7 +1120,8 @@ def run_gemv(args):
     # algorithmic bytes: W once, x, y (any split-K exchange is the kernel's overhead)
     io = T * Kd * 2 + T * N * 2
     line["roofline"] = roofline(w_bytes + io, ms, "gemv", f"gemv_T{T}_N{N}_K{Kd}")
-    line["cpu_baseline"] = cpu_baseline_gemv(T, N, Kd, seed=92, budget_s=args.cpu_budget)
+    if not getattr(args, "secondary_row", False):
+        line["cpu_baseline"] = cpu_baseline_gemv(T, N, Kd, seed=92, budget_s=args.cpu_budget)
     line["clocks"] = clk
     return h.finish(line)
 
@@ -1189,6 +1204,65 @@ def run_front(args):
     return h.finish(line)
 
 
+# Secondary rows measured by the default run after the headline (one GPU, rank 0 only): the
+# other hot-path rows at their workload sizes, each with its own timing and roofline, summarised in
+# the headline's JSON line under "secondary" (no CPU baseline, no end-to-end leg).
+SECONDARY_ROWS = [
+    ("packed_B256_bf16_state", {"workload": "packed", "B": 256, "state_dtype": "bf16"}),
+    ("packed_B16", {"workload": "packed", "B": 16}),
+    ("buffered_B256_L16", {"workload": "buffered", "B": 256, "L": 16}),
+    ("fused_kda_T128", {"workload": "fused", "T": 128}),
+    ("fused_kda_T8", {"workload": "fused", "T": 8}),
+    ("stack48_B16_chained", {"workload": "stack", "B": 16, "layers": 48, "steps": 50, "pairs": 2}),
+    ("mamba_B1024_N16", {"workload": "mamba", "B": 1024, "N": 16}),
+    ("mamba_B1024_N64", {"workload": "mamba", "B": 1024, "N": 64}),
+    ("gemv_17408x5120_T8", {"workload": "gemv", "T": 8}),
+    ("front_T1", {"workload": "front", "T": 1}),
+]
+
+
+def secondary_summary(line):
+    r = line.get("roofline", {})
+    out = {"workload": line["config"].get("workload"), "metric": line["metric"], "value": line["value"],
+           "unit": line["unit"], "us_per_call": line["us_per_step"], "roofline_frac": r.get("frac"),
+           "roofline_achieved": r.get("achieved"), "timing_spread": line.get("timing_spread"),
+           "clocks": line.get("clocks")}
+    for k in ("drift_vs_oracle", "per_layer_us", "state_traffic_gbs"):
+        if k in line:
+            out[k] = line[k]
+    return out
+
+
+def run_default_with_secondary(args):
+    """The headline (packed B=256) line, then the secondary rows, printed as one JSON line."""
+    import copy
+    captured = []
+    args.capture = captured
+    run_packed(args)
+    line = captured[0]
+    secondary = {}
+    t0 = time.time()
+    for name, over in SECONDARY_ROWS:
+        a2 = copy.copy(args)
+        for k, v in over.items():
+            setattr(a2, k, v)
+        if "steps" not in over:
+            a2.steps = 20
+        a2.warmup = max(3, min(args.warmup, 5))
+        a2.secondary_row = True
+        a2.capture = []
+        try:
+            {"packed": run_packed, "buffered": run_buffered, "fused": run_fused, "stack": run_stack,
+             "mamba": run_mamba, "gemv": run_gemv, "front": run_front}[a2.workload](a2)
+            secondary[name] = secondary_summary(a2.capture[0])
+        except Exception as e:   # a failed secondary row is reported, never hides the headline
+            secondary[name] = {"error": f"{type(e).__name__}: {e}"[:300]}
+    line["secondary"] = secondary
+    line["secondary_wall_s"] = round(time.time() - t0, 1)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
@@ -1212,12 +1286,19 @@ def main(argv=None):
     p.add_argument("--N", type=int, default=16)
     p.add_argument("--layers", type=int, default=48)
     p.add_argument("--pairs", type=int, default=8)
+    p.add_argument("--no-chain", action="store_true",
+                   help="stack workload: ordinary launches for every layer (no programmatic overlap)")
     p.add_argument("--cpu-budget", type=float, default=10.0)
+    p.add_argument("--no-secondary", action="store_true",
+                   help="default workload only: skip the secondary rows measured after the headline")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
     if args.impl == "reference":
         return run_reference(args)
+    if (args.workload == "packed" and args.B == 256 and args.state_dtype == "f32" and not args.no_secondary
+            and dist_env()[1] == 1):
+        return run_default_with_secondary(args)
     return {"packed": run_packed, "buffered": run_buffered, "fused": run_fused,
             "stack": run_stack, "mamba": run_mamba, "gemv": run_gemv,
             "front": run_front}[args.workload](args)

@@ -56,3 +56,15 @@ def test_oracle_baselines_of_the_mamba_and_projection_lines():
     assert m["value"] > 0 and m["kind"] == "oracle" and "single-row" in m["sample"]
     g = bench.cpu_baseline_gemv(2, 300, 128, seed=1, budget_s=0.05, rows=64)
     assert g["value"] > 0 and "64 of the 300 weight rows" in g["sample"]
+
+
+def test_secondary_rows_cover_the_hot_path_rows_and_summarise():
+    import bench
+    names = [n for n, _ in bench.SECONDARY_ROWS]
+    assert len(names) == len(set(names))
+    workloads = {o["workload"] for _, o in bench.SECONDARY_ROWS}
+    assert {"packed", "buffered", "fused", "stack", "mamba", "gemv", "front"} <= workloads
+    line = {"config": {"workload": "w"}, "metric": "m", "value": 1.0, "unit": "GB/s",
+            "us_per_step": 2.0, "roofline": {"frac": 0.5, "achieved": 3.0}, "per_layer_us": 4.0}
+    s = bench.secondary_summary(line)
+    assert s["roofline_frac"] == 0.5 and s["per_layer_us"] == 4.0 and s["us_per_call"] == 2.0
