@@ -75,7 +75,7 @@ def kernel_sources_hash(files) -> str:
 KERNEL_FILES = {
     "step": ["ssm_recurrent_decode_gb300/csrc/step_kernel.cu", "ssm_recurrent_decode_gb300/csrc/gdn_tile.cuh",
              "ssm_recurrent_decode_gb300/csrc/gdn_common.cuh"],
-    "step_bf16": ["ssm_recurrent_decode_gb300/csrc/step_pipe_bf16.cu", "ssm_recurrent_decode_gb300/csrc/gdn_pipe.cuh",
+    "step_bf16": ["ssm_recurrent_decode_gb300/csrc/step_stage_bf16.cu", "ssm_recurrent_decode_gb300/csrc/gdn_pipe.cuh",
                   "ssm_recurrent_decode_gb300/csrc/gdn_tile.cuh", "ssm_recurrent_decode_gb300/csrc/gdn_common.cuh"],
     "buffered": ["ssm_recurrent_decode_gb300/csrc/buffered_pipe.cu", "ssm_recurrent_decode_gb300/csrc/gdn_pipe.cuh",
                  "ssm_recurrent_decode_gb300/csrc/gdn_tile.cuh", "ssm_recurrent_decode_gb300/csrc/gdn_common.cuh"],

@@ -206,9 +206,9 @@ int gdn_decode_step_indexed(const gdn_step_args *args, const int32_t *cache_indi
  * before it: no kernel in that run may write this call's state tiles or cache_indices. Give every
  * chained layer its own state pool, and make the first call of each step an ordinary call, so that
  * two calls on the same pool are never in one run. The overlap takes one launch gap and the
- * previous layer's tail off each layer. A bf16 state at K = V = 128 from four tiles per SM runs
- * the ordinary kernel (no overlap). Arguments, results and status codes as for
- * gdn_decode_step_indexed. Source: as gdn_decode_step_indexed; the layer loop is the model of
+ * previous layer's tail off each layer. A bf16 state at K = V = 128 from 128 tiles on, and grids
+ * of eight or more waves of CTAs, run the ordinary kernel (no overlap). Arguments, results and
+ * status codes as for gdn_decode_step_indexed. Source: as gdn_decode_step_indexed; the layer loop is the model of
  * "Optimization Log: Qwen3.5-27B Dense on B200" (decode is launch-bound at small batch, "Triton
  * decode kernel + MBU analysis", Kernel design).
  */

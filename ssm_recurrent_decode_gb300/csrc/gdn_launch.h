@@ -53,10 +53,11 @@ int launch_step(const StepLaunch &p, cudaStream_t stream, bool chained = false);
 int launch_buffered(const StepLaunch &p, int ring_dtype, cudaStream_t stream);
 int launch_fused(const FusedLaunch &p, cudaStream_t stream, bool chained = false);
 
-// The persistent, warp-specialised step for a bf16 state at K = V = 128, and whether a call
-// qualifies for it (bf16 state, K = V = 128, 16-byte aligned state and q/k/v rows).
-bool step_pipe_bf16_ok(const gdn_step_args &a);
-int launch_step_pipe_bf16(const StepLaunch &p, cudaStream_t stream);
+// The step for a bf16 state at K = V = 128 with each tile staged in shared memory by a bulk copy
+// (step_stage_bf16.cu), and whether a call qualifies for it (bf16 state, K = V = 128, 16-byte
+// aligned state and q/k/v rows).
+bool step_stage_bf16_ok(const gdn_step_args &a);
+int launch_step_stage_bf16(const StepLaunch &p, cudaStream_t stream);
 
 // Dynamic shared memory the buffered kernel needs for ring length L, value dim V and key dim K.
 size_t buffered_smem_bytes(int L, int V, int K);

@@ -104,25 +104,4 @@ __device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src, uint32
         : "memory");
 }
 
-// bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from this CTA's shared
-// memory to global memory, in the thread's bulk async-group, with an L2 cache-policy hint. The
-// generic-proxy writes to the source must be fenced (fence_proxy_async) before it is issued.
-__device__ __forceinline__ void bulk_s2g_hint(void *dst, const void *src, uint32_t bytes, uint64_t policy)
-{
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(dst),
-                 "r"(smem_u32(src)), "r"(bytes), "l"(policy)
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// wait until every committed bulk store of this thread has finished reading its shared memory
-__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-// wait until every committed bulk store of this thread has completed
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
-// barrier over the `threads` threads (a multiple of 32) that use named barrier `id` (1 .. 15)
-__device__ __forceinline__ void named_barrier(int id, int threads)
-{
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-
 }  // namespace gdn

@@ -227,6 +227,12 @@ template <int K, typename Tin, typename TS, int R>
 static void launch_rows(const StepLaunch &p, unsigned tiles, cudaStream_t stream, bool chained)
 {
     const int splits = R >= 16 ? 1 : (p.a.V + Tile<K, R>::ROWS_PASS - 1) / Tile<K, R>::ROWS_PASS;
+    // A chained launch gains the previous layer's tail, which matters when a layer is a few waves
+    // of CTAs: on GB300 the 48-layer graph took 18.68 against 19.50 us per layer at B = 16 (2.5
+    // waves) but 244.3 against 242.5 at B = 256 (40 waves). From eight waves on it launches as usual.
+    const unsigned per_sm = R >= 16 ? 2u : 4u;
+    const unsigned waves_x8 = 8u * per_sm * (unsigned)(sm_count() > 0 ? sm_count() : 152);
+    if (chained && tiles * (unsigned)splits >= waves_x8) chained = false;
     if (!chained) {
         step_kernel<K, Tin, TS, R, false><<<tiles * (unsigned)splits, kThreads, 0, stream>>>(p, splits);
         return;
@@ -258,9 +264,10 @@ static int launch_step_t(const StepLaunch &p, cudaStream_t stream, bool chained)
         return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
     }
     if constexpr (sizeof(TS) == 2 && K == 128) {
-        // bf16 state at K = V = 128: tiles staged through shared memory by a persistent kernel
-        // (step_pipe_bf16.cu) once every SM has several tiles
-        if (tiles >= target && step_pipe_bf16_ok(p.a)) return launch_step_pipe_bf16(p, stream);
+        // bf16 state at K = V = 128: each tile staged in shared memory by a bulk copy
+        // (step_stage_bf16.cu) from 128 tiles on; on GB300 it beat the row split at B = 8 and 16
+        // (HV = 32: 5.92 against 7.47 us, 8.52 against 10.37) and lost at B = 1 (3.52 against 3.29)
+        if (tiles >= 128u && step_stage_bf16_ok(p.a)) return launch_step_stage_bf16(p, stream);
     }
     if (tiles >= target) {
         bool paired = false;
