@@ -621,6 +621,29 @@ def packed_workload(B, H, HV, K, V, seed, device, layer=0, state_dtype="f32"):
     return dict(x=x, a=a, b=b, A_log=A_log, dt_bias=dt_bias, state=state, idx=idx, out=out)
 
 
+def inplace_stream_gbs(buf, h, reps=20):
+    """Context for the roofline: a plain in-place read-modify-write stream over the same buffer as
+    the state (torch's elementwise multiply by 1.0: every element read and written once, values
+    unchanged), timed with CUDA events on this GPU in the same run; median of `reps`."""
+    torch = h.torch
+    nbytes = 2 * buf.numel() * buf.element_size()
+    for _ in range(3):
+        buf.mul_(1.0)
+    times = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(h.stream)
+        buf.mul_(1.0)
+        e1.record(h.stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+    med = statistics.median(times)
+    return {"value": round(nbytes / (med * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "how": f"torch in-place multiply by 1.0 over the {buf.numel() * buf.element_size() / 1e9:.2f} GB "
+                   f"state buffer (read + write), median of {reps} CUDA-event timings in this run; "
+                   f"context for the roofline, not its peak"}
+
+
 def packed_io_bytes(B, H, HV, K, V):
     """Bytes of the step's inputs and outputs besides the state: mixed_qkv, a, b, A_log, dt_bias,
     cache indices, out."""
@@ -739,6 +762,8 @@ def run_packed(args):
         steps)
     line["pct_of_peak"] = round(100 * gbs / h.world / peak, 2)            # of the measured copy bandwidth
     line["pct_of_nominal_peak"] = round(100 * gbs / h.world / NOMINAL_HBM_GBS, 2)  # of 7.9 TB/s
+    if not getattr(args, "secondary_row", False):
+        line["stream_reference"] = inplace_stream_gbs(pools[0], h)
     line["roofline"] = roofline(state_bytes + packed_io_bytes(B, H, HV, K, V), ms,
                                 "step_bf16" if args.state_dtype == "bf16" else "step",
                                 f"packed_B{B}" + ("_bf16state" if args.state_dtype == "bf16" else ""))
