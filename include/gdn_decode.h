@@ -166,10 +166,13 @@ typedef struct gdn_fused_args {
     int32_t gate_act;         /* gdn_act applied to out_gate */
     void *out;                /* bf16 [T, heads, head_dim] */
     int32_t *err_flags;       /* optional */
-    int32_t kernel;           /* GDN_KERNEL_AUTO: the pipelined kernel when head_dim == 128, the conv
+    int32_t kernel;           /* GDN_KERNEL_AUTO: the staged kernels when head_dim == 128, the conv
                                  state is in the DS or SD layout, rows are 16-byte aligned and there
-                                 are more than two (token, head) tiles per SM, else the per-tile
-                                 kernel; GDN_KERNEL_TILE / GDN_KERNEL_PIPE force one */
+                                 are more than two (token, head) tiles per SM (from eight tiles per
+                                 SM one CTA per tile with its tile staged in shared memory by bulk
+                                 copies, below that the persistent pipelined kernel), else the
+                                 per-tile kernel; GDN_KERNEL_TILE / GDN_KERNEL_PIPE force the
+                                 per-tile kernel / the staged ones */
     int64_t raw_g_stride;     /* row (token) strides in elements of raw_g, raw_beta and out_gate, at
                                  least the dense row width; 0 selects the dense width. The pipelined */
     int64_t raw_beta_stride;  /* kernel needs out_gate's (and a KDA raw_g's) to be a multiple of 8, */

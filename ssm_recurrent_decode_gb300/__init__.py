@@ -481,9 +481,11 @@ def gdn_decode_fused(x, conv_w, conv_state, raw_g, raw_beta, A_log, dt_bias, sta
                      norm_eps=1e-5, gate_act="silu", err_flags=None, kernel="auto", stream=None,
                      prepare=False):
     """Fused decode: conv update -> delta step -> gated RMSNorm, one launch.
-    kernel: "auto" (the persistent pipelined kernel when head_dim is 128, the conv state is in the
-    DS or SD layout, rows are 16-byte aligned and there are more than two (token, head) tiles per
-    SM), "tile" or "pipe" to force one.
+    kernel: "auto" (the staged kernels when head_dim is 128, the conv state is in the DS or SD
+    layout, rows are 16-byte aligned and there are more than two (token, head) tiles per SM: one
+    CTA per tile staged in shared memory from eight tiles per SM, the persistent pipelined kernel
+    below that; else the per-tile kernel), "tile" or "pipe" to force the per-tile or the staged
+    kernels.
     x bf16 [T, 3*dim]; conv_w fp32 [3*dim, 4]; conv_state bf16 with logical shape
     [num_slots, 3*dim, 3] (any strides: the "DS" layout is the plain tensor, the "SD" layout a
     transposed view of [num_slots, 3, 3*dim]); raw_g bf16 [T, heads, D] (kda) or [T, heads] (gdn);

@@ -399,4 +399,229 @@ int launch_fused_pipe(const FusedLaunch &p, bool sd, cudaStream_t stream, bool c
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
 }
 
+
+// ------------------------------------------------------------------------------------------------
+// One (token, head) tile per CTA of 256 threads with the same staging: thread 0 bulk-copies the
+// state tile and the conv-state rows (neither is written by a chained launch's previous kernel),
+// waits for that kernel, then copies x and the gate rows; all threads compute the tile's scalars
+// meanwhile. The arithmetic is the consumer group's above, with block barriers in place of the
+// group's mbarriers. 68 KB of shared memory per CTA: three CTAs per SM.
+// ------------------------------------------------------------------------------------------------
+template <bool SD>
+__global__ void __launch_bounds__(256, 3) fused_stage_kernel(const __grid_constant__ FusedLaunch P)
+{
+    constexpr int D = 128;
+    using TR = Tile<128, 8, kFGW>;
+    using FL = FusedLayout;
+    extern __shared__ __align__(128) unsigned char stage[];
+    __shared__ float ys[3 * D];
+    __shared__ float red[kFGW];
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag, zero_flag;
+
+    const gdn_fused_args &a = P.a;
+    const int heads = a.heads;
+    const size_t dim = (size_t)heads * D;
+    const int tile = blockIdx.x, tt = tile / heads, h = tile - tt * heads;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+    bf16 *const cstate = static_cast<bf16 *>(a.conv_state);
+    bf16 *out = static_cast<bf16 *>(a.out) + ((size_t)tt * heads + h) * D;
+    const bool kda = a.gate_kind == GDN_FUSED_GATE_KDA;
+
+    grid_launch_dependents();
+    const int slot = a.state_indices[tt];
+    const bool skip = slot == a.pad_slot_id || slot < 0 || slot >= a.num_slots;   // uniform over the CTA
+    const bool out_of_range = !skip && !fused_tile_in_range(a, tt, h, slot);      // debug build only
+    if (skip || out_of_range) {
+        grid_dependency_wait();
+        if (skip && slot != a.pad_slot_id && tid == 0) raise_flag(a.err_flags, GDN_DEVERR_BAD_INDEX);
+        if (skip && tid < D) out[tid] = __float2bfloat16_rn(0.f);
+        return;
+    }
+    const uint64_t pol = policy_evict_first();
+    const bf16 *csr = cstate + (size_t)slot * a.cs_stride_slot;
+    if (tid == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        zero_flag = 0;
+        fence_barrier_init();
+        mbar_arrive_expect_tx(&bar, 65536u + 768u + 2304u + 256u + (kda ? 256u + 512u : 0u));
+        bulk_g2s_hint(stage, a.state + ((size_t)slot * heads + h) * (size_t)(D * D), 65536u, &bar, pol);
+        for (int part = 0; part < 3; ++part) {
+            const size_t ch0 = part * dim + (size_t)h * D;
+            if (SD) {
+                for (int tap = 0; tap < 3; ++tap)
+                    bulk_g2s(stage + FL::cs + (part * 3 + tap) * 256u, csr + ch0 + tap * a.cs_stride_tap, 256u, &bar);
+            } else {
+                bulk_g2s(stage + FL::cs + part * 768u, csr + ch0 * 3, 768u, &bar);
+            }
+        }
+        if (kda) bulk_g2s(stage + FL::db, a.dt_bias + (size_t)h * D, 512u, &bar);
+    }
+    // a chained launch: x and the gate rows may be the previous kernel's output
+    grid_dependency_wait();
+    if (tid == 0) {
+        const bf16 *xr = static_cast<const bf16 *>(a.x) + (size_t)tt * a.x_stride + (size_t)h * D;
+        for (int part = 0; part < 3; ++part) bulk_g2s(stage + FL::x + part * 256u, xr + part * dim, 256u, &bar);
+        bulk_g2s(stage + FL::og, static_cast<const bf16 *>(a.out_gate) + (size_t)tt * a.out_gate_stride + (size_t)h * D, 256u, &bar);
+        if (kda) bulk_g2s(stage + FL::rg, static_cast<const bf16 *>(a.raw_g) + (size_t)tt * a.raw_g_stride + (size_t)h * D, 256u, &bar);
+    }
+    // the tile's scalars, the conv weights of this thread's channels and the norm weights
+    const float beta = sigmoid_f(__bfloat162float(static_cast<const bf16 *>(a.raw_beta)[(size_t)tt * a.raw_beta_stride + h]));
+    const float A = expf(a.A_log[h]);
+    float g_head = 0.f;
+    if (!kda) g_head = -A * softplus_f(__bfloat162float(static_cast<const bf16 *>(a.raw_g)[(size_t)tt * a.raw_g_stride + h]) + a.dt_bias[h]);
+    float4 w_cur[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int c = tid + u * 256;
+        if (c < 3 * D) {
+            const int part = c / D, j = c - part * D;
+            w_cur[u] = __ldg(reinterpret_cast<const float4 *>(a.conv_w + (part * dim + (size_t)h * D + j) * 4));
+        }
+    }
+    TR t;
+    t.init(warp);
+    const int row0 = warp * 16;
+    const int rsub = (t.sub % 16) / 2;
+    float w_norm[2];
+#pragma unroll
+    for (int c = 0; c < 2; ++c) w_norm[c] = a.norm_w[row0 + 8 * c + rsub];
+    __syncthreads();   // the barrier is initialised before anyone waits on it
+    if (!mbar_wait_warp(&bar, 0u, &abort_flag, kFWaitLimit)) {
+        if (lane == 0) raise_flag(a.err_flags, GDN_DEVERR_TIMEOUT);
+        if (tid == 0) mbar_wait(&bar, 0u, &zero_flag, kFWaitLimit);   // copies still in flight land first
+        return;
+    }
+
+    // (1) conv update of the head's 3 x 128 channels
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int c = tid + u * 256;
+        if (c < 3 * D) {
+            const int part = c / D, j = c - part * D;
+            float x0, x1, x2;
+            if (SD) {
+                x0 = bfs(stage, FL::cs, (part * 3 + 0) * D + j);
+                x1 = bfs(stage, FL::cs, (part * 3 + 1) * D + j);
+                x2 = bfs(stage, FL::cs, (part * 3 + 2) * D + j);
+            } else {
+                x0 = bfs(stage, FL::cs, part * 3 * D + j * 3 + 0);
+                x1 = bfs(stage, FL::cs, part * 3 * D + j * 3 + 1);
+                x2 = bfs(stage, FL::cs, part * 3 * D + j * 3 + 2);
+            }
+            const float xin = bfs(stage, FL::x, part * D + j);
+            const float4 w = w_cur[u];
+            float acc = w.x * x0;
+            acc = fmaf(w.y, x1, acc);
+            acc = fmaf(w.z, x2, acc);
+            acc = fmaf(w.w, xin, acc);
+            const size_t ch = part * dim + (size_t)h * D + j;
+            if (a.conv_b) acc += a.conv_b[ch];
+            ys[c] = acc * sigmoid_f(acc);
+            bf16 *cp = cstate + (size_t)slot * a.cs_stride_slot + ch * a.cs_stride_chan;
+            cp[0] = __float2bfloat16_rn(x1);
+            cp[a.cs_stride_tap] = __float2bfloat16_rn(x2);
+            cp[2 * a.cs_stride_tap] = __float2bfloat16_rn(xin);
+        }
+    }
+    // (2) gates of this lane's four key columns, output gate of its rows
+    float4 dec;
+    if (kda) {
+        float gv[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const float xg = bfs(stage, FL::rg, t.col + c) + reinterpret_cast<const float *>(stage + FL::db)[t.col + c];
+            gv[c] = a.kda_gate_form == 0 ? fmaxf(a.lower_bound, -A * softplus_f(xg)) : a.lower_bound * sigmoid_f(A * xg);
+        }
+        dec = make_float4(expf(gv[0]), expf(gv[1]), expf(gv[2]), expf(gv[3]));
+    } else {
+        const float e = expf(g_head);
+        dec = make_float4(e, e, e, e);
+    }
+    float gate[2];
+#pragma unroll
+    for (int c = 0; c < 2; ++c) gate[c] = bfs(stage, FL::og, row0 + 8 * c + rsub);
+    __syncthreads();   // conv outputs complete
+
+    // (3) the step, both dots straight from the staged tile, eight rows at a time
+    const float4 kh = l2_normalise4<32>(*reinterpret_cast<const float4 *>(ys + D + t.col), a.use_qk_l2norm != 0, 1.f);
+    const float4 qh = l2_normalise4<32>(*reinterpret_cast<const float4 *>(ys + t.col), a.use_qk_l2norm != 0, P.scale);
+    const float kq = group_sum<32>(dot4(kh, qh));
+    const float *Ss = reinterpret_cast<const float *>(stage);
+    float dvc0 = 0.f, dvc1 = 0.f, oc0 = 0.f, oc1 = 0.f;
+    {
+        const float4 kd = mul4(kh, dec), qd = mul4(qh, dec);
+#pragma unroll 1
+        for (int c = 0; c < 2; ++c) {
+            float x[TR::N];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 srow = *reinterpret_cast<const float4 *>(Ss + (size_t)(row0 + 8 * c + i) * D + t.col);
+                x[i] = dot4(srow, kd);
+                x[8 + i] = dot4(srow, qd);
+            }
+            t.reduce_scatter(x);
+            const float vv = t.holds_k_dot() ? ys[2 * D + row0 + 8 * c + rsub] : 0.f;
+            const float d = beta * (vv - x[0]);
+            const float dq = __shfl_up_sync(kFull, d, 16);
+            const float o = fmaf(dq, kq, x[0]);
+            if (c == 0) {
+                dvc0 = d;
+                oc0 = o;
+            } else {
+                dvc1 = d;
+                oc1 = o;
+            }
+        }
+    }
+    {
+        float *S = a.state + ((size_t)slot * heads + h) * (size_t)(D * D);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float d = __shfl_sync(kFull, c == 0 ? dvc0 : dvc1, 2 * i);
+                const float4 srow = *reinterpret_cast<const float4 *>(Ss + (size_t)(row0 + 8 * c + i) * D + t.col);
+                st_stream(S + (size_t)(row0 + 8 * c + i) * D + t.col, decay_update4(dec, srow, d, kh));
+            }
+        }
+    }
+    // (4) gated RMSNorm over the head's 128 outputs
+    const bool owner = !t.holds_k_dot() && (t.sub & 1) == 0;
+    float sq = owner ? oc0 * oc0 + oc1 * oc1 : 0.f;
+    sq = group_sum<32>(sq);
+    if (lane == 0) red[warp] = sq;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < kFGW; ++w) tot += red[w];
+    const float rs = 1.0f / sqrtf(tot / D + a.norm_eps);
+    if (owner) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const float act = a.gate_act == GDN_ACT_SILU ? gate[c] * sigmoid_f(gate[c]) : sigmoid_f(gate[c]);
+            out[row0 + 8 * c + rsub] = __float2bfloat16_rn((c == 0 ? oc0 : oc1) * rs * w_norm[c] * act);
+        }
+    }
+}
+
+int launch_fused_stage(const FusedLaunch &p, bool sd, cudaStream_t stream, bool chained)
+{
+    const size_t smem = FusedLayout::meta;   // state tile, x, conv state, raw_g, dt_bias, out_gate
+    auto kern = sd ? fused_stage_kernel<true> : fused_stage_kernel<false>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return GDN_ERR_LAUNCH;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3((unsigned)(p.a.T * p.a.heads));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    if (chained) set_programmatic(attr[cfg.numAttrs++]);
+    if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return GDN_ERR_LAUNCH;
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
+}
+
 }  // namespace gdn

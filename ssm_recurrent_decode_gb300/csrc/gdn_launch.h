@@ -36,6 +36,7 @@ struct FusedPlan {
     bool empty;      // T == 0: nothing to launch
     bool use_pipe;   // the persistent pipelined kernel
     bool sd;         // its conv state is in the SD layout
+    int sms;         // SMs of the device (the pipelined and staged kernels' choice)
 };
 
 // The host checks of gdn_decode_fused (the same status codes) and its kernel choice; no CUDA launch.
@@ -71,5 +72,8 @@ bool buffered_pipe_fits(int L, int in_dtype, int ring_dtype, int max_smem);
 // the SD layout when sd is true).
 int launch_fused_pipe(const FusedLaunch &p, bool sd, cudaStream_t stream, bool chained = false);
 bool fused_pipe_fits(int max_smem);
+// The same op with one (token, head) tile per CTA staged in shared memory (the pipelined kernel's
+// requirements).
+int launch_fused_stage(const FusedLaunch &p, bool sd, cudaStream_t stream, bool chained = false);
 
 }  // namespace gdn
