@@ -1300,7 +1300,7 @@ def main(argv=None):
     p.add_argument("--L", type=int, default=16)
     p.add_argument("--T", type=int, default=128)
     p.add_argument("--layout", choices=["DS", "SD"], default="DS")
-    p.add_argument("--kernel", choices=["auto", "tile", "pipe"], default="auto",
+    p.add_argument("--kernel", choices=["auto", "tile", "pipe", "stage"], default="auto",
                    help="kernel family of the buffered, fused and front workloads")
     p.add_argument("--state-dtype", choices=["f32", "bf16"], default="f32")
     p.add_argument("--D", type=int, default=1536)

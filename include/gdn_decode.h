@@ -117,13 +117,16 @@ typedef struct gdn_ring_args {
     void *k_cache;            /* [num_slots, H, L, K] normalised-key records */
     float *g_cache;           /* [num_slots, HV, L] log-decay records */
     const int32_t *write_pos; /* [B] cursor of each row, 0 <= write_pos[b] < L; read only */
-    int32_t kernel;           /* GDN_KERNEL_AUTO (0): the pipelined kernel when it applies and L > 1,
-                                 else the per-tile kernel; GDN_KERNEL_TILE (1) / GDN_KERNEL_PIPE (2) force one
-                                 (PIPE needs K == V == 128, L == 1 or a multiple of 4, and 16-byte
-                                 aligned rows and rings: GDN_ERR_SHAPE or GDN_ERR_ALIGN otherwise) */
+    int32_t kernel;           /* GDN_KERNEL_AUTO (0): the persistent pipelined kernel when it applies and
+                                 L > 1, else the per-tile kernel; GDN_KERNEL_TILE (1) / GDN_KERNEL_PIPE
+                                 (2) / GDN_KERNEL_STAGE (3, one CTA per tile staged in shared memory)
+                                 force one
+                                 (PIPE and STAGE need K == V == 128, L == 1 or a multiple of 4, and
+                                 16-byte aligned rows and rings: GDN_ERR_SHAPE or GDN_ERR_ALIGN
+                                 otherwise) */
 } gdn_ring_args;
 
-typedef enum gdn_kernel { GDN_KERNEL_AUTO = 0, GDN_KERNEL_TILE = 1, GDN_KERNEL_PIPE = 2 } gdn_kernel;
+typedef enum gdn_kernel { GDN_KERNEL_AUTO = 0, GDN_KERNEL_TILE = 1, GDN_KERNEL_PIPE = 2, GDN_KERNEL_STAGE = 3 } gdn_kernel;
 
 typedef enum gdn_fused_gate {
     GDN_FUSED_GATE_KDA = 0,   /* one log-decay per key channel, bounded below by lower_bound */
@@ -166,13 +169,12 @@ typedef struct gdn_fused_args {
     int32_t gate_act;         /* gdn_act applied to out_gate */
     void *out;                /* bf16 [T, heads, head_dim] */
     int32_t *err_flags;       /* optional */
-    int32_t kernel;           /* GDN_KERNEL_AUTO: the staged kernels when head_dim == 128, the conv
-                                 state is in the DS or SD layout, rows are 16-byte aligned and there
-                                 are more than two (token, head) tiles per SM (from eight tiles per
-                                 SM one CTA per tile with its tile staged in shared memory by bulk
-                                 copies, below that the persistent pipelined kernel), else the
-                                 per-tile kernel; GDN_KERNEL_TILE / GDN_KERNEL_PIPE force the
-                                 per-tile kernel / the staged ones */
+    int32_t kernel;           /* GDN_KERNEL_AUTO: when head_dim == 128, the conv state is in the DS or
+                                 SD layout, rows are 16-byte aligned and there are more than two
+                                 (token, head) tiles per SM, one CTA per tile staged in shared memory
+                                 by bulk copies from sixteen tiles per SM and the persistent pipelined
+                                 kernel below that; else the per-tile kernel. GDN_KERNEL_TILE /
+                                 GDN_KERNEL_PIPE / GDN_KERNEL_STAGE force one */
     int64_t raw_g_stride;     /* row (token) strides in elements of raw_g, raw_beta and out_gate, at
                                  least the dense row width; 0 selects the dense width. The pipelined */
     int64_t raw_beta_stride;  /* kernel needs out_gate's (and a KDA raw_g's) to be a multiple of 8, */

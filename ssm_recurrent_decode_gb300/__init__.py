@@ -40,7 +40,7 @@ GDN_FUSED_GATE_KDA, GDN_FUSED_GATE_GDN = 0, 1
 GDN_ACT_SILU, GDN_ACT_SIGMOID = 0, 1
 GDN_DEVERR_BAD_INDEX, GDN_DEVERR_BAD_WRITE_POS, GDN_DEVERR_TIMEOUT = 0x1, 0x2, 0x4
 GDN_DEVERR_RANGE = 0x8
-GDN_KERNEL = {"auto": 0, "tile": 1, "pipe": 2}
+GDN_KERNEL = {"auto": 0, "tile": 1, "pipe": 2, "stage": 3}
 ABI_VERSION = 6
 
 # every function the header declares
@@ -372,7 +372,8 @@ def gdn_decode_buffered(q, k, v, state, out, d_cache, k_cache, g_cache, write_po
     k_cache [num_slots, H, L, K] (both fp32 or both bf16), g_cache [num_slots, HV, L] fp32;
     write_pos int32 [B] is read, never advanced (the caller moves it to (p+1) % L).
     kernel: "auto" (the persistent pipelined kernel when K == V == 128, rows are 16-byte aligned
-    and L > 1, else the per-tile kernel), "tile" or "pipe" to force one."""
+    and L > 1, else the per-tile kernel), "tile", "pipe" or "stage" (one CTA per tile staged in
+    shared memory) to force one."""
     torch = _torch()
     s = _step_args(q, k, v, state, out, H=H, a=a, b=b, A_log=A_log, dt_bias=dt_bias, g=g,
                    beta=beta, scale=scale, use_qk_l2norm=use_qk_l2norm, err_flags=err_flags)
@@ -481,11 +482,10 @@ def gdn_decode_fused(x, conv_w, conv_state, raw_g, raw_beta, A_log, dt_bias, sta
                      norm_eps=1e-5, gate_act="silu", err_flags=None, kernel="auto", stream=None,
                      prepare=False):
     """Fused decode: conv update -> delta step -> gated RMSNorm, one launch.
-    kernel: "auto" (the staged kernels when head_dim is 128, the conv state is in the DS or SD
-    layout, rows are 16-byte aligned and there are more than two (token, head) tiles per SM: one
-    CTA per tile staged in shared memory from eight tiles per SM, the persistent pipelined kernel
-    below that; else the per-tile kernel), "tile" or "pipe" to force the per-tile or the staged
-    kernels.
+    kernel: "auto" (when head_dim is 128, the conv state is in the DS or SD layout, rows are
+    16-byte aligned and there are more than two (token, head) tiles per SM: one CTA per tile
+    staged in shared memory from sixteen tiles per SM, the persistent pipelined kernel below that;
+    else the per-tile kernel), "tile", "pipe" or "stage" to force one.
     x bf16 [T, 3*dim]; conv_w fp32 [3*dim, 4]; conv_state bf16 with logical shape
     [num_slots, 3*dim, 3] (any strides: the "DS" layout is the plain tensor, the "SD" layout a
     transposed view of [num_slots, 3, 3*dim]); raw_g bf16 [T, heads, D] (kda) or [T, heads] (gdn);

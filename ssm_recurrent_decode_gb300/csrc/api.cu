@@ -96,7 +96,7 @@ int prepare_fused(const gdn_fused_args *a, FusedPlan *plan)
     if (!aligned(a->conv_w, 16) || !aligned(a->state, 16) || !aligned(a->A_log, 4) ||
         !aligned(a->dt_bias, 4) || !aligned(a->norm_w, 4) || (a->conv_b && !aligned(a->conv_b, 4)))
         return GDN_ERR_ALIGN;
-    if (a->kernel < GDN_KERNEL_AUTO || a->kernel > GDN_KERNEL_PIPE) return GDN_ERR_ARG;
+    if (a->kernel < GDN_KERNEL_AUTO || a->kernel > GDN_KERNEL_STAGE) return GDN_ERR_ARG;
     gdn::FusedLaunch &p = plan->p;
     std::memset(&p, 0, sizeof(p));
     p.a = *a;
@@ -126,30 +126,29 @@ int prepare_fused(const gdn_fused_args *a, FusedPlan *plan)
     // four tiles per SM the pipelined kernel wins.
     const bool few_tiles = (int64_t)a->T * a->heads <= 2 * (int64_t)sms;
     bool use_pipe = pipe_ok && pipe_aligned && !few_tiles;
-    if (a->kernel == GDN_KERNEL_PIPE) {
+    // From sixteen tiles per SM one CTA per tile staged in shared memory beat the persistent kernel
+    // (T = 128: 243.8 against 267.4 us; T = 32, 20 tiles per SM: 65.7 against 68.6); at ten and
+    // five per SM it lost (T = 16: 37.2 against 35.6; T = 8: 22.5 against 20.2).
+    bool use_stage = use_pipe && (int64_t)a->T * a->heads >= 16 * (int64_t)sms;
+    if (a->kernel == GDN_KERNEL_PIPE || a->kernel == GDN_KERNEL_STAGE) {
         if (!pipe_ok) return GDN_ERR_SHAPE;
         if (!pipe_aligned) return GDN_ERR_ALIGN;
         use_pipe = true;
+        use_stage = a->kernel == GDN_KERNEL_STAGE;
     } else if (a->kernel == GDN_KERNEL_TILE) {
-        use_pipe = false;
+        use_pipe = use_stage = false;
     }
     plan->use_pipe = use_pipe;
+    plan->use_stage = use_stage;
     plan->sd = sd;
-    plan->sms = sms > 0 ? sms : 152;
     return GDN_OK;
 }
 
 int launch_fused_plan(const FusedPlan &plan, cudaStream_t stream, bool chained)
 {
     if (plan.empty) return GDN_OK;
-    if (plan.use_pipe) {
-        // Many tiles per SM: one CTA per tile, staged in shared memory (T = 128: 243.8 against
-        // 267.4 us for the persistent kernel; T = 32: 65.7 against 68.6). A few tiles per SM: the
-        // persistent kernel (T = 8, five tiles per SM: 20.2 against 22.5).
-        if ((int64_t)plan.p.a.T * plan.p.a.heads >= 8 * (int64_t)plan.sms)
-            return launch_fused_stage(plan.p, plan.sd, stream, chained);
-        return launch_fused_pipe(plan.p, plan.sd, stream, chained);
-    }
+    if (plan.use_stage) return launch_fused_stage(plan.p, plan.sd, stream, chained);
+    if (plan.use_pipe) return launch_fused_pipe(plan.p, plan.sd, stream, chained);
     return launch_fused(plan.p, stream, chained);
 }
 
@@ -198,7 +197,7 @@ int gdn_decode_buffered(const gdn_step_args *args, const int32_t *cache_indices,
     if (!aligned(ring->k_cache, 4 * dtype_size(ring->ring_dtype)) ||
         !aligned(ring->d_cache, dtype_size(ring->ring_dtype)) || !aligned(ring->g_cache, 4))
         return GDN_ERR_ALIGN;
-    if (ring->kernel < GDN_KERNEL_AUTO || ring->kernel > GDN_KERNEL_PIPE) return GDN_ERR_ARG;
+    if (ring->kernel < GDN_KERNEL_AUTO || ring->kernel > GDN_KERNEL_STAGE) return GDN_ERR_ARG;
     const bool tile_ok = gdn::buffered_smem_bytes(ring->L, args->V, args->K) <= 200 * 1024;
     bool pipe_ok = args->K == 128 && args->V == 128 && (ring->L == 1 || ring->L % 4 == 0);
     const size_t es = dtype_size(args->in_dtype);
@@ -207,23 +206,29 @@ int gdn_decode_buffered(const gdn_step_args *args, const int32_t *cache_indices,
         (args->q_stride * (int64_t)es) % 16 == 0 && (args->k_stride * (int64_t)es) % 16 == 0 &&
         (args->v_stride * (int64_t)es) % 16 == 0 && aligned(ring->d_cache, 16) && aligned(ring->k_cache, 16) &&
         aligned(ring->g_cache, 16);
+    int sms = 0;
     if (pipe_ok) {
         int dev = 0, max_smem = 0;
         pipe_ok = cudaGetDevice(&dev) == cudaSuccess &&
                   cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess &&
-                  gdn::buffered_pipe_fits(ring->L, args->in_dtype, ring->ring_dtype, max_smem);
+                  gdn::buffered_pipe_fits(ring->L, args->in_dtype, ring->ring_dtype, max_smem) &&
+                  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess;
     }
-    bool use_pipe;
-    if (ring->kernel == GDN_KERNEL_PIPE) {
+    bool use_pipe, use_stage = false;
+    if (ring->kernel == GDN_KERNEL_PIPE || ring->kernel == GDN_KERNEL_STAGE) {
         if (!pipe_ok) return GDN_ERR_SHAPE;
         if (!pipe_aligned) return GDN_ERR_ALIGN;
         use_pipe = true;
+        use_stage = ring->kernel == GDN_KERNEL_STAGE;
     } else if (ring->kernel == GDN_KERNEL_TILE) {
         if (!tile_ok) return GDN_ERR_SHAPE;
         use_pipe = false;
     } else {
         // At L = 1 every step flushes and the per-tile kernel was faster on GB300 (170.4 against
         // 174.4 us at B = 256); from L = 8 the pipelined kernel is far ahead (96 against 147 us).
+        // One CTA per tile staged in shared memory (GDN_KERNEL_STAGE) measured the same as the
+        // persistent kernel (B = 256: 96.2 against 95.1 us at L = 16, 95.5 against 96.0 at L = 8), so
+        // the persistent kernel stays the default.
         use_pipe = pipe_ok && pipe_aligned && !(ring->L == 1 && tile_ok);
         if (!use_pipe && !tile_ok) return GDN_ERR_SHAPE;
     }
@@ -233,6 +238,7 @@ int gdn_decode_buffered(const gdn_step_args *args, const int32_t *cache_indices,
     p.k_cache = ring->k_cache;
     p.g_cache = ring->g_cache;
     p.write_pos = ring->write_pos;
+    if (use_stage) return gdn::launch_buffered_stage(p, ring->ring_dtype, reinterpret_cast<cudaStream_t>(stream));
     if (use_pipe) return gdn::launch_buffered_pipe(p, ring->ring_dtype, reinterpret_cast<cudaStream_t>(stream));
     return gdn::launch_buffered(p, ring->ring_dtype, reinterpret_cast<cudaStream_t>(stream));
 }

@@ -404,4 +404,202 @@ int launch_buffered_pipe(const StepLaunch &p, int ring_dtype, cudaStream_t strea
     return ring_dtype == GDN_BF16 ? launch_pipe_t<float, bf16>(p, stream) : launch_pipe_t<float, float>(p, stream);
 }
 
+
+// ------------------------------------------------------------------------------------------------
+// One tile per CTA of 256 threads with the same staging: thread 0 reads the row's slot and cursor
+// and bulk-copies the 64 KB checkpoint tile, the q/k/v rows and the tile's p ring records (delta
+// rows, key rows, log-decays) into the CTA's shared memory on one mbarrier; the arithmetic is the
+// consumer group's above with block barriers in place of the group's mbarrier. 73 KB of shared
+// memory at L = 16 with a bf16 ring: three CTAs per SM, each with its copies in flight, and
+// consecutive launches overlap like any per-tile kernel.
+// ------------------------------------------------------------------------------------------------
+template <typename Tin, typename Tring>
+__global__ void __launch_bounds__(kThreads, 3) buffered_stage_kernel(const __grid_constant__ StepLaunch P)
+{
+    constexpr int K = 128, V = 128;
+    using TL = Tile<128, 16, kWarps>;
+    extern __shared__ __align__(128) unsigned char stage[];
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag, zero_flag, s_status, s_slot, s_p;
+
+    const gdn_step_args &a = P.a;
+    const int HV = a.HV, L = P.L, G = P.G;
+    const int tile = blockIdx.x, b = tile / HV, hv = tile - b * HV, h = hv / G;
+    const int lane = threadIdx.x & 31, tid = threadIdx.x;
+    const PipeLayout lay(L, sizeof(Tin), sizeof(Tring));
+    PipeMeta *meta = reinterpret_cast<PipeMeta *>(stage + lay.meta);
+    const size_t out_base = ((size_t)b * HV + hv) * V;
+    const uint32_t es = sizeof(Tin), rs = sizeof(Tring);
+
+    if (tid == 0) {
+        int slot = b, status = 0;
+        if (P.idx) {
+            slot = P.idx[b];
+            if (slot == P.pad) status = 1;
+            else if (slot < 0 || slot >= a.num_slots) status = 2;
+        }
+        int p = P.write_pos[b];
+        if (status == 0 && (p < 0 || p >= L)) status = 3;
+        if (status == 0 && (!step_tile_in_range(a, b, hv, h, slot) || !ring_in_range(a, L, slot, hv, h, p)))
+            status = 4;   // an index out of range (debug build): skipped, nothing written
+        if (status != 0) p = 0;
+        s_status = status;
+        s_slot = slot;
+        s_p = p;
+        abort_flag = 0;
+        zero_flag = 0;
+        if (status == 0) {
+            mbar_init(&bar, 1);
+            fence_barrier_init();
+            const uint32_t gbytes = p > 0 ? round16((uint32_t)p * 4u) : 0u;
+            mbar_arrive_expect_tx(&bar, 128u * 128u * 4u + 3u * 128u * es + 2u * (uint32_t)p * 128u * rs + gbytes);
+            const float *S = static_cast<const float *>(a.state) + ((size_t)slot * HV + hv) * (size_t)(V * K);
+            bulk_g2s_hint(stage, S, 128u * 128u * 4u, &bar, policy_evict_first());
+            bulk_g2s(stage + lay.q, static_cast<const Tin *>(a.q) + (size_t)b * a.q_stride + (size_t)h * K, 128u * es, &bar);
+            bulk_g2s(stage + lay.k, static_cast<const Tin *>(a.k) + (size_t)b * a.k_stride + (size_t)h * K, 128u * es, &bar);
+            bulk_g2s(stage + lay.v, static_cast<const Tin *>(a.v) + (size_t)b * a.v_stride + (size_t)hv * V, 128u * es, &bar);
+            if (p > 0) {
+                const Tring *dr = static_cast<const Tring *>(P.d_cache) + ((size_t)slot * HV + hv) * L * V;
+                const Tring *kr = static_cast<const Tring *>(P.k_cache) + ((size_t)slot * a.H + h) * L * K;
+                bulk_g2s(stage + lay.d, dr, (uint32_t)p * 128u * rs, &bar);
+                bulk_g2s(stage + lay.kr, kr, (uint32_t)p * 128u * rs, &bar);
+                bulk_g2s(meta->gr, P.g_cache + ((size_t)slot * HV + hv) * L, gbytes, &bar);
+            }
+        }
+    }
+    float g, beta;
+    step_gates<Tin>(a, b, hv, g, beta);
+    TL t;
+    t.init();
+    __syncthreads();
+    const int status = s_status, slot = s_slot, p = s_p;
+    if (status != 0) {   // uniform over the CTA
+        if ((status == 2 || status == 3) && tid == 0)
+            raise_flag(a.err_flags, status == 2 ? GDN_DEVERR_BAD_INDEX : GDN_DEVERR_BAD_WRITE_POS);
+        if (status != 4 && tid < V) store_out(a.out, a.out_dtype, out_base + tid, 0.f);
+        return;
+    }
+    if (!mbar_wait_warp(&bar, 0u, &abort_flag, kWaitLimit)) {
+        if (lane == 0) raise_flag(a.err_flags, GDN_DEVERR_TIMEOUT);
+        if (tid == 0) mbar_wait(&bar, 0u, &zero_flag, kWaitLimit);   // copies still in flight land first
+        return;
+    }
+    const bool flush = p == L - 1;
+    const Tin *qs = reinterpret_cast<const Tin *>(stage + lay.q);
+    const Tin *ks = reinterpret_cast<const Tin *>(stage + lay.k);
+    const Tin *vs = reinterpret_cast<const Tin *>(stage + lay.v);
+    const Tring *ds = reinterpret_cast<const Tring *>(stage + lay.d);
+    const Tring *krs = reinterpret_cast<const Tring *>(stage + lay.kr);
+    const float *Ss = reinterpret_cast<const float *>(stage);
+
+    const float4 kh = l2_normalise4<32>(load4(ks + t.col), a.use_qk_l2norm != 0, 1.f);
+    const float4 qh = l2_normalise4<32>(load4(qs + t.col), a.use_qk_l2norm != 0, P.scale);
+    const float kq = group_sum<32>(dot4(kh, qh));
+    // record scalars, one warp per record
+    for (int j = t.warp; j < p; j += kWarps) {
+        const float4 kj = load4(krs + (size_t)j * K + t.col);
+        const float dk = group_sum<32>(dot4(kj, kh));
+        const float dq = group_sum<32>(dot4(kj, qh));
+        if (lane == 0) {
+            float acc = g;
+            for (int i = j + 1; i < p; ++i) acc += meta->gr[i];
+            const float c = expf(acc);
+            meta->c[j] = c;
+            meta->alpha[j] = c * dk;
+            meta->gamma[j] = c * dq;
+        }
+    }
+    float gsum = g;
+    for (int i = 0; i < p; ++i) gsum += meta->gr[i];
+    const float Gam = expf(gsum);
+
+    // the two dots, straight from the staged tile (16 rows x 4 columns per lane)
+    const int row0 = t.row(0, 0);
+    const int r_own = t.row(0, t.owned_chunk(0));
+    const float vv = t.holds_k_dot() ? to_f32(vs[r_own]) : 0.f;
+    float x[TL::N];
+    {
+        const float4 gk = scale4(kh, Gam), gq = scale4(qh, Gam);
+#pragma unroll
+        for (int i = 0; i < TL::R; ++i) {
+            const float4 srow = *reinterpret_cast<const float4 *>(Ss + (size_t)(row0 + i) * K + t.col);
+            x[i] = dot4(srow, gk);
+            x[TL::R + i] = dot4(srow, gq);
+        }
+    }
+    t.reduce_scatter(x);
+    __syncthreads();   // the record scalars are complete
+    {
+        const float *coef = t.holds_k_dot() ? meta->alpha : meta->gamma;
+        float acc = x[0];
+        for (int j = 0; j < p; ++j) acc = fmaf(ring_in(ds[(size_t)j * V + r_own]), coef[j], acc);
+        x[0] = acc;
+    }
+    float dv[TL::M];
+    dv[0] = beta * (vv - x[0]);
+    const float dq = t.delta_for_q(dv[0]);
+    Tring *dring = static_cast<Tring *>(P.d_cache) + ((size_t)slot * HV + hv) * L * V;
+    if (t.writer()) {
+        if (t.holds_k_dot())
+            dring[(size_t)p * V + r_own] = ring_out<Tring>(dv[0]);
+        else
+            store_out(a.out, a.out_dtype, out_base + r_own, fmaf(dq, kq, x[0]));
+    }
+    if (flush) {
+        // S = Gamma S_c + delta k^T + sum_j d_j (c_j k_j)^T, eight rows at a time
+        float *S = static_cast<float *>(a.state) + ((size_t)slot * HV + hv) * (size_t)(V * K);
+#pragma unroll
+        for (int i8 = 0; i8 < TL::R; i8 += 8) {
+            float4 acc[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 srow = *reinterpret_cast<const float4 *>(Ss + (size_t)(row0 + i8 + i) * K + t.col);
+                acc[i] = axpby4(Gam, srow, t.delta_of(dv, i8 + i), kh);
+            }
+            for (int j = 0; j < p; ++j) {
+                const float4 kj = scale4(load4(krs + (size_t)j * K + t.col), meta->c[j]);
+                float dj[8];
+                load8(ds + (size_t)j * V + row0 + i8, dj);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    acc[i].x = fmaf(dj[i], kj.x, acc[i].x);
+                    acc[i].y = fmaf(dj[i], kj.y, acc[i].y);
+                    acc[i].z = fmaf(dj[i], kj.z, acc[i].z);
+                    acc[i].w = fmaf(dj[i], kj.w, acc[i].w);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) st_stream(S + (size_t)(row0 + i8 + i) * K + t.col, acc[i]);
+        }
+    }
+    // this step's key record (first value head of the group) and log-decay record
+    if (hv % G == 0 && t.warp == 0) {
+        Tring *dst = static_cast<Tring *>(P.k_cache) + (((size_t)slot * a.H + h) * L + p) * K + t.col;
+        dst[0] = ring_out<Tring>(kh.x);
+        dst[1] = ring_out<Tring>(kh.y);
+        dst[2] = ring_out<Tring>(kh.z);
+        dst[3] = ring_out<Tring>(kh.w);
+    }
+    if (tid == 0) P.g_cache[((size_t)slot * HV + hv) * L + p] = g;
+}
+
+template <typename Tin, typename Tring>
+static int launch_stage_t(const StepLaunch &p, cudaStream_t stream)
+{
+    const PipeLayout lay(p.L, sizeof(Tin), sizeof(Tring));
+    const size_t smem = lay.stage;
+    auto kern = buffered_stage_kernel<Tin, Tring>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return GDN_ERR_LAUNCH;
+    kern<<<(unsigned)(p.a.B * p.a.HV), kThreads, smem, stream>>>(p);
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
+}
+
+int launch_buffered_stage(const StepLaunch &p, int ring_dtype, cudaStream_t stream)
+{
+    if (p.a.in_dtype == GDN_BF16)
+        return ring_dtype == GDN_BF16 ? launch_stage_t<bf16, bf16>(p, stream) : launch_stage_t<bf16, float>(p, stream);
+    return ring_dtype == GDN_BF16 ? launch_stage_t<float, bf16>(p, stream) : launch_stage_t<float, float>(p, stream);
+}
+
 }  // namespace gdn

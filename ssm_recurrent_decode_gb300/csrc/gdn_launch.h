@@ -34,9 +34,9 @@ struct FusedLaunch {
 struct FusedPlan {
     FusedLaunch p;
     bool empty;      // T == 0: nothing to launch
-    bool use_pipe;   // the persistent pipelined kernel
+    bool use_pipe;   // the persistent pipelined kernel (or, with use_stage, the staged one)
+    bool use_stage;  // one CTA per tile staged in shared memory
     bool sd;         // its conv state is in the SD layout
-    int sms;         // SMs of the device (the pipelined and staged kernels' choice)
 };
 
 // The host checks of gdn_decode_fused (the same status codes) and its kernel choice; no CUDA launch.
@@ -67,6 +67,9 @@ size_t buffered_smem_bytes(int L, int V, int K);
 int launch_buffered_pipe(const StepLaunch &p, int ring_dtype, cudaStream_t stream);
 // Whether its two-stage shared-memory footprint fits in max_smem bytes per CTA.
 bool buffered_pipe_fits(int L, int in_dtype, int ring_dtype, int max_smem);
+// The same step with one tile per CTA staged in shared memory (the pipelined kernel's
+// requirements; one stage of shared memory per CTA).
+int launch_buffered_stage(const StepLaunch &p, int ring_dtype, cudaStream_t stream);
 
 // The persistent, warp-specialised fused kernel (head_dim 128; conv state in the DS layout, or in
 // the SD layout when sd is true).

@@ -96,8 +96,9 @@ def test_step_writes_only_its_buffers(B, K, V, sdt):
 # ------------------------------------------------------------------------------------------------
 # buffered decode, pipelined kernel
 # ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("kernel", ["pipe", "stage"])
 @pytest.mark.parametrize("L,start", [(8, 0), (8, 7), (16, 5)])
-def test_buffered_pipe_writes_only_its_buffers(L, start):
+def test_buffered_pipe_writes_only_its_buffers(L, start, kernel):
     B, H, HV, K, V = 8, 16, 32, 128, 128
     seed = 720 + L + start
     x = torch.empty((B, 2 * H * K + HV * V), dtype=torch.bfloat16, device="cuda")
@@ -121,11 +122,11 @@ def test_buffered_pipe_writes_only_its_buffers(L, start):
     q, k, v = gdn.split_mixed_qkv(x, H, HV, K, V)
     plain = [t.clone() for t in (state0, out0, d0, k0, g0)]
     gdn.gdn_decode_buffered(q, k, v, plain[0], plain[1], plain[2], plain[3], plain[4], wp, H=H, a=a,
-                            b=b, A_log=A_log, dt_bias=dt_bias, kernel="pipe")
+                            b=b, A_log=A_log, dt_bias=dt_bias, kernel=kernel)
     g = [Guarded(t) for t in (state0, out0, d0, k0, g0)]
     ge = Guarded(torch.zeros(1, dtype=torch.int32, device="cuda"))
     gdn.gdn_decode_buffered(q, k, v, g[0].t, g[1].t, g[2].t, g[3].t, g[4].t, wp, H=H, a=a, b=b,
-                            A_log=A_log, dt_bias=dt_bias, err_flags=ge.t, kernel="pipe")
+                            A_log=A_log, dt_bias=dt_bias, err_flags=ge.t, kernel=kernel)
     assert all(x.intact() for x in g) and ge.intact()
     for x, p in zip(g, plain):
         assert _same(x.t, p)
@@ -135,9 +136,10 @@ def test_buffered_pipe_writes_only_its_buffers(L, start):
 # ------------------------------------------------------------------------------------------------
 # fused decode, pipelined kernel (DS and SD conv-state layouts)
 # ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("kernel", ["pipe", "stage"])
 @pytest.mark.parametrize("layout", ["DS", "SD"])
 @pytest.mark.parametrize("T", [4, 9])
-def test_fused_pipe_writes_only_its_buffers(layout, T):
+def test_fused_pipe_writes_only_its_buffers(layout, T, kernel):
     heads, D = 96, 128
     dim = heads * D
     seed = 740 + T
@@ -163,7 +165,7 @@ def test_fused_pipe_writes_only_its_buffers(layout, T):
     def call(state, cs, out, err=None):
         gdn.gdn_decode_fused(x, common["conv_w"], view(cs), common["raw_g"], common["raw_beta"],
                              common["A_log"], common["dt_bias"], state, idx, gate, common["norm_w"], out,
-                             pad_slot_id=0, err_flags=err, kernel="pipe")
+                             pad_slot_id=0, err_flags=err, kernel=kernel)
 
     plain = [state0.clone(), cs_phys.clone(), out0.clone()]
     call(*plain)

@@ -70,7 +70,7 @@ def test_step(B, K, V, sdt, chained):
     _both(run)
 
 
-@pytest.mark.parametrize("kernel,L", [("pipe", 8), ("tile", 8), ("tile", 3)])
+@pytest.mark.parametrize("kernel,L", [("pipe", 8), ("stage", 8), ("stage", 16), ("tile", 8), ("tile", 3)])
 def test_buffered(kernel, L):
     B, H, HV, K, V = 8, 16, 32, 128, 128
     seed = 820 + L
@@ -101,8 +101,8 @@ def test_buffered(kernel, L):
     _both(run)
 
 
-@pytest.mark.parametrize("T,layout,kernel", [(4, "DS", "pipe"), (4, "SD", "pipe"), (2, "DS", "tile"),
-                                             (3, "SD", "tile")])
+@pytest.mark.parametrize("T,layout,kernel", [(4, "DS", "pipe"), (4, "SD", "pipe"), (4, "DS", "stage"),
+                                             (4, "SD", "stage"), (2, "DS", "tile"), (3, "SD", "tile")])
 def test_fused(T, layout, kernel):
     heads, D = 96, 128
     seed = 840 + T

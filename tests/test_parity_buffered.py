@@ -79,17 +79,18 @@ def test_exact_ring_tiny_two_cycles(L):
 
 
 @pytest.mark.parametrize("K,G,kernel", [(32, 1, "auto"), (64, 3, "auto"), (128, 2, "tile"),
-                                        (128, 2, "pipe"), (128, 3, "pipe")])
+                                        (128, 2, "pipe"), (128, 3, "pipe"), (128, 2, "stage"),
+                                        (128, 3, "stage")])
 def test_exact_ring_shapes_mixed_phases(K, G, kernel):
     """Rows at different cursors in one call (each row's own phase), records of one q/k head
-    shared by G value heads; at K = V = 128 both the per-tile and the pipelined kernel."""
+    shared by G value heads; at K = V = 128 the per-tile, the pipelined and the staged kernel."""
     H = 2
     w = _run_buffered(3, H, H * G, K, K, 4, "f32", "f32", seed=K + G, steps=7, start_pos=[0, 1, 3],
                       indexed=True, kernel=kernel)
     assert max(w.values()) <= 1e-5, w
 
 
-@pytest.mark.parametrize("kernel", ["auto", "tile", "pipe"])
+@pytest.mark.parametrize("kernel", ["auto", "tile", "pipe", "stage"])
 @pytest.mark.parametrize("L", [1, 8, 16])
 def test_bf16_ring_packed_shapes(L, kernel):
     """The packed decode shapes (H=16, HV=32, K=V=128) with bf16 inputs, outputs and records over
@@ -108,10 +109,20 @@ def test_pipelined_kernel_many_tiles_per_cta():
     assert w["out"] <= 2e-2 and w["state"] <= 2e-2 and w["ring"] <= 2e-2, w
 
 
-def test_pipelined_kernel_exact_ring_fp32_inputs():
+@pytest.mark.parametrize("kernel", ["pipe", "stage"])
+def test_pipelined_kernel_exact_ring_fp32_inputs(kernel):
     w = _run_buffered(6, 4, 8, 128, 128, 4, "f32", "f32", seed=92, steps=9, indexed=True,
-                      start_pos=[0, 1, 2, 3, 0, 1], kernel="pipe")
+                      start_pos=[0, 1, 2, 3, 0, 1], kernel=kernel)
     assert max(w.values()) <= 1e-5, w
+
+
+def test_staged_kernel_many_tiles():
+    """1536 tiles, one CTA per tile staged in shared memory; rows at mixed cursors and a pad row,
+    two cycles of L = 8."""
+    B = 48
+    w = _run_buffered(B, 16, 32, 128, 128, 8, "bf16", "bf16", seed=93, steps=17, indexed=True,
+                      start_pos=[(5 * r) % 8 for r in range(B)], pad_rows=(7,), kernel="stage")
+    assert w["out"] <= 2e-2 and w["state"] <= 2e-2 and w["ring"] <= 2e-2, w
 
 
 def test_pad_rows_are_skipped():

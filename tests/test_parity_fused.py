@@ -89,27 +89,28 @@ def _run_fused(T, heads, D, *, layout="DS", gate_kind="kda", form=0, act="silu",
     return worst
 
 
-@pytest.mark.parametrize("kernel", ["tile", "pipe"])
+@pytest.mark.parametrize("kernel", ["tile", "pipe", "stage"])
 @pytest.mark.parametrize("layout", ["DS", "SD"])
 @pytest.mark.parametrize("T", [1, 2, 4, 8])
 def test_kda_config_shapes(layout, T, kernel):
     """The fused KDA decode shapes: 96 heads x 128, conv width 4, lower bound -5, silu gate, at
-    the token counts where the library picks the per-tile kernel (one CTA per (token, head)); both
-    kernels forced."""
+    the token counts where the library picks the per-tile kernel (one CTA per (token, head)); the
+    per-tile, pipelined and staged kernels forced."""
     w = _run_fused(T, 96, 128, layout=layout, seed=T, kernel=kernel)
     assert w["out"] <= 2e-2 and w["state"] <= 1e-5, w
 
 
-@pytest.mark.parametrize("kernel", ["tile", "pipe"])
+@pytest.mark.parametrize("kernel", ["tile", "pipe", "stage", "auto"])
 def test_kda_32_tokens_sampled_rows(kernel):
-    """3072 tiles: the pipelined kernel walks about twenty per CTA through its stages."""
+    """3072 tiles: the pipelined kernel walks about twenty per CTA through its stages; the library's
+    own choice at this size is one CTA per tile staged in shared memory."""
     w = _run_fused(32, 96, 128, seed=32, sample_rows=[0, 7, 19, 31], kernel=kernel, steps=2)
     assert w["out"] <= 2e-2 and w["state"] <= 1e-5, w
 
 
 def test_kda_full_size_sampled_rows():
-    """The benchmark's launch: 128 tokens x 96 heads (12288 tiles, the pipelined kernel's default
-    choice, about 80 tiles per persistent CTA), sampled token rows against the oracle."""
+    """The benchmark's launch: 128 tokens x 96 heads (12288 tiles; the library's choice is one CTA
+    per tile staged in shared memory), sampled token rows against the oracle."""
     w = _run_fused(128, 96, 128, seed=128, sample_rows=[0, 41, 90, 127])
     assert w["out"] <= 2e-2 and w["state"] <= 1e-5, w
 
@@ -130,7 +131,7 @@ def test_gdn_gate_and_small_heads(D, kernel):
     assert w["out"] <= 2e-2 and w["state"] <= 1e-5, w
 
 
-@pytest.mark.parametrize("D,kernel", [(64, "auto"), (128, "pipe"), (128, "tile")])
+@pytest.mark.parametrize("D,kernel", [(64, "auto"), (128, "pipe"), (128, "tile"), (128, "stage")])
 def test_null_slot_rows_are_skipped(D, kernel):
     w = _run_fused(6, 4, D, seed=9, pad_rows=(0, 4), steps=2, kernel=kernel)
     assert w["out"] <= 2e-2 and w["state"] <= 1e-5, w
