@@ -129,10 +129,16 @@ __global__ void __launch_bounds__(kMambaThreads, kMambaGsCtasPerSmBound) mamba_g
     const int sub = (int)(tid % LPR);
     const int n0 = sub * EPL;
     long long r = tid / LPR;
+    // the row's state and its per-row scalars (x, dt and, for the lane that writes y, z) are
+    // loaded one row ahead, so that no load from HBM waits in the computing row's path
     float4 c0 = make_float4(0.f, 0.f, 0.f, 0.f), c1 = c0;
+    float cx = 0.f, cdt = 0.f, cz = 0.f;
     if (r < rows) {
         c0 = ld_stream(P.h + (size_t)r * N + n0);
         c1 = ld_stream(P.h + (size_t)r * N + n0 + 4);
+        cx = ld1<Tin>(P.x, (size_t)r);
+        cdt = ld1<Tin>(P.dt, (size_t)r);
+        if (P.z && sub == 0) cz = ld1<Tin>(P.z, (size_t)r);
     }
     // every lane of the warp stays in the loop until none of its rows is left (the group sums
     // take all 32 lanes); lanes past the end compute on zeros and store nothing
@@ -141,14 +147,17 @@ __global__ void __launch_bounds__(kMambaThreads, kMambaGsCtasPerSmBound) mamba_g
         if (!__any_sync(0xFFFFFFFFu, live)) break;
         const long long rn = r + rstep;
         float4 n0v = make_float4(0.f, 0.f, 0.f, 0.f), n1v = n0v;
+        float nx = 0.f, ndt = 0.f, nz = 0.f;
         if (rn < rows) {
             n0v = ld_stream(P.h + (size_t)rn * N + n0);
             n1v = ld_stream(P.h + (size_t)rn * N + n0 + 4);
+            nx = ld1<Tin>(P.x, (size_t)rn);
+            ndt = ld1<Tin>(P.dt, (size_t)rn);
+            if (P.z && sub == 0) nz = ld1<Tin>(P.z, (size_t)rn);
         }
         const long long rr = live ? r : 0;
         const int b = (int)(rr / D), d = (int)(rr - (long long)b * D);
-        const float x = live ? ld1<Tin>(P.x, (size_t)rr) : 0.f;
-        const float dt = live ? ld1<Tin>(P.dt, (size_t)rr) : 0.f;
+        const float x = cx, dt = cdt;
         const float dtx = dt * x;
         float hv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
         float y = 0.f;
@@ -173,10 +182,7 @@ __global__ void __launch_bounds__(kMambaThreads, kMambaGsCtasPerSmBound) mamba_g
         }
         if (live && sub == 0) {
             if (P.Dskip) y = fmaf(P.Dskip[d], x, y);
-            if (P.z) {
-                const float z = ld1<Tin>(P.z, (size_t)r);
-                y *= z * sigmoid_f(z);
-            }
+            if (P.z) y *= cz * sigmoid_f(cz);
             if (P.out_dtype == GDN_BF16)
                 static_cast<bf16 *>(P.y)[r] = __float2bfloat16_rn(y);
             else
@@ -184,6 +190,9 @@ __global__ void __launch_bounds__(kMambaThreads, kMambaGsCtasPerSmBound) mamba_g
         }
         c0 = n0v;
         c1 = n1v;
+        cx = nx;
+        cdt = ndt;
+        cz = nz;
     }
 }
 
