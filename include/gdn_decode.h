@@ -260,10 +260,11 @@ int gdn_selftest_bounded_wait(int32_t *err_flags, int64_t limit_cycles, int32_t 
 const char *gdn_strerror(int status);
 
 /* ABI checks for bindings: sizeof of the args structs (which: 0 step, 1 ring, 2 fused, 3 the
- * decode projection's gdn_gemv_args of gdn_gemv.h, 4 gdn_front_args of gdn_front.h). */
+ * decode projection's gdn_gemv_args of gdn_gemv.h, 4 gdn_front_args of gdn_front.h, 5
+ * mamba_decode_args of mamba_decode.h). */
 size_t gdn_abi_struct_size(int which);
 
-/* Library ABI version (incremented on any change of the args structs; currently 6). */
+/* Library ABI version (incremented on any change of the args structs; currently 7). */
 int gdn_abi_version(void);
 
 #ifdef __cplusplus

@@ -41,6 +41,9 @@ typedef struct mamba_decode_args {
     float *h;               /* [B, D, N] fp32 state: read; updated in place when h_out is NULL */
     float *h_out;           /* [B, D, N] or NULL: where the new state goes (may not overlap h) */
     void *y;                /* [B, D] out_dtype */
+    int32_t *err_flags;     /* optional device word: GDN_DEVERR_TIMEOUT is ORed in when a bounded
+                               wait of the staged kernel gives up (its rows are then left as they
+                               were); NULL: not reported */
 } mamba_decode_args;
 
 /*

@@ -41,7 +41,7 @@ GDN_ACT_SILU, GDN_ACT_SIGMOID = 0, 1
 GDN_DEVERR_BAD_INDEX, GDN_DEVERR_BAD_WRITE_POS, GDN_DEVERR_TIMEOUT = 0x1, 0x2, 0x4
 GDN_DEVERR_RANGE = 0x8
 GDN_KERNEL = {"auto": 0, "tile": 1, "pipe": 2, "stage": 3}
-ABI_VERSION = 6
+ABI_VERSION = 7
 
 # every function the header declares
 EXPORTS = ("gdn_decode_step", "gdn_decode_step_indexed", "gdn_decode_buffered", "gdn_decode_fused",
@@ -90,7 +90,7 @@ class GdnFrontArgs(ctypes.Structure):
 class MambaArgs(ctypes.Structure):
     _fields_ = [("B", _i32), ("D", _i32), ("N", _i32), ("in_dtype", _i32), ("out_dtype", _i32),
                 ("x", _vp), ("dt", _vp), ("A", _vp), ("Bm", _vp), ("Cm", _vp), ("Dskip", _vp),
-                ("z", _vp), ("h", _vp), ("h_out", _vp), ("y", _vp)]
+                ("z", _vp), ("h", _vp), ("h_out", _vp), ("y", _vp), ("err_flags", _vp)]
 
 
 class GemvArgs(ctypes.Structure):
@@ -151,9 +151,9 @@ def _load(path: str):
     L.gdn_strerror.restype = ctypes.c_char_p
     L.gdn_abi_struct_size.argtypes = [ctypes.c_int]
     L.gdn_abi_struct_size.restype = ctypes.c_size_t
-    sizes = [L.gdn_abi_struct_size(i) for i in range(5)]
+    sizes = [L.gdn_abi_struct_size(i) for i in range(6)]
     want = [ctypes.sizeof(GdnStepArgs), ctypes.sizeof(GdnRingArgs), ctypes.sizeof(GdnFusedArgs),
-            ctypes.sizeof(GemvArgs), ctypes.sizeof(GdnFrontArgs)]
+            ctypes.sizeof(GemvArgs), ctypes.sizeof(GdnFrontArgs), ctypes.sizeof(MambaArgs)]
     if sizes != want or L.gdn_abi_version() != ABI_VERSION:
         raise RuntimeError(f"libgdn_decode.so ABI mismatch: struct sizes {sizes} vs {want}")
     return L
@@ -588,11 +588,11 @@ def fused_kda_decode(x, weight, bias, conv_state, raw_g, raw_beta, A_log, dt_bia
 
 
 def mamba_selective_scan_decode(x, dt, A, Bm, Cm, h, y, *, Dskip=None, z=None, h_out=None,
-                                stream=None, prepare=False):
+                                err_flags=None, stream=None, prepare=False):
     """Mamba-1 selective-scan decode step (declared in include/mamba_decode.h).
     x, dt: [B, D] and Bm, Cm: [B, N] (fp32 or bf16, one dtype); A: [D, N] fp32; Dskip: [D] fp32 or
     None; z: [B, D] or None; h: [B, D, N] fp32 state, updated in place unless h_out (same shape)
-    is given; y: [B, D] fp32 or bf16."""
+    is given; y: [B, D] fp32 or bf16; err_flags: an int32 CUDA tensor of one element or None."""
     torch = _torch()
     B, D = x.shape
     N = A.shape[1]
@@ -612,6 +612,7 @@ def mamba_selective_scan_decode(x, dt, A, Bm, Cm, h, y, *, Dskip=None, z=None, h
     m.h = _ptr(_dense(h, "h"), "h", torch.float32)
     m.h_out = _ptr(None if h_out is None else _dense(h_out, "h_out"), "h_out", torch.float32)
     m.y = _ptr(_dense(y, "y"), "y")
+    m.err_flags = _ptr(err_flags, "err_flags", torch.int32)
     return _run_or_prepare("mamba_selective_scan_decode", (ctypes.byref(m),), (m,), stream, prepare, y)
 
 

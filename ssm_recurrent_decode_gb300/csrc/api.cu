@@ -8,10 +8,11 @@
 #include "gdn_front.h"
 #include "gdn_gemv.h"
 #include "gdn_launch.h"
+#include "mamba_decode.h"
 
 namespace {
 
-constexpr int kAbiVersion = 6;
+constexpr int kAbiVersion = 7;
 
 bool k_supported(int K) { return K == 16 || K == 32 || K == 64 || K == 128; }
 bool dtype_ok(int d) { return d == GDN_F32 || d == GDN_BF16; }
@@ -274,6 +275,7 @@ size_t gdn_abi_struct_size(int which)
     case 2: return sizeof(gdn_fused_args);
     case 3: return sizeof(gdn_gemv_args);
     case 4: return sizeof(gdn_front_args);
+    case 5: return sizeof(mamba_decode_args);
     default: return 0;
     }
 }

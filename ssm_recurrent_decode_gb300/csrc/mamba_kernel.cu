@@ -13,6 +13,7 @@
 #include <cstdint>
 
 #include "gdn_common.cuh"
+#include "gdn_pipe.cuh"
 #include "mamba_decode.h"
 
 namespace gdn {
@@ -196,18 +197,140 @@ __global__ void __launch_bounds__(kMambaThreads, kMambaGsCtasPerSmBound) mamba_g
     }
 }
 
+// Staged form for N = 16 .. 128 (powers of two) and large batches: one CTA per block of four batch
+// rows b0 .. b0 + 3 by RPP consecutive channels d0 .. (32 KB of state, four contiguous runs of RPP
+// state rows). Thread 0 bulk-copies the four runs and the four B and C rows (cp.async.bulk,
+// completion on one mbarrier) into shared memory as the CTA starts; meanwhile every thread loads
+// the eight A entries of its channel, which all four batch rows share, and the x, dt and z scalars
+// of its four rows. The update then reads only shared memory and registers, one batch row per
+// pass, and stores with streaming stores, so a CTA's shared memory is busy for the copy and a short
+// arithmetic phase, not for round trips to L2 (58 registers, four CTAs per SM: 128 KB of copies in
+// flight per SM). An earlier form, one block of consecutive rows per CTA with the A, B and C rows
+// read from L2 during the update, was slower than the grid-stride form (158.7 against 142.0 us at
+// B = 1024, N = 64), and bounding this one to five CTAs per SM (48 registers, a few spilled) lost
+// 2-8%. The wait is bounded: on a timeout the CTA raises
+// GDN_DEVERR_TIMEOUT in err_flags, thread 0 waits (bounded) for its copies, and the block's rows are
+// left as they were.
+constexpr long long kMambaWaitLimit = 1LL << 31;   // SM clock cycles, about one second
+constexpr uint32_t kMambaBlockBytes = 32768u;
+constexpr int kMambaRowsPerBlock = 4;              // batch rows of a block, one per pass
+
+template <int NP, typename Tin>
+__global__ void __launch_bounds__(kMambaThreads) mamba_stage_kernel(const __grid_constant__ mamba_decode_args P)
+{
+    constexpr int EPL = 8;
+    constexpr int LPR = NP / EPL;                    // lanes per state row
+    constexpr int RPP = kMambaThreads / LPR;         // channels of a block
+    constexpr int NB = kMambaRowsPerBlock;
+    static_assert(NB * RPP * NP * 4 == (int)kMambaBlockBytes, "a block is 32 KB of state");
+    __shared__ __align__(128) float hs[NB * RPP * NP];
+    __shared__ __align__(16) Tin bs[NB * NP];
+    __shared__ __align__(16) Tin cs[NB * NP];
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag, zero_flag;
+    const int D = P.D;
+    const int dblocks = (D + RPP - 1) / RPP;
+    const int bblk = blockIdx.x / dblocks, dblk = blockIdx.x - bblk * dblocks;
+    const int b0 = bblk * NB, d0 = dblk * RPP;
+    const int nb = P.B - b0 < NB ? P.B - b0 : NB, nd = D - d0 < RPP ? D - d0 : RPP;
+    const int sub = threadIdx.x % LPR, n0 = sub * EPL, lrow = threadIdx.x / LPR;
+    const bool dlive = lrow < nd;
+    const int d = d0 + (dlive ? lrow : 0);
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        zero_flag = 0;
+        fence_barrier_init();
+        const uint32_t run = (uint32_t)nd * NP * 4u, brow = (uint32_t)nb * NP * (uint32_t)sizeof(Tin);
+        mbar_arrive_expect_tx(&bar, (uint32_t)nb * run + 2u * brow);
+        const uint64_t pol = policy_evict_first();
+        for (int p = 0; p < nb; ++p)
+            bulk_g2s_hint(hs + p * RPP * NP, P.h + ((size_t)(b0 + p) * D + d0) * NP, run, &bar, pol);
+        bulk_g2s(bs, static_cast<const Tin *>(P.Bm) + (size_t)b0 * NP, brow, &bar);
+        bulk_g2s(cs, static_cast<const Tin *>(P.Cm) + (size_t)b0 * NP, brow, &bar);
+    }
+    // this channel's A entries and the scalars of its four rows, while the copies are in flight
+    const float4 a_lo = *reinterpret_cast<const float4 *>(P.A + (size_t)d * NP + n0);
+    const float4 a_hi = *reinterpret_cast<const float4 *>(P.A + (size_t)d * NP + n0 + 4);
+    const float av[8] = {a_lo.x, a_lo.y, a_lo.z, a_lo.w, a_hi.x, a_hi.y, a_hi.z, a_hi.w};
+    float xs[NB], dts[NB], zs[NB];
+#pragma unroll
+    for (int p = 0; p < NB; ++p) {
+        const bool live = dlive && p < nb;
+        const size_t r = (size_t)(b0 + p) * D + d;
+        xs[p] = live ? ld1<Tin>(P.x, r) : 0.f;
+        dts[p] = live ? ld1<Tin>(P.dt, r) : 0.f;
+        zs[p] = live && P.z && sub == 0 ? ld1<Tin>(P.z, r) : 0.f;
+    }
+    __syncthreads();   // the barrier is initialised before anyone waits on it
+    if (!mbar_wait_warp(&bar, 0u, &abort_flag, kMambaWaitLimit)) {
+        if ((threadIdx.x & 31) == 0) raise_flag(P.err_flags, GDN_DEVERR_TIMEOUT);
+        if (threadIdx.x == 0) mbar_wait(&bar, 0u, &zero_flag, kMambaWaitLimit);   // the copies land first
+        return;
+    }
+    float *out = P.h_out ? P.h_out : P.h;
+#pragma unroll
+    for (int p = 0; p < NB; ++p) {
+        const bool live = dlive && p < nb;   // rows past the edges: computed, never stored
+        const int hrow = p * RPP + (dlive ? lrow : 0);
+        const float x = xs[p], dt = dts[p], dtx = dt * x;
+        float hv[8];
+        float y = 0.f;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const float4 h4 = *reinterpret_cast<const float4 *>(hs + hrow * NP + n0 + 4 * q);
+            const float4 b4 = load4(bs + p * NP + n0 + 4 * q), c4 = load4(cs + p * NP + n0 + 4 * q);
+            const float hq[4] = {h4.x, h4.y, h4.z, h4.w}, bq[4] = {b4.x, b4.y, b4.z, b4.w}, cq[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                // rows past the edges read whatever the stage holds and are never stored
+                hv[4 * q + j] = fmaf(__expf(dt * av[4 * q + j]), hq[j], dtx * bq[j]);
+                y = fmaf(cq[j], hv[4 * q + j], y);
+            }
+        }
+        if (!live) y = 0.f;
+        y = group_sum<LPR>(y);
+        if (!live) continue;
+        const size_t r = (size_t)(b0 + p) * D + d;
+        float *op = out + r * NP + n0;
+        st_stream(op, make_float4(hv[0], hv[1], hv[2], hv[3]));
+        st_stream(op + 4, make_float4(hv[4], hv[5], hv[6], hv[7]));
+        if (sub == 0) {
+            if (P.Dskip) y = fmaf(P.Dskip[d], x, y);
+            if (P.z) y *= zs[p] * sigmoid_f(zs[p]);
+            if (P.out_dtype == GDN_BF16)
+                static_cast<bf16 *>(P.y)[r] = __float2bfloat16_rn(y);
+            else
+                static_cast<float *>(P.y)[r] = y;
+        }
+    }
+}
+
 template <int NP, typename Tin>
 static int launch_mamba_np(const mamba_decode_args &p, cudaStream_t s)
 {
     const long long threads = (long long)p.B * p.D * (NP / (NP >= 8 ? 8 : 4));
     const unsigned blocks = (unsigned)((threads + kMambaThreads - 1) / kMambaThreads);
-    if constexpr (NP >= 32) {
+    if constexpr (NP >= 16) {
         if (p.N == NP) {
             int dev = 0, sms = 0;
             if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
                 return GDN_ERR_LAUNCH;
+            // the staged form from two waves of its 32 KB blocks (four CTAs per SM), with B and C
+            // rows 16-byte aligned for their bulk copies. On GB300 at D = 1536 it beat the other
+            // forms from B = 512 (N = 16: 18.84 against 19.17 us; B = 1024, N = 64: 132.6 against
+            // 142.1; N = 128: 266.7 against 288.9) and lost at 1.3 waves (B = 256, N = 16: 11.46
+            // against 11.09)
+            constexpr int rpp = kMambaThreads / (NP / 8);
+            const long long sblocks = (long long)((p.D + rpp - 1) / rpp) * ((p.B + kMambaRowsPerBlock - 1) / kMambaRowsPerBlock);
+            const bool al16 = (reinterpret_cast<uintptr_t>(p.Bm) & 15u) == 0 && (reinterpret_cast<uintptr_t>(p.Cm) & 15u) == 0;
+            if (al16 && sblocks >= 8LL * sms) {
+                mamba_stage_kernel<NP, Tin><<<(unsigned)sblocks, kMambaThreads, 0, s>>>(p);
+                return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
+            }
             const unsigned cap = (unsigned)sms * kMambaGsCtasPerSmBound;
-            if (blocks >= 2u * cap) {
+            if (NP >= 32 && blocks >= 2u * cap) {
                 mamba_gs_kernel<NP, Tin><<<cap, kMambaThreads, 0, s>>>(p);
                 return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
             }

@@ -33,10 +33,10 @@ static gdn_step_args valid_step(void)
 int main(void)
 {
     printf("version %d\n", gdn_abi_version());
-    printf("c_sizes %zu %zu %zu %zu %zu\n", sizeof(gdn_step_args), sizeof(gdn_ring_args),
-           sizeof(gdn_fused_args), sizeof(gdn_gemv_args), sizeof(gdn_front_args));
-    printf("lib_sizes %zu %zu %zu %zu %zu\n", gdn_abi_struct_size(0), gdn_abi_struct_size(1),
-           gdn_abi_struct_size(2), gdn_abi_struct_size(3), gdn_abi_struct_size(4));
+    printf("c_sizes %zu %zu %zu %zu %zu %zu\n", sizeof(gdn_step_args), sizeof(gdn_ring_args),
+           sizeof(gdn_fused_args), sizeof(gdn_gemv_args), sizeof(gdn_front_args), sizeof(mamba_decode_args));
+    printf("lib_sizes %zu %zu %zu %zu %zu %zu\n", gdn_abi_struct_size(0), gdn_abi_struct_size(1),
+           gdn_abi_struct_size(2), gdn_abi_struct_size(3), gdn_abi_struct_size(4), gdn_abi_struct_size(5));
 
     gdn_step_args s = valid_step();
     printf("null_args %d\n", gdn_decode_step(NULL, NULL));

@@ -44,6 +44,7 @@ def test_struct_layout_and_version():
     assert L.gdn_abi_struct_size(2) == ctypes.sizeof(gdn.GdnFusedArgs)
     assert L.gdn_abi_struct_size(3) == ctypes.sizeof(gdn.GemvArgs)
     assert L.gdn_abi_struct_size(4) == ctypes.sizeof(gdn.GdnFrontArgs)
+    assert L.gdn_abi_struct_size(5) == ctypes.sizeof(gdn.MambaArgs)
     assert L.gdn_abi_struct_size(9) == 0
     assert L.gdn_abi_version() == gdn.ABI_VERSION
 

@@ -52,15 +52,17 @@ def _same(a: torch.Tensor, b: torch.Tensor) -> bool:
 # ------------------------------------------------------------------------------------------------
 # packed / indexed step
 # ------------------------------------------------------------------------------------------------
-@pytest.mark.parametrize("B,K,V,sdt", [
-    (1, 128, 200, "f32"),      # 32 tiles: 2 rows per thread, ragged last row pass
-    (8, 128, 200, "f32"),      # 256 tiles: 4 rows per thread
-    (16, 128, 200, "f32"),     # 512 tiles: 8 rows per thread (two CTAs per tile)
-    (32, 64, 200, "f32"),      # K = 64, 1024 tiles: 16 rows per thread
-    (32, 128, 128, "bf16"),    # the bf16-state kernel
-    (2, 128, 200, "bf16"),     # bf16 state through the row split
+@pytest.mark.parametrize("B,K,V,sdt,chained", [
+    (1, 128, 200, "f32", False),      # 32 tiles: 2 rows per thread, ragged last row pass
+    (8, 128, 200, "f32", False),      # 256 tiles: 4 rows per thread
+    (16, 128, 200, "f32", False),     # 512 tiles: 8 rows per thread (two CTAs per tile)
+    (32, 64, 200, "f32", False),      # K = 64, 1024 tiles: 16 rows per thread
+    (32, 128, 128, "bf16", False),    # the bf16-state kernel
+    (2, 128, 200, "bf16", False),     # bf16 state through the row split
+    (16, 128, 128, "f32", True),      # the chained instance, two CTAs per tile
+    (3, 128, 128, "f32", True),       # the chained instance, eight CTAs per tile
 ])
-def test_step_writes_only_its_buffers(B, K, V, sdt):
+def test_step_writes_only_its_buffers(B, K, V, sdt, chained):
     H, HV = 16, 32
     seed = 700 + B + K
     num_slots = B + 3
@@ -87,7 +89,7 @@ def test_step_writes_only_its_buffers(B, K, V, sdt):
                                 dt_bias=dt_bias)
     gs, go, ge = Guarded(state0), Guarded(out0), Guarded(torch.zeros(1, dtype=torch.int32, device="cuda"))
     gdn.gdn_decode_step_indexed(q, k, v, gs.t, go.t, idx0, H=H, a=a, b=b, A_log=A_log,
-                                dt_bias=dt_bias, err_flags=ge.t)
+                                dt_bias=dt_bias, err_flags=ge.t, chained=chained)
     assert gs.intact() and go.intact() and ge.intact()
     assert _same(gs.t, plain_state) and _same(go.t, plain_out)
     assert int(ge.t.item()) == 0
@@ -136,9 +138,8 @@ def test_buffered_pipe_writes_only_its_buffers(L, start, kernel):
 # ------------------------------------------------------------------------------------------------
 # fused decode, pipelined kernel (DS and SD conv-state layouts)
 # ------------------------------------------------------------------------------------------------
-@pytest.mark.parametrize("kernel", ["pipe", "stage"])
+@pytest.mark.parametrize("T,kernel", [(4, "pipe"), (9, "pipe"), (4, "stage"), (9, "stage")])
 @pytest.mark.parametrize("layout", ["DS", "SD"])
-@pytest.mark.parametrize("T", [4, 9])
 def test_fused_pipe_writes_only_its_buffers(layout, T, kernel):
     heads, D = 96, 128
     dim = heads * D
@@ -155,7 +156,8 @@ def test_fused_pipe_writes_only_its_buffers(layout, T, kernel):
     gate = torch.empty((T, heads, D), dtype=torch.bfloat16, device="cuda")
     syn.fill_normal_(gate, seed, syn.Tag.OUT_GATE, 0, 1.0)
     idx = torch.arange(1, T + 1, dtype=torch.int32, device="cuda")
-    idx[1] = 0                                                      # a pad row (NULL slot 0)
+    if T > 1:
+        idx[1] = 0                                                  # a pad row (NULL slot 0)
     common = dict(conv_w=torch.from_numpy(ins["conv_w"]).cuda(),
                   raw_g=bits_to_torch_bf16(ins["raw_g"]), raw_beta=bits_to_torch_bf16(ins["raw_beta"]),
                   A_log=torch.from_numpy(ins["A_log"]).cuda(), dt_bias=torch.from_numpy(ins["dt_bias"]).cuda(),
@@ -263,7 +265,9 @@ def test_guard_helper_detects_a_write_into_the_band():
 # Mamba-1 decode (the second recurrence)
 # ------------------------------------------------------------------------------------------------
 @pytest.mark.parametrize("B,D,N,in_place", [(3, 96, 64, True), (5, 40, 16, False), (2, 33, 48, True),
-                                            (4, 64, 128, False)])
+                                            (4, 64, 128, False),
+                                            (128, 1536, 64, True), (402, 1000, 32, False),  # staged form
+                                            (48, 1536, 64, False)])                         # grid-stride
 def test_mamba_writes_only_its_buffers(B, D, N, in_place):
     m = syn.mamba_inputs(B, D, N, "f32", 900 + N)
     t = {k: torch.from_numpy(np.ascontiguousarray(v)).cuda() for k, v in m.items()}

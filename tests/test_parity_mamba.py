@@ -83,3 +83,18 @@ def test_new_state_buffer_leaves_the_old_one():
 def test_large_batch():
     wy, wh = _run(256, 1536, 16, seed=14)
     assert wy <= 1e-5 and wh <= 1e-5, (wy, wh)
+
+
+@pytest.mark.parametrize("B,D,N,dtype,out_dtype,functional", [
+    (128, 1536, 64, "f32", "f32", False),    # 1536 blocks of 4 rows x 32 channels: the staged form
+    (64, 1536, 128, "bf16", "bf16", False),  # 1536 blocks of 4 rows x 16 channels, bf16 in and out
+    (402, 1000, 32, "f32", "f32", True),     # ragged channel and row blocks (1000 / 64, 402 / 4); h_out
+    (512, 1536, 16, "f32", "f32", False),    # 1536 blocks of 4 rows x 128 channels
+    (48, 1536, 64, "f32", "f32", False),     # 576 blocks: below the staged form, the grid-stride one
+])
+def test_staged_and_grid_stride_forms(B, D, N, dtype, out_dtype, functional):
+    """Batches large enough for the staged form (each 32 KB block of state rows bulk-copied into
+    shared memory) and for the grid-stride form, over two sequential steps."""
+    wy, wh = _run(B, D, N, dtype=dtype, out_dtype=out_dtype, seed=20 + N, steps=2, functional=functional)
+    tol = 2e-2 if out_dtype == "bf16" else 1e-5
+    assert wy <= tol and wh <= 1e-5, (wy, wh)

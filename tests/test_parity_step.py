@@ -34,7 +34,8 @@ def _tol(out_dtype):
 
 
 def _run(B, H, HV, K, V, dtype, out_dtype, seed, *, steps=1, indexed=True, num_slots=None,
-         pad_rows=(), bad_rows=(), use_l2=True, scale=None, state_dtype="f32", first_out=None):
+         pad_rows=(), bad_rows=(), use_l2=True, scale=None, state_dtype="f32", first_out=None,
+         chained=False):
     """Run `steps` sequential steps on both sides; compare out every step and the state at the
     end. Returns the worst errors (first_out, if a list, receives the first step's error)."""
     num_slots = num_slots or (B + len(pad_rows) + 2 if indexed else B)
@@ -59,7 +60,7 @@ def _run(B, H, HV, K, V, dtype, out_dtype, seed, *, steps=1, indexed=True, num_s
         kw = dict(H=H, a=c.a, b=c.b, A_log=c.A_log, dt_bias=c.dt_bias, scale=scale,
                   use_qk_l2norm=use_l2, err_flags=err)
         if indexed:
-            gdn.gdn_decode_step_indexed(q, k, v, state, out, idx, pad_slot_id=-1, **kw)
+            gdn.gdn_decode_step_indexed(q, k, v, state, out, idx, pad_slot_id=-1, chained=chained, **kw)
         else:
             gdn.gdn_decode_step(q, k, v, state, out, **kw)
         o_ref, bad = oracle.gdn_step_packed(*c.oracle_args(), S64, H=H, HV=HV, K=K, V=V,
@@ -349,3 +350,21 @@ def test_chained_layers_wait_for_the_previous_layer_output(B, K):
         assert rel_err(results[True][0][2 * it + 1].reshape(B, HV, V), o1) <= TOL_F32
     for l in range(2):
         assert rel_err(results[True][1][l], S[l]) <= TOL_F32
+
+
+@pytest.mark.parametrize("B,H,HV,dtype,out_dtype,pad_rows,bad_rows,steps", [
+    (3, 16, 32, "bf16", "bf16", (1,), (), 3),      # 96 tiles: eight CTAs per tile
+    (16, 16, 32, "bf16", "bf16", (2,), (5,), 2),   # a pad row and a bad slot index
+    (75, 16, 32, "bf16", "bf16", (), (), 1),       # 2400 tiles: two CTAs per tile
+    (8, 4, 16, "f32", "f32", (), (), 4),           # fp32 inputs, four value heads per q/k head
+    (1, 16, 32, "bf16", "f32", (), (), 2),         # 32 tiles: eight CTAs per tile
+])
+def test_chained_calls_against_the_oracle(B, H, HV, dtype, out_dtype, pad_rows, bad_rows, steps):
+    """gdn_decode_step_indexed_chained on packed bf16 (and fp32) inputs with raw gates: sequential
+    steps against the oracle, with pad rows and a bad index (flagged, its output zero), across the
+    row splits the chained instance runs at these batch sizes."""
+    wo, ws, flags = _run(B, H, HV, 128, 128, dtype, out_dtype, 960 + B, steps=steps, pad_rows=pad_rows,
+                         bad_rows=bad_rows, chained=True)
+    assert wo <= _tol(out_dtype)
+    assert ws <= TOL_F32
+    assert flags == (gdn.GDN_DEVERR_BAD_INDEX if bad_rows else 0)
