@@ -44,6 +44,10 @@ __global__ void __launch_bounds__(kMambaThreads, 7) mamba_decode_kernel(const __
     const bool live = r < rows;
     const int b = live ? (int)(r / D) : 0, d = live ? (int)(r - (long long)b * D) : 0;
     const int n0 = sub * EPL;
+    // 16-byte accesses: entries 4 sub + VS q .. + 3 of the row (q < EPL / 4), so that each access
+    // of a row's lanes covers 16 LPR contiguous bytes
+    constexpr int VS = 4 * LPR;
+    const int vc = 4 * sub;
 
     float hv[EPL];
 #pragma unroll
@@ -56,15 +60,15 @@ __global__ void __launch_bounds__(kMambaThreads, 7) mamba_decode_kernel(const __
         if (VEC) {
 #pragma unroll
             for (int q = 0; q < EPL / 4; ++q) {
-                const float4 h4 = ld_stream(hp + 4 * q);
+                const float4 h4 = ld_stream(P.h + (size_t)r * N + vc + VS * q);
                 hv[4 * q] = h4.x; hv[4 * q + 1] = h4.y; hv[4 * q + 2] = h4.z; hv[4 * q + 3] = h4.w;
             }
             const float dtx = dt * x;
 #pragma unroll
             for (int q = 0; q < EPL / 4; ++q) {
-                const float4 a4 = *reinterpret_cast<const float4 *>(P.A + (size_t)d * N + n0 + 4 * q);
-                const float4 b4 = load4(static_cast<const Tin *>(P.Bm) + (size_t)b * N + n0 + 4 * q);
-                const float4 c4 = load4(static_cast<const Tin *>(P.Cm) + (size_t)b * N + n0 + 4 * q);
+                const float4 a4 = *reinterpret_cast<const float4 *>(P.A + (size_t)d * N + vc + VS * q);
+                const float4 b4 = load4(static_cast<const Tin *>(P.Bm) + (size_t)b * N + vc + VS * q);
+                const float4 c4 = load4(static_cast<const Tin *>(P.Cm) + (size_t)b * N + vc + VS * q);
                 const float av[4] = {a4.x, a4.y, a4.z, a4.w}, bv[4] = {b4.x, b4.y, b4.z, b4.w},
                             cv[4] = {c4.x, c4.y, c4.z, c4.w};
 #pragma unroll
@@ -90,9 +94,10 @@ __global__ void __launch_bounds__(kMambaThreads, 7) mamba_decode_kernel(const __
     if (!live) return;
     float *op = (P.h_out ? P.h_out : P.h) + (size_t)r * N + n0;
     if (VEC) {
+        float *ov = (P.h_out ? P.h_out : P.h) + (size_t)r * N + vc;
 #pragma unroll
         for (int q = 0; q < EPL / 4; ++q)
-            st_stream(op + 4 * q, make_float4(hv[4 * q], hv[4 * q + 1], hv[4 * q + 2], hv[4 * q + 3]));
+            st_stream(ov + VS * q, make_float4(hv[4 * q], hv[4 * q + 1], hv[4 * q + 2], hv[4 * q + 3]));
     } else {
 #pragma unroll
         for (int j = 0; j < EPL; ++j)
@@ -128,7 +133,10 @@ __global__ void __launch_bounds__(kMambaThreads, kMambaGsCtasPerSmBound) mamba_g
     const long long tid = (long long)blockIdx.x * kMambaThreads + threadIdx.x;
     const long long rstep = (long long)gridDim.x * kMambaThreads / LPR;
     const int sub = (int)(tid % LPR);
-    const int n0 = sub * EPL;
+    // entries 4 sub .. 4 sub + 3 and HALF + 4 sub .. + 3 of a row: each access of a row's lanes
+    // covers 16 LPR contiguous bytes
+    constexpr int HALF = 4 * LPR;
+    const int n0 = 4 * sub;
     long long r = tid / LPR;
     // the row's state and its per-row scalars (x, dt and, for the lane that writes y, z) are
     // loaded one row ahead, so that no load from HBM waits in the computing row's path
@@ -136,7 +144,7 @@ __global__ void __launch_bounds__(kMambaThreads, kMambaGsCtasPerSmBound) mamba_g
     float cx = 0.f, cdt = 0.f, cz = 0.f;
     if (r < rows) {
         c0 = ld_stream(P.h + (size_t)r * N + n0);
-        c1 = ld_stream(P.h + (size_t)r * N + n0 + 4);
+        c1 = ld_stream(P.h + (size_t)r * N + n0 + HALF);
         cx = ld1<Tin>(P.x, (size_t)r);
         cdt = ld1<Tin>(P.dt, (size_t)r);
         if (P.z && sub == 0) cz = ld1<Tin>(P.z, (size_t)r);
@@ -151,7 +159,7 @@ __global__ void __launch_bounds__(kMambaThreads, kMambaGsCtasPerSmBound) mamba_g
         float nx = 0.f, ndt = 0.f, nz = 0.f;
         if (rn < rows) {
             n0v = ld_stream(P.h + (size_t)rn * N + n0);
-            n1v = ld_stream(P.h + (size_t)rn * N + n0 + 4);
+            n1v = ld_stream(P.h + (size_t)rn * N + n0 + HALF);
             nx = ld1<Tin>(P.x, (size_t)rn);
             ndt = ld1<Tin>(P.dt, (size_t)rn);
             if (P.z && sub == 0) nz = ld1<Tin>(P.z, (size_t)rn);
@@ -164,9 +172,9 @@ __global__ void __launch_bounds__(kMambaThreads, kMambaGsCtasPerSmBound) mamba_g
         float y = 0.f;
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
-            const float4 a4 = *reinterpret_cast<const float4 *>(P.A + (size_t)d * N + n0 + 4 * q);
-            const float4 b4 = load4(static_cast<const Tin *>(P.Bm) + (size_t)b * N + n0 + 4 * q);
-            const float4 c4 = load4(static_cast<const Tin *>(P.Cm) + (size_t)b * N + n0 + 4 * q);
+            const float4 a4 = *reinterpret_cast<const float4 *>(P.A + (size_t)d * N + n0 + HALF * q);
+            const float4 b4 = load4(static_cast<const Tin *>(P.Bm) + (size_t)b * N + n0 + HALF * q);
+            const float4 c4 = load4(static_cast<const Tin *>(P.Cm) + (size_t)b * N + n0 + HALF * q);
             const float av[4] = {a4.x, a4.y, a4.z, a4.w}, bv[4] = {b4.x, b4.y, b4.z, b4.w}, cv[4] = {c4.x, c4.y, c4.z, c4.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -179,7 +187,7 @@ __global__ void __launch_bounds__(kMambaThreads, kMambaGsCtasPerSmBound) mamba_g
         if (live) {
             float *op = (P.h_out ? P.h_out : P.h) + (size_t)r * N + n0;
             st_stream(op, make_float4(hv[0], hv[1], hv[2], hv[3]));
-            st_stream(op + 4, make_float4(hv[4], hv[5], hv[6], hv[7]));
+            st_stream(op + HALF, make_float4(hv[4], hv[5], hv[6], hv[7]));
         }
         if (live && sub == 0) {
             if (P.Dskip) y = fmaf(P.Dskip[d], x, y);
@@ -233,7 +241,12 @@ __global__ void __launch_bounds__(kMambaThreads) mamba_stage_kernel(const __grid
     const int bblk = blockIdx.x / dblocks, dblk = blockIdx.x - bblk * dblocks;
     const int b0 = bblk * NB, d0 = dblk * RPP;
     const int nb = P.B - b0 < NB ? P.B - b0 : NB, nd = D - d0 < RPP ? D - d0 : RPP;
-    const int sub = threadIdx.x % LPR, n0 = sub * EPL, lrow = threadIdx.x / LPR;
+    // lane `sub` of a row holds the entries 4 sub .. 4 sub + 3 and 4 LPR + 4 sub .. + 3, so that
+    // the LPR lanes of a row read and write 16 LPR contiguous bytes per access (no bank conflicts
+    // in shared memory, whole sectors in global memory)
+    const int sub = threadIdx.x % LPR, lrow = threadIdx.x / LPR;
+    constexpr int HALF = 4 * LPR;
+    const int n0 = 4 * sub;
     const bool dlive = lrow < nd;
     const int d = d0 + (dlive ? lrow : 0);
 
@@ -252,7 +265,7 @@ __global__ void __launch_bounds__(kMambaThreads) mamba_stage_kernel(const __grid
     }
     // this channel's A entries and the scalars of its four rows, while the copies are in flight
     const float4 a_lo = *reinterpret_cast<const float4 *>(P.A + (size_t)d * NP + n0);
-    const float4 a_hi = *reinterpret_cast<const float4 *>(P.A + (size_t)d * NP + n0 + 4);
+    const float4 a_hi = *reinterpret_cast<const float4 *>(P.A + (size_t)d * NP + n0 + HALF);
     const float av[8] = {a_lo.x, a_lo.y, a_lo.z, a_lo.w, a_hi.x, a_hi.y, a_hi.z, a_hi.w};
     float xs[NB], dts[NB], zs[NB];
 #pragma unroll
@@ -279,8 +292,8 @@ __global__ void __launch_bounds__(kMambaThreads) mamba_stage_kernel(const __grid
         float y = 0.f;
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
-            const float4 h4 = *reinterpret_cast<const float4 *>(hs + hrow * NP + n0 + 4 * q);
-            const float4 b4 = load4(bs + p * NP + n0 + 4 * q), c4 = load4(cs + p * NP + n0 + 4 * q);
+            const float4 h4 = *reinterpret_cast<const float4 *>(hs + hrow * NP + n0 + HALF * q);
+            const float4 b4 = load4(bs + p * NP + n0 + HALF * q), c4 = load4(cs + p * NP + n0 + HALF * q);
             const float hq[4] = {h4.x, h4.y, h4.z, h4.w}, bq[4] = {b4.x, b4.y, b4.z, b4.w}, cq[4] = {c4.x, c4.y, c4.z, c4.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -295,7 +308,7 @@ __global__ void __launch_bounds__(kMambaThreads) mamba_stage_kernel(const __grid
         const size_t r = (size_t)(b0 + p) * D + d;
         float *op = out + r * NP + n0;
         st_stream(op, make_float4(hv[0], hv[1], hv[2], hv[3]));
-        st_stream(op + 4, make_float4(hv[4], hv[5], hv[6], hv[7]));
+        st_stream(op + HALF, make_float4(hv[4], hv[5], hv[6], hv[7]));
         if (sub == 0) {
             if (P.Dskip) y = fmaf(P.Dskip[d], x, y);
             if (P.z) y *= zs[p] * sigmoid_f(zs[p]);
