@@ -208,9 +208,11 @@ int gdn_decode_step_indexed(const gdn_step_args *args, const int32_t *cache_indi
  * complete before it reads q, k, v, the gate inputs or the gates and before it writes anything.
  * Every other buffer may be that kernel's output. Because each chained kernel lets the next one
  * start at once, a chained call may overlap any kernel of the run of consecutive chained calls
- * before it: no kernel in that run may write this call's state tiles or cache_indices. Give every
- * chained layer its own state pool, and make the first call of each step an ordinary call, so that
- * two calls on the same pool are never in one run. The overlap takes one launch gap and the
+ * before it and the library call just before that run (an ordinary step call lets the next kernel
+ * start once the work before it is complete): no kernel in that run, nor that call, may write this
+ * call's state tiles or cache_indices. Give every chained layer its own state pool, and make the
+ * first call of each step an ordinary call on a pool of its own, so that two calls on the same
+ * pool are never in one run. The overlap takes one launch gap and the
  * previous layer's tail off each layer. A bf16 state at K = V = 128 from 128 tiles on, and grids
  * of eight or more waves of CTAs, run the ordinary kernel (no overlap). Arguments, results and
  * status codes as for gdn_decode_step_indexed. Source: as gdn_decode_step_indexed; the layer loop is the model of

@@ -32,7 +32,13 @@ namespace gdn {
 // launch (a layer of a multi-layer graph). It lets the next kernel start its CTAs at once, reads
 // the slot index and issues its state loads, and only then waits for the kernel before it on the
 // stream to complete; every other input is read, and every output written, after that wait. The
-// ordinary instance has no wait: a wait after outstanding loads slowed ordinary launches.
+// ordinary instance is launched with the same attribute but waits before it touches memory and
+// only then lets the next kernel start (ordinary_launch_start), so the next call's CTAs can be
+// resident when this one ends: on GB300 3.20 against 3.42 us per call at B = 1, 13.28 against
+// 13.39 at B = 16, no change from B = 64 (a wait after outstanding loads, by contrast, slowed
+// ordinary launches). The bf16-state kernels of their own (step_kernel_bf16, and the staged one
+// from 128 tiles) keep plain launches: with tiles staged in shared memory the early CTAs made
+// B = 16 slower (9.47 against 8.48 us).
 template <int K, typename Tin, typename TS, int R, bool CHAIN>
 __global__ void __launch_bounds__(kThreads, R >= 16 ? 2 : 4) step_kernel(const __grid_constant__ StepLaunch P, int splits)
 {
@@ -44,6 +50,7 @@ __global__ void __launch_bounds__(kThreads, R >= 16 ? 2 : 4) step_kernel(const _
     const size_t out_base = ((size_t)b * HV + hv) * V;
     const int first_row = blk * TL::ROWS_PASS, row_step = splits * TL::ROWS_PASS;
     if constexpr (CHAIN) grid_launch_dependents();
+    else ordinary_launch_start();
 
     int slot = b;
     if (P.idx) {
@@ -234,7 +241,7 @@ static void launch_rows(const StepLaunch &p, unsigned tiles, cudaStream_t stream
     const unsigned waves_x8 = 8u * per_sm * (unsigned)(sm_count() > 0 ? sm_count() : 152);
     if (chained && tiles * (unsigned)splits >= waves_x8) chained = false;
     if (!chained) {
-        step_kernel<K, Tin, TS, R, false><<<tiles * (unsigned)splits, kThreads, 0, stream>>>(p, splits);
+        launch_ordinary(step_kernel<K, Tin, TS, R, false>, dim3(tiles * (unsigned)splits), dim3(kThreads), 0, stream, p, splits);
         return;
     }
     cudaLaunchConfig_t cfg = {};
