@@ -47,6 +47,24 @@ struct FusedLayout {
     static constexpr uint32_t stage = (meta + (uint32_t)sizeof(FusedMeta) + 127u) & ~127u;
 };
 
+// a . b over four elements as two fp32 pairs (fma.rn.f32x2: the same rounding per element as the
+// scalar operations, half the instructions)
+__device__ __forceinline__ float dot4_pairs(float4 a, float4 b)
+{
+    float2 p = __fmul2_rn(make_float2(a.x, a.y), make_float2(b.x, b.y));
+    p = __ffma2_rn(make_float2(a.z, a.w), make_float2(b.z, b.w), p);
+    return p.x + p.y;
+}
+
+// dec * s + d * k elementwise, as two fp32 pairs
+__device__ __forceinline__ float4 decay_update_pairs(float4 dec, float4 s, float d, float4 k)
+{
+    const float2 d2 = make_float2(d, d);
+    const float2 lo = __ffma2_rn(d2, make_float2(k.x, k.y), __fmul2_rn(make_float2(dec.x, dec.y), make_float2(s.x, s.y)));
+    const float2 hi = __ffma2_rn(d2, make_float2(k.z, k.w), __fmul2_rn(make_float2(dec.z, dec.w), make_float2(s.z, s.w)));
+    return make_float4(lo.x, lo.y, hi.x, hi.y);
+}
+
 __device__ __forceinline__ float bfs(const unsigned char *base, uint32_t off, int i)
 {
     return __bfloat162float(reinterpret_cast<const bf16 *>(base + off)[i]);
@@ -60,6 +78,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_pipe_kernel(const __grid_c
     using FL = FusedLayout;
     extern __shared__ __align__(128) unsigned char sm[];
     __shared__ float ysm[kFGroups][3 * D];      // conv outputs q | k | v of the group's tile
+    __shared__ __align__(16) float decsm[kFGroups][D];   // per-key decays exp(g_k) of the group's tile (KDA)
     __shared__ float red[kFGroups][2][kFGW];    // per-warp sums of o^2 (double-buffered)
     __shared__ __align__(8) uint64_t gbar[kFGroups][2];   // group syncs: conv -> step, o^2 -> norm
     __shared__ int abort_flag;
@@ -267,24 +286,21 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_pipe_kernel(const __grid_c
                 cp[2 * a.cs_stride_tap] = __float2bfloat16_rn(xin);
             }
         }
+        // (2) the KDA per-key decays, once per tile: threads 128..255 (one conv channel each above)
+        // take one key column each; the other warps read them after the group barrier. (Each warp
+        // computing all 128 itself cost 1.5-1.9k of a tile's 9k cycles per group at T = 8; with
+        // fp32-pair dots and updates the call took 20.37 against 20.61 us, T = 4: 13.47 against
+        // 13.86, as the other phases, which share the SM with the second group, took up the rest.)
+        if (kda && tid >= 128) {
+            const int col = tid - 128;
+            const float xg = bfs(stage, FL::rg, col) + reinterpret_cast<const float *>(stage + FL::db)[col];
+            const float gv = a.kda_gate_form == 0 ? fmaxf(a.lower_bound, -meta->A * softplus_f(xg))
+                                                  : a.lower_bound * sigmoid_f(meta->A * xg);
+            decsm[group][col] = expf(gv);
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&gbar[group][0]);
 
-        // (2) gates of this lane's four key columns, output gate of its row (from the stage)
-        float4 dec;
-        if (kda) {
-            float gv[4];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const float xg = bfs(stage, FL::rg, t.col + c) + reinterpret_cast<const float *>(stage + FL::db)[t.col + c];
-                gv[c] = a.kda_gate_form == 0 ? fmaxf(a.lower_bound, -meta->A * softplus_f(xg))
-                                             : a.lower_bound * sigmoid_f(meta->A * xg);
-            }
-            dec = make_float4(expf(gv[0]), expf(gv[1]), expf(gv[2]), expf(gv[3]));
-        } else {
-            const float e = expf(meta->g_head);
-            dec = make_float4(e, e, e, e);
-        }
         const float beta = meta->beta;
         float gate[2];
 #pragma unroll
@@ -295,6 +311,13 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_pipe_kernel(const __grid_c
                 raise_flag(a.err_flags, GDN_DEVERR_TIMEOUT);
             }
             break;
+        }
+        float4 dec;
+        if (kda) {
+            dec = *reinterpret_cast<const float4 *>(&decsm[group][t.col]);
+        } else {
+            const float e = expf(meta->g_head);
+            dec = make_float4(e, e, e, e);
         }
 
         // (3) the step, both dots straight from the staged tile, eight rows at a time
@@ -311,8 +334,8 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_pipe_kernel(const __grid_c
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const float4 srow = *reinterpret_cast<const float4 *>(Ss + (size_t)(row0 + 8 * c + i) * D + t.col);
-                    x[i] = dot4(srow, kd);
-                    x[8 + i] = dot4(srow, qd);
+                    x[i] = dot4_pairs(srow, kd);
+                    x[8 + i] = dot4_pairs(srow, qd);
                 }
                 t.reduce_scatter(x);
                 const float vv = t.holds_k_dot() ? ys[2 * D + row0 + 8 * c + rsub] : 0.f;
@@ -336,7 +359,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_pipe_kernel(const __grid_c
                 for (int i = 0; i < 8; ++i) {
                     const float d = __shfl_sync(kFull, c == 0 ? dvc0 : dvc1, 2 * i);
                     const float4 srow = *reinterpret_cast<const float4 *>(Ss + (size_t)(row0 + 8 * c + i) * D + t.col);
-                    st_stream(S + (size_t)(row0 + 8 * c + i) * D + t.col, decay_update4(dec, srow, d, kh));
+                    st_stream(S + (size_t)(row0 + 8 * c + i) * D + t.col, decay_update_pairs(dec, srow, d, kh));
                 }
             }
         }
