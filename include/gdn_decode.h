@@ -172,7 +172,7 @@ typedef struct gdn_fused_args {
     int32_t kernel;           /* GDN_KERNEL_AUTO: when head_dim == 128, the conv state is in the DS or
                                  SD layout, rows are 16-byte aligned and there are more than two
                                  (token, head) tiles per SM, one CTA per tile staged in shared memory
-                                 by bulk copies from sixteen tiles per SM and the persistent pipelined
+                                 by bulk copies from twelve tiles per SM and the persistent pipelined
                                  kernel below that; else the per-tile kernel. GDN_KERNEL_TILE /
                                  GDN_KERNEL_PIPE / GDN_KERNEL_STAGE force one */
     int64_t raw_g_stride;     /* row (token) strides in elements of raw_g, raw_beta and out_gate, at

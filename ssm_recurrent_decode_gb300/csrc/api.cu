@@ -127,10 +127,11 @@ int prepare_fused(const gdn_fused_args *a, FusedPlan *plan)
     // four tiles per SM the pipelined kernel wins.
     const bool few_tiles = (int64_t)a->T * a->heads <= 2 * (int64_t)sms;
     bool use_pipe = pipe_ok && pipe_aligned && !few_tiles;
-    // From sixteen tiles per SM one CTA per tile staged in shared memory beat the persistent kernel
-    // (T = 128: 243.8 against 267.4 us; T = 32, 20 tiles per SM: 65.7 against 68.6); at ten and
-    // five per SM it lost (T = 16: 37.2 against 35.6; T = 8: 22.5 against 20.2).
-    bool use_stage = use_pipe && (int64_t)a->T * a->heads >= 16 * (int64_t)sms;
+    // From twelve tiles per SM one CTA per tile staged in shared memory beat the persistent kernel
+    // (T = 128: 243.8 against 267.4 us; T = 32, 20 tiles per SM: 65.9 against 68.3; T = 24: 51.7
+    // against 52.4; T = 20, 12.6 per SM: 44.1 against 44.4); at ten and five per SM it lost
+    // (T = 16: 37.2 against 35.3; T = 8: 22.5 against 20.4).
+    bool use_stage = use_pipe && (int64_t)a->T * a->heads >= 12 * (int64_t)sms;
     if (a->kernel == GDN_KERNEL_PIPE || a->kernel == GDN_KERNEL_STAGE) {
         if (!pipe_ok) return GDN_ERR_SHAPE;
         if (!pipe_aligned) return GDN_ERR_ALIGN;
