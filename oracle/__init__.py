@@ -15,9 +15,11 @@ Readings of points the sources leave open:
 The Mamba-1 selective-scan decode ("Triton decode kernel + MBU analysis", Kernel design) is a
 second recurrence through the same kind of boundary.
 
-Parity status: every routine is pinned by tests/test_oracle_pins.py except the KDA gate formula,
-whose two readings are pinned only to their own special values (the sources name the inputs and
-the -5 lower bound but print no formula): "parity unpinned" for that formula.
+Parity status: every routine is pinned by tests/test_oracle_pins.py. The KDA gate's two readings
+are pinned to closed values of their own formulas (points where exp(A_log[h]), the head index and
+the per-key dt_bias change the value), and mutants that drop or misindex those terms fail
+(tests/test_oracle_mutants.py). Which formula the KDA page means is a reading, since it names the
+inputs and the -5 lower bound but prints no formula.
 """
 from __future__ import annotations
 
