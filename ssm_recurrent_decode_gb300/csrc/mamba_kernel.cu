@@ -210,32 +210,30 @@ __global__ void __launch_bounds__(kMambaThreads, kMambaGsCtasPerSmBound) mamba_g
     }
 }
 
-// Staged form for N = 16 .. 128 (powers of two) and large batches: one CTA per block of four batch
-// rows b0 .. b0 + 3 by RPP consecutive channels d0 .. (32 KB of state, four contiguous runs of RPP
-// state rows). Thread 0 bulk-copies the four runs and the four B and C rows (cp.async.bulk,
+// Staged form for N = 16 .. 128 (powers of two) and large batches: one CTA per block of NB = 4 (or
+// 2) batch rows b0 .. by RPP consecutive channels d0 .. (32 KB, or 16 KB, of state: NB contiguous
+// runs of RPP state rows). Thread 0 bulk-copies the runs and the NB B and C rows (cp.async.bulk,
 // completion on one mbarrier) into shared memory as the CTA starts; meanwhile every thread loads
-// the eight A entries of its channel, which all four batch rows share, and the x, dt and z scalars
-// of its four rows. The update then reads only shared memory and registers, one batch row per
+// the eight A entries of its channel, which all NB batch rows share, and the x, dt and z scalars
+// of its NB rows. The update then reads only shared memory and registers, one batch row per
 // pass, and stores with streaming stores, so a CTA's shared memory is busy for the copy and a short
-// arithmetic phase, not for round trips to L2 (58 registers, four CTAs per SM: 128 KB of copies in
-// flight per SM). An earlier form, one block of consecutive rows per CTA with the A, B and C rows
+// arithmetic phase, not for round trips to L2 (NB = 4: 58 registers, four CTAs per SM, 128 KB of
+// copies in flight per SM; NB = 2: 48 registers, five CTAs per SM). An earlier form, one block of consecutive rows per CTA with the A, B and C rows
 // read from L2 during the update, was slower than the grid-stride form (158.7 against 142.0 us at
 // B = 1024, N = 64), and bounding this one to five CTAs per SM (48 registers, a few spilled) lost
 // 2-8%. The wait is bounded: on a timeout the CTA raises
 // GDN_DEVERR_TIMEOUT in err_flags, thread 0 waits (bounded) for its copies, and the block's rows are
 // left as they were.
 constexpr long long kMambaWaitLimit = 1LL << 31;   // SM clock cycles, about one second
-constexpr uint32_t kMambaBlockBytes = 32768u;
-constexpr int kMambaRowsPerBlock = 4;              // batch rows of a block, one per pass
 
-template <int NP, typename Tin>
+// NB batch rows per block (one per pass): 4 (32 KB of state) or 2 (16 KB)
+template <int NP, int NB, typename Tin>
 __global__ void __launch_bounds__(kMambaThreads) mamba_stage_kernel(const __grid_constant__ mamba_decode_args P)
 {
     constexpr int EPL = 8;
     constexpr int LPR = NP / EPL;                    // lanes per state row
     constexpr int RPP = kMambaThreads / LPR;         // channels of a block
-    constexpr int NB = kMambaRowsPerBlock;
-    static_assert(NB * RPP * NP * 4 == (int)kMambaBlockBytes, "a block is 32 KB of state");
+    static_assert(RPP * NP * 4 == 8192, "a batch row of a block is 8 KB of state");
     __shared__ __align__(128) float hs[NB * RPP * NP];
     __shared__ __align__(16) Tin bs[NB * NP];
     __shared__ __align__(16) Tin cs[NB * NP];
@@ -335,16 +333,22 @@ static int launch_mamba_np(const mamba_decode_args &p, cudaStream_t s)
             int dev = 0, sms = 0;
             if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
                 return GDN_ERR_LAUNCH;
-            // the staged form from two waves of its 32 KB blocks (four CTAs per SM), with B and C
-            // rows 16-byte aligned for their bulk copies. On GB300 at D = 1536 it beat the other
-            // forms from B = 512 (N = 16: 18.84 against 19.17 us; B = 1024, N = 64: 132.6 against
-            // 142.1; N = 128: 266.7 against 288.9) and lost at 1.3 waves (B = 256, N = 16: 11.46
-            // against 11.09)
+            // The staged form (B and C rows 16-byte aligned for their bulk copies): 32 KB blocks
+            // from six waves of them, 16 KB blocks from two waves. On GB300 at D = 1536: B = 1024,
+            // N = 64 118.6 us with 32 KB blocks against 120.9 with 16 KB and 142.1 for the
+            // grid-stride form; N = 128 233.2 against 241.3 and 288.9; B = 256, N = 16 10.40 with
+            // 16 KB blocks against 10.69 for the per-row kernel; B = 512, N = 16 17.95 against
+            // 18.40 with 32 KB blocks; B = 256, N = 64 32.59 against 32.82.
             constexpr int rpp = kMambaThreads / (NP / 8);
-            const long long sblocks = (long long)((p.D + rpp - 1) / rpp) * ((p.B + kMambaRowsPerBlock - 1) / kMambaRowsPerBlock);
+            const long long dblocks = (p.D + rpp - 1) / rpp;
+            const long long sb4 = dblocks * ((p.B + 3) / 4), sb2 = dblocks * ((p.B + 1) / 2);
             const bool al16 = (reinterpret_cast<uintptr_t>(p.Bm) & 15u) == 0 && (reinterpret_cast<uintptr_t>(p.Cm) & 15u) == 0;
-            if (al16 && sblocks >= 8LL * sms) {
-                mamba_stage_kernel<NP, Tin><<<(unsigned)sblocks, kMambaThreads, 0, s>>>(p);
+            if (al16 && sb4 >= 24LL * sms) {
+                mamba_stage_kernel<NP, 4, Tin><<<(unsigned)sb4, kMambaThreads, 0, s>>>(p);
+                return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
+            }
+            if (al16 && sb2 >= 8LL * sms) {
+                mamba_stage_kernel<NP, 2, Tin><<<(unsigned)sb2, kMambaThreads, 0, s>>>(p);
                 return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
             }
             const unsigned cap = (unsigned)sms * kMambaGsCtasPerSmBound;

@@ -266,7 +266,8 @@ def test_guard_helper_detects_a_write_into_the_band():
 # ------------------------------------------------------------------------------------------------
 @pytest.mark.parametrize("B,D,N,in_place", [(3, 96, 64, True), (5, 40, 16, False), (2, 33, 48, True),
                                             (4, 64, 128, False),
-                                            (128, 1536, 64, True), (402, 1000, 32, False),  # staged form
+                                            (128, 1536, 64, True), (403, 1000, 32, False),  # staged, 2 rows
+                                            (514, 1000, 64, True),                          # staged, 4 rows
                                             (48, 1536, 64, False)])                         # grid-stride
 def test_mamba_writes_only_its_buffers(B, D, N, in_place):
     m = syn.mamba_inputs(B, D, N, "f32", 900 + N)

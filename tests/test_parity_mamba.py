@@ -86,15 +86,16 @@ def test_large_batch():
 
 
 @pytest.mark.parametrize("B,D,N,dtype,out_dtype,functional", [
-    (128, 1536, 64, "f32", "f32", False),    # 1536 blocks of 4 rows x 32 channels: the staged form
-    (64, 1536, 128, "bf16", "bf16", False),  # 1536 blocks of 4 rows x 16 channels, bf16 in and out
-    (402, 1000, 32, "f32", "f32", True),     # ragged channel and row blocks (1000 / 64, 402 / 4); h_out
-    (512, 1536, 16, "f32", "f32", False),    # 1536 blocks of 4 rows x 128 channels
+    (128, 1536, 64, "f32", "f32", False),    # 3072 blocks of 2 rows x 32 channels: the staged form
+    (64, 1536, 128, "bf16", "bf16", False),  # 3072 blocks of 2 rows x 16 channels, bf16 in and out
+    (403, 1000, 32, "f32", "f32", True),     # ragged channel and row blocks (1000 / 64, 403 / 2); h_out
+    (512, 1536, 16, "f32", "f32", False),    # 3072 blocks of 2 rows x 128 channels
+    (514, 1000, 64, "f32", "f32", False),    # 4128 blocks of 4 rows x 32 channels, both edges ragged
     (48, 1536, 64, "f32", "f32", False),     # 576 blocks: below the staged form, the grid-stride one
 ])
 def test_staged_and_grid_stride_forms(B, D, N, dtype, out_dtype, functional):
-    """Batches large enough for the staged form (each 32 KB block of state rows bulk-copied into
-    shared memory) and for the grid-stride form, over two sequential steps."""
+    """Batches large enough for the staged form (each block of 2 or 4 batch rows' state bulk-copied
+    into shared memory) and for the grid-stride form, over two sequential steps."""
     wy, wh = _run(B, D, N, dtype=dtype, out_dtype=out_dtype, seed=20 + N, steps=2, functional=functional)
     tol = 2e-2 if out_dtype == "bf16" else 1e-5
     assert wy <= tol and wh <= 1e-5, (wy, wh)
