@@ -288,24 +288,25 @@ __global__ void __launch_bounds__(kMambaThreads) mamba_stage_kernel(const __grid
     float *out = P.h_out ? P.h_out : P.h;
 #pragma unroll
     for (int p = 0; p < NB; ++p) {
-        const bool live = dlive && p < nb;   // rows past the edges: computed, never stored
-        const int hrow = p * RPP + (dlive ? lrow : 0);
+        const bool live = dlive && p < nb;   // rows past the edges: computed on zeros, never stored
+        const int hrow = p * RPP + lrow;
         const float x = xs[p], dt = dts[p], dtx = dt * x;
         float hv[8];
         float y = 0.f;
+        const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
-            const float4 h4 = *reinterpret_cast<const float4 *>(hs + hrow * NP + n0 + HALF * q);
-            const float4 b4 = load4(bs + p * NP + n0 + HALF * q), c4 = load4(cs + p * NP + n0 + HALF * q);
+            // rows past the edges of a ragged block were not copied: they compute on zeros
+            const float4 h4 = live ? *reinterpret_cast<const float4 *>(hs + hrow * NP + n0 + HALF * q) : z4;
+            const float4 b4 = live ? load4(bs + p * NP + n0 + HALF * q) : z4;
+            const float4 c4 = live ? load4(cs + p * NP + n0 + HALF * q) : z4;
             const float hq[4] = {h4.x, h4.y, h4.z, h4.w}, bq[4] = {b4.x, b4.y, b4.z, b4.w}, cq[4] = {c4.x, c4.y, c4.z, c4.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                // rows past the edges read whatever the stage holds and are never stored
                 hv[4 * q + j] = fmaf(__expf(dt * av[4 * q + j]), hq[j], dtx * bq[j]);
                 y = fmaf(cq[j], hv[4 * q + j], y);
             }
         }
-        if (!live) y = 0.f;
         y = group_sum<LPR>(y);
         if (!live) continue;
         const size_t r = (size_t)(b0 + p) * D + d;
