@@ -303,18 +303,25 @@ def test_bf16_state_rejected_by_the_buffered_decode():
 
 @pytest.mark.parametrize("B,K", [(16, 128), (4, 128), (1, 128), (32, 64)])
 def test_chained_layers_wait_for_the_previous_layer_output(B, K):
-    """Two layers through gdn_decode_step_indexed_chained, the second taking the first one's output
-    as its v (a data dependence between layers): the second kernel may start early and load its
-    state, but must read v only after the first has finished. Repeated with fresh inputs; the
-    results must equal, bit for bit, the same two layers as ordinary launches, and match the
-    oracle. Covers 8, 4 and 2 rows per thread at K = 128 and whole tiles at K = 64."""
+    """Two layers, the second taking the first one's output as its v (a data dependence between
+    layers), in every order of ordinary and chained calls: a chained kernel may start early and
+    load its state, but must read v only after the kernel before it has finished; an ordinary one
+    (launched programmatically) waits before it touches memory. Repeated with fresh inputs; the
+    results must equal, bit for bit, the two layers as ordinary calls, and match the oracle. Covers
+    8, 4 and 2 rows per thread at K = 128 and whole tiles at K = 64."""
     H, HV, V = 4, 16, K
     G = HV // H
     num_slots = B + 2
     idx_np = syn.permutation(91, num_slots)[:B].copy()
     idx = torch.from_numpy(idx_np).cuda()
     results = {}
-    for chained in (False, True):
+    # (first layer chained, second layer chained): an ordinary call waits before it touches memory
+    # and only then lets the next kernel start, so every order must give the ordinary results. The
+    # pools are reused every iteration, so a chained first layer follows a plain torch kernel (which
+    # lets nothing start early): no run of chained calls then holds two calls on one pool.
+    orders = [(False, False), (True, True), (False, True), (True, False)]
+    fence = torch.zeros(1, device="cuda")
+    for order in orders:
         pools = [torch.from_numpy(host_state(num_slots, HV, V, K, 90 + l).astype(np.float32)).cuda()
                  for l in range(2)]
         outs = []
@@ -326,15 +333,18 @@ def test_chained_layers_wait_for_the_previous_layer_output(B, K):
             beta = torch.full((B, HV), 0.5, device="cuda")
             out0 = torch.empty((B, HV * V), device="cuda")
             out1 = torch.empty((B, HV * V), device="cuda")
+            if order[0]:
+                fence.add_(1.0)
             gdn.gdn_decode_step_indexed(q0, k0, v0, pools[0], out0, idx, H=H, g=g, beta=beta,
-                                        chained=chained)
+                                        chained=order[0])
             gdn.gdn_decode_step_indexed(q0, k0, out0, pools[1], out1, idx, H=H, g=g, beta=beta,
-                                        chained=chained)
+                                        chained=order[1])
             outs.append((out0, out1))
         torch.cuda.synchronize()
-        results[chained] = ([o.cpu().numpy() for pair in outs for o in pair], [p.cpu().numpy() for p in pools])
-    for a, b in zip(results[False][0] + results[False][1], results[True][0] + results[True][1]):
-        np.testing.assert_array_equal(a, b)
+        results[order] = ([o.cpu().numpy() for pair in outs for o in pair], [p.cpu().numpy() for p in pools])
+    for order in orders[1:]:
+        for a, b in zip(results[orders[0]][0] + results[orders[0]][1], results[order][0] + results[order][1]):
+            np.testing.assert_array_equal(a, b)
     # the last iteration against the oracle, from the layers' states before it
     S = [host_state(num_slots, HV, V, K, 90 + l) for l in range(2)]
     for it in range(6):
@@ -344,12 +354,12 @@ def test_chained_layers_wait_for_the_previous_layer_output(B, K):
         g = np.full((B, HV), np.float32(-0.1), dtype=np.float64)
         beta = np.full((B, HV), 0.5)
         o0, _ = oracle.delta_step(q0, k0, v0, g, beta, S[0], scale=K ** -0.5, idx=idx_np)
-        v1 = results[True][0][2 * it].reshape(B, HV, V).astype(np.float64)   # the GPU's layer-0 output
+        v1 = results[(True, True)][0][2 * it].reshape(B, HV, V).astype(np.float64)   # the GPU's layer-0 output
         o1, _ = oracle.delta_step(q0, k0, v1, g, beta, S[1], scale=K ** -0.5, idx=idx_np)
-        assert rel_err(results[True][0][2 * it].reshape(B, HV, V), o0) <= TOL_F32
-        assert rel_err(results[True][0][2 * it + 1].reshape(B, HV, V), o1) <= TOL_F32
+        assert rel_err(results[(True, True)][0][2 * it].reshape(B, HV, V), o0) <= TOL_F32
+        assert rel_err(results[(True, True)][0][2 * it + 1].reshape(B, HV, V), o1) <= TOL_F32
     for l in range(2):
-        assert rel_err(results[True][1][l], S[l]) <= TOL_F32
+        assert rel_err(results[(True, True)][1][l], S[l]) <= TOL_F32
 
 
 @pytest.mark.parametrize("B,H,HV,dtype,out_dtype,pad_rows,bad_rows,steps", [
