@@ -135,3 +135,11 @@ def test_gdn_gate_and_small_heads(D, kernel):
 def test_null_slot_rows_are_skipped(D, kernel):
     w = _run_fused(6, 4, D, seed=9, pad_rows=(0, 4), steps=2, kernel=kernel)
     assert w["out"] <= 2e-2 and w["state"] <= 1e-5, w
+
+
+@pytest.mark.parametrize("T", [20, 24])
+def test_kda_auto_choice_near_the_staged_threshold(T):
+    """Token counts just past the staged kernel's threshold (about twelve tiles per SM) under the
+    library's own choice, on sampled rows over two steps."""
+    w = _run_fused(T, 96, 128, seed=40 + T, sample_rows=[0, T // 2, T - 1], kernel="auto", steps=2)
+    assert w["out"] <= 2e-2 and w["state"] <= 1e-5, w

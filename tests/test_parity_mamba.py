@@ -91,6 +91,7 @@ def test_large_batch():
     (403, 1000, 32, "f32", "f32", True),     # ragged channel and row blocks (1000 / 64, 403 / 2); h_out
     (512, 1536, 16, "f32", "f32", False),    # 3072 blocks of 2 rows x 128 channels
     (514, 1000, 64, "f32", "f32", False),    # 4128 blocks of 4 rows x 32 channels, both edges ragged
+    (512, 1536, 64, "bf16", "f32", False),   # 6144 blocks of 4 rows x 32 channels, bf16 inputs
     (48, 1536, 64, "f32", "f32", False),     # 576 blocks: below the staged form, the grid-stride one
 ])
 def test_staged_and_grid_stride_forms(B, D, N, dtype, out_dtype, functional):
