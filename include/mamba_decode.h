@@ -52,10 +52,11 @@ typedef struct mamba_decode_args {
  * fp32 accumulation, fp32 state) and "Microbench" (the bytes-moved model). Returns GDN_OK,
  * GDN_ERR_NULL, GDN_ERR_SHAPE (N outside 1..128, negative sizes), GDN_ERR_DTYPE, GDN_ERR_ALIGN
  * (h, h_out and A must be 16-byte aligned when N is a multiple of 4) or GDN_ERR_LAUNCH. For
- * N = 16, 32, 64 or 128 and batches of at least two waves of its 32 KB blocks, the call runs a
- * kernel that bulk-copies blocks of state, B and C into shared memory (B and C must then be
- * 16-byte aligned, else another kernel runs); a bounded wait there reports GDN_DEVERR_TIMEOUT
- * through err_flags. Launches only; no allocation, no synchronisation.
+ * N = 16, 32, 64 or 128 and batches of at least two waves of its 16 KB blocks (two batch rows of a
+ * channel range; 32 KB, four rows, from six waves), the call runs a kernel that bulk-copies
+ * blocks of state, B and C into shared memory (B and C must then be 16-byte aligned, else another
+ * kernel runs); a bounded wait there reports GDN_DEVERR_TIMEOUT through err_flags. Launches only;
+ * no allocation, no synchronisation.
  */
 int mamba_selective_scan_decode(const mamba_decode_args *args, gdn_stream_t stream);
 
