@@ -923,7 +923,7 @@ def run_fused(args):
 
 
 def stack_decode(layers=48, B=256, H=16, HV=48, K=128, V=128, steps=1000, seed=2024, pairs=8,
-                 heads_per_pair=2, device=None, verbose=False, chained=True):
+                 heads_per_pair=2, device=None, verbose=False, chained=True, sample_clocks=False):
     """The stacked decode under CUDA graphs: `layers` independent state pools, one graph that
     draws fresh seeded inputs for every layer on the device (keyed by seed, layer and a device step
     counter), and one graph of `layers` decode calls, replayed `steps` times (chained: every layer
@@ -978,6 +978,11 @@ def stack_decode(layers=48, B=256, H=16, HV=48, K=128, V=128, steps=1000, seed=2
     torch.cuda.synchronize(dev)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = None
+    if sample_clocks:   # SM clocks and throttle reasons during the timed steps
+        sampler = ClockSampler(dev.index)
+        sampler.start()
+    t_start = time.time()
     with torch.cuda.stream(s):
         w0.record(s)
         for i in range(steps):
@@ -987,6 +992,10 @@ def stack_decode(layers=48, B=256, H=16, HV=48, K=128, V=128, steps=1000, seed=2
             ev[i][1].record(s)
         w1.record(s)
     torch.cuda.synchronize(dev)
+    clocks = None
+    if sampler is not None:
+        sampler.mark(t_start, time.time())
+        clocks = sampler.stop()
     dec_ms = [a.elapsed_time(b) for a, b in ev]
     total_ms = w0.elapsed_time(w1)
 
@@ -1021,7 +1030,7 @@ def stack_decode(layers=48, B=256, H=16, HV=48, K=128, V=128, steps=1000, seed=2
             print(f"pair layer={l} slot={slot} heads={h0}..{h0 + heads_per_pair - 1}: drift so far {drift:.3g}")
     return {"dec_ms_per_step": statistics.mean(dec_ms), "dec_ms_median": statistics.median(dec_ms),
             "total_ms_per_step": total_ms / steps, "drift": drift, "last_out_err": out_err,
-            "picks": picks, "state_bytes_per_step": 2 * layers * B * HV * V * K * 4}
+            "picks": picks, "state_bytes_per_step": 2 * layers * B * HV * V * K * 4, "clocks": clocks}
 
 
 def run_stack(args):
@@ -1031,7 +1040,7 @@ def run_stack(args):
     layers, B, H, HV, K, V = args.layers, args.B, 16, 48, 128, 128
     steps = args.steps
     res = stack_decode(layers, B, H, HV, K, V, steps=steps, device=h.dev, pairs=args.pairs,
-                       chained=not args.no_chain)
+                       chained=not args.no_chain, sample_clocks=True)
     ms = res["dec_ms_median"]
     (ms,) = max_over_ranks([ms], h.world)
     if h.rank != 0:
@@ -1046,6 +1055,7 @@ def run_stack(args):
                                      "state_bytes_per_step": state_bytes,
                                      "chained_layers": not args.no_chain}, steps * layers)
     line["per_layer_us"] = round(ms * 1e3 / layers, 3)
+    line["clocks"] = res["clocks"]
     line["with_input_generation_ms_per_step"] = round(res["total_ms_per_step"], 4)
     line["drift_vs_oracle"] = {"max_rel_state_err": res["drift"], "last_step_out_err": res["last_out_err"],
                                "pairs": [list(p) for p in res["picks"]], "steps": steps,
